@@ -1,0 +1,295 @@
+"""Pins for the oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when it disagrees with
+a fact that does not come from the oracle itself: a library softmax-attention routine
+(PyTorch's scaled_dot_product_attention in float64), a closed form, a figure printed on the
+pages (``golden/pages_figures.json``, each with its citation), or brute force on tiny
+inputs. The pins run against the committed oracle in ``test_oracle_pins.py`` and against
+deliberately broken copies of it in ``test_oracle_mutations.py``.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import synth
+
+CONTIGUOUS, ZIGZAG, STRIPED = 0, 1, 2
+FULL, DIAG, SKIP = 0, 1, 2
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_figures.json")))
+
+
+def _qkv(seed, B, T, h, n_kv, d, k_mult=1.0):
+    q = synth.normal_bf16(seed, synth.TAG_Q, (B, T, h, d))
+    k = synth.normal_bf16(seed, synth.TAG_K, (B, T, n_kv, d), mult=k_mult)
+    v = synth.normal_bf16(seed, synth.TAG_V, (B, T, n_kv, d))
+    return q, k, v
+
+
+def _f64(bits):
+    return torch.from_numpy(synth.bf16_bits_to_f32(bits).astype(np.float64))
+
+
+def _sdpa(q, k, v, causal, scale=None, mask=None):
+    """Library reference: torch SDPA in float64 on [B,T,h,d] inputs, K/V heads repeat-interleaved."""
+    Q, K, V = (_f64(x).permute(0, 2, 1, 3) for x in (q, k, v))
+    g = Q.shape[1] // K.shape[1]
+    K = K.repeat_interleave(g, dim=1)
+    V = V.repeat_interleave(g, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, is_causal=causal and mask is None,
+                                                           scale=scale)
+    return out.permute(0, 2, 1, 3).numpy()
+
+
+def _maxabs(a, b):
+    return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+
+
+# --------------------------------------------------------------------------------------
+# The attention definition against a library routine
+# --------------------------------------------------------------------------------------
+
+def pin_sdpa_mha(orc):
+    q, k, v = _qkv(11, 2, 37, 3, 3, 16)
+    for causal in (True, False):
+        o, _ = orc.attention(q, k, v, causal=causal)
+        assert _maxabs(o, _sdpa(q, k, v, causal)) < 1e-12, "MHA output differs from SDPA"
+    o, _ = orc.attention(q, k, v, causal=True, scale=0.37)
+    assert _maxabs(o, _sdpa(q, k, v, True, scale=0.37)) < 1e-12, "explicit scale not honoured"
+
+
+def pin_sdpa_gqa(orc):
+    q, k, v = _qkv(12, 1, 29, 6, 2, 16)
+    for causal in (True, False):
+        o, _ = orc.attention(q, k, v, causal=causal)
+        assert _maxabs(o, _sdpa(q, k, v, causal)) < 1e-12, "GQA head map differs from repeat-interleave"
+
+
+def pin_pos_mask(orc):
+    """Position ids decide the causal mask: key u visible to query t iff pos[u] <= pos[t]."""
+    q, k, v = _qkv(13, 1, 24, 2, 1, 16)
+    rng = np.random.default_rng(5)
+    for pos in (rng.permutation(24).astype(np.int32), rng.integers(0, 6, 24).astype(np.int32)):
+        o, _ = orc.attention(q, k, v, causal=True, pos=pos)
+        mask = torch.from_numpy(pos[None, :] <= pos[:, None])          # [t, u]
+        assert _maxabs(o, _sdpa(q, k, v, False, mask=mask)) < 1e-12, "position-id mask wrong"
+
+
+def pin_rows_and_keys(orc):
+    q, k, v = _qkv(14, 1, 40, 2, 2, 16)
+    full_o, full_l = orc.attention(q, k, v, causal=True)
+    rows = np.array([39, 0, 17, 5])
+    o, l = orc.attention(q, k, v, causal=True, rows=rows)
+    assert _maxabs(o, full_o[:, rows]) == 0.0 and _maxabs(l, full_l[:, :, rows]) == 0.0, "row subset"
+    keys = np.array([3, 9, 10, 11, 30, 31, 38])
+    o, _ = orc.attention(q, k, v, causal=False, keys=keys)
+    ref = _sdpa(q, k[:, keys], v[:, keys], False)
+    assert _maxabs(o, ref) < 1e-12, "key subset differs from SDPA on the subset"
+
+
+# --------------------------------------------------------------------------------------
+# Closed forms
+# --------------------------------------------------------------------------------------
+
+def pin_uniform_scores(orc):
+    """Q = 0 gives equal scores: O[t] = mean of the visible V, lse = ln |V(t)|."""
+    B, T, h, d = 1, 33, 2, 16
+    _, k, v = _qkv(15, B, T, h, h, d)
+    q = np.zeros((B, T, h, d), dtype=np.uint16)
+    vf = synth.bf16_bits_to_f32(v).astype(np.float64)
+    o, l = orc.attention(q, k, v, causal=True)
+    cmean = np.cumsum(vf, axis=1) / np.arange(1, T + 1)[None, :, None, None]
+    assert _maxabs(o, cmean) < 1e-12, "causal uniform-score mean"
+    assert _maxabs(l[0, 0], np.log(np.arange(1, T + 1))) < 1e-12, "causal lse = ln(t+1)"
+    o, l = orc.attention(q, k, v, causal=False)
+    assert _maxabs(o, np.broadcast_to(vf.mean(axis=1, keepdims=True), o.shape)) < 1e-12, "non-causal mean"
+    assert _maxabs(l, np.full(l.shape, math.log(T))) < 1e-12, "non-causal lse = ln T"
+
+
+def pin_single_key(orc):
+    """Causal token 0 sees only key 0: O = V[0], lse = scale * <q_0, k_0>."""
+    q, k, v = _qkv(16, 1, 8, 2, 1, 32)
+    o, l = orc.attention(q, k, v, causal=True)
+    qf, kf, vf = (synth.bf16_bits_to_f32(x).astype(np.float64) for x in (q, k, v))
+    scale = 1.0 / math.sqrt(32)
+    for i in range(2):
+        assert _maxabs(o[0, 0, i], vf[0, 0, 0]) < 1e-15, "O at t=0"
+        assert abs(l[0, i, 0] - scale * float(qf[0, 0, i] @ kf[0, 0, 0])) < 1e-12, "lse at t=0"
+
+
+# --------------------------------------------------------------------------------------
+# The ring and the merge against the definition
+# --------------------------------------------------------------------------------------
+
+def pin_ring_equals_definition(orc):
+    """The pages: blockwise online softmax around the ring is exact."""
+    for layout in (CONTIGUOUS, ZIGZAG, STRIPED):
+        for n_cp in (1, 2, 4):
+            for causal in (True, False):
+                q, k, v = _qkv(17 + n_cp, 1, 32, 4, 2, 16, k_mult=2.0)
+                ref_o, ref_l = orc.attention(q, k, v, causal=causal)
+                for block in (1, 3, 16):
+                    o, l = orc.ring(q, k, v, n_cp, layout, causal=causal, block=block)
+                    assert _maxabs(o, ref_o) < 1e-12 and _maxabs(l, ref_l) < 1e-12, \
+                        f"ring != definition (layout {layout}, n_cp {n_cp}, causal {causal}, block {block})"
+
+
+def pin_merge_partition(orc):
+    """Merging partials over a partition of the keys gives the full result; empty parts are identities."""
+    q, k, v = _qkv(21, 1, 30, 2, 2, 16)
+    T = 30
+    full_o, full_l = orc.attention(q, k, v, causal=True)
+    rng = np.random.default_rng(3)
+    label = rng.integers(0, 4, T)
+    label[:3] = 0                                       # part 3 may be empty for early rows
+    parts_o, parts_l = [], []
+    for s in range(5):                                  # part 4 is empty for every row
+        keys = np.nonzero(label == s)[0]
+        if keys.size:
+            o, l = orc.attention(q, k, v, causal=True, keys=keys)
+        else:
+            o = np.zeros_like(full_o)
+            l = np.full_like(full_l, -np.inf)
+        parts_o.append(o[0])
+        parts_l.append(l[0])
+    mo, ml = orc.merge(np.stack(parts_o), np.stack(parts_l))
+    assert _maxabs(mo, full_o[0]) < 1e-12 and _maxabs(ml, full_l[0]) < 1e-12, "merge of a partition"
+    so, sl = orc.merge(np.stack(parts_o[:1]), np.stack(parts_l[:1]))
+    assert _maxabs(so, parts_o[0]) < 1e-15 and _maxabs(sl[np.isfinite(sl)], parts_l[0][np.isfinite(sl)]) < 1e-15
+    eo, el = orc.merge(np.zeros((2, 3, 1, 4)), np.full((2, 1, 3), -np.inf))
+    assert np.all(eo == 0) and np.all(el == -np.inf), "all-empty merge"
+    # equal lse: plain average, lse + ln 2
+    a = np.ones((1, 1, 1, 4)); b = 3 * np.ones((1, 1, 1, 4))
+    mo, ml = orc.merge(np.concatenate([a, b]), np.array([[[0.5]], [[0.5]]]))
+    assert _maxabs(mo, 2 * np.ones((1, 1, 4))) < 1e-15 and abs(ml[0, 0] - (0.5 + math.log(2))) < 1e-15
+
+
+# --------------------------------------------------------------------------------------
+# Placement, block classes, work and bytes
+# --------------------------------------------------------------------------------------
+
+def pin_layout_examples(orc):
+    """T = 16 over 4 ranks, written out by hand from the pages' descriptions."""
+    assert orc.layout_map(16, 4, CONTIGUOUS)[1].tolist() == [4, 5, 6, 7]
+    assert orc.layout_map(16, 4, ZIGZAG)[1].tolist() == [2, 3, 12, 13]     # chunks 1 and 6 of 8
+    assert orc.layout_map(16, 4, STRIPED)[1].tolist() == [1, 5, 9, 13]
+    z0 = orc.layout_map(16, 4, ZIGZAG)[0].tolist()
+    assert z0[:2] == [0, 1] and z0[2:] == [14, 15], "GPU 0 gets the first chunk and the last"
+    assert orc.chunk_assignment(4, ZIGZAG, 1) == [1, 6]
+    assert orc.chunk_assignment(4, CONTIGUOUS, 2) == [2]
+    for layout in (CONTIGUOUS, ZIGZAG, STRIPED):
+        for T, n_cp in ((16, 4), (48, 3), (64, 8), (10, 1)):
+            m = orc.layout_map(T, n_cp, layout)
+            assert sorted(m.ravel().tolist()) == list(range(T)), "layout is a bijection"
+            assert all(orc.token_of(T, n_cp, layout, r, j) == m[r, j] for r in range(n_cp) for j in range(T // n_cp))
+
+
+def pin_classify_small(orc):
+    assert orc.classify([5, 6], [1, 2]) == FULL
+    assert orc.classify([5, 6], [1, 5]) == FULL
+    assert orc.classify([5, 6], [7, 8]) == SKIP
+    assert orc.classify([5, 6], [5, 7]) == DIAG
+    assert orc.classify([5, 6], [6, 7]) == DIAG
+    assert orc.classify([5, 6], [7, 8], causal=False) == FULL
+
+
+def pin_half_units(orc):
+    """Contiguous causal: rank r does 2r+1 half blocks, so the last does 2n_cp-1 times the first;
+    zigzag: every rank does the same (4 n_cp half chunks)."""
+    fig = GOLDEN["causal_imbalance"]
+    assert fig["printed_ratio_formula"] == "2*n_cp - 1" and fig["zigzag_equal"]
+    for n_cp in (1, 2, 4, 8, 16):
+        c = orc.half_units(n_cp * 8, n_cp, CONTIGUOUS)
+        assert c.tolist() == [2 * r + 1 for r in range(n_cp)]
+        assert c[-1] == (2 * n_cp - 1) * c[0]
+        z = orc.half_units(n_cp * 8, n_cp, ZIGZAG)
+        assert z.tolist() == [4 * n_cp] * n_cp
+        s = orc.half_units(n_cp * 8, n_cp, STRIPED)
+        assert len(set(s.tolist())) == 1
+    assert orc.half_units(64, 4, CONTIGUOUS, causal=False).tolist() == [8] * 4
+
+
+def pin_pairs_closed_forms(orc):
+    T, n_cp = 512, 4
+    n, m = T // n_cp, T // (2 * n_cp)
+    c = orc.plan_counts(T, n_cp, CONTIGUOUS)["pairs"].tolist()
+    assert c == [8256, 24640, 41024, 57408]                     # n^2 r + n(n+1)/2 at n = 128
+    assert c == [n * n * r + n * (n + 1) // 2 for r in range(n_cp)]
+    z = orc.plan_counts(T, n_cp, ZIGZAG)["pairs"].tolist()
+    assert z == [m * (T + 1)] * n_cp
+    s = orc.plan_counts(T, n_cp, STRIPED)["pairs"].tolist()
+    assert s == [n_cp * n * (n - 1) // 2 + n * (r + 1) for r in range(n_cp)]
+    for counts in (c, z, s):
+        assert sum(counts) == T * (T + 1) // 2
+    nc = orc.plan_counts(T, n_cp, ZIGZAG, causal=False)["pairs"].tolist()
+    assert nc == [n * T] * n_cp
+
+
+def pin_step_classes(orc):
+    """Block classes per (rank, ring step) at block granularity. At step s rank r holds the block
+    of (r - s) mod n_cp: its left neighbour's block arrives each step."""
+    T, n_cp = 64, 4
+    n, m = T // n_cp, T // (2 * n_cp)
+    pc = orc.plan_counts(T, n_cp, CONTIGUOUS, bq=n, bk=n)
+    for r in range(n_cp):
+        for s in range(n_cp):
+            want = DIAG if s == 0 else (FULL if s <= r else SKIP)
+            got = [pc["full"][r, s], pc["diag"][r, s], pc["skip"][r, s]]
+            assert got == [int(want == FULL), int(want == DIAG), int(want == SKIP)], f"contiguous r{r} s{s}"
+    pz = orc.plan_counts(T, n_cp, ZIGZAG, bq=m, bk=m)
+    for r in range(n_cp):
+        assert [pz["full"][r, 0], pz["diag"][r, 0], pz["skip"][r, 0]] == [1, 2, 1], "zigzag own step"
+        for s in range(1, n_cp):
+            assert [pz["full"][r, s], pz["diag"][r, s], pz["skip"][r, s]] == [2, 0, 2], "zigzag foreign step"
+    ps = orc.plan_counts(T, n_cp, STRIPED, bq=n, bk=n)
+    assert np.all(ps["diag"] == 1), "striped blocks are all partly visible"
+    tiles = orc.plan_counts(T, n_cp, CONTIGUOUS, bq=5, bk=7)
+    nt = (-(-n // 5)) * (-(-n // 7))
+    assert np.all(tiles["full"] + tiles["diag"] + tiles["skip"] == nt), "ragged tiles cover the block"
+
+
+def pin_bytes_pages(orc):
+    fig = GOLDEN["ring_kv_bytes_405b"]
+    T, n_cp, d_k, n_kv, h = fig["T"], fig["n_cp"], fig["d_k"], fig["n_kv_per_gpu"], fig["h_per_gpu"]
+    n = T // n_cp
+    b = orc.kv_bytes_recv(1, n, n_kv, d_k, n_cp)
+    assert b == 4 * n * n_kv * d_k * (n_cp - 1) == 62_914_560
+    assert round(b / 1e6) == fig["printed_megabytes"]
+    assert round(b / 50e9 * 1e3, 1) == fig["printed_ms"]                 # InfiniBand, 50 GB/s (reading)
+    no_gqa = orc.kv_bytes_recv(1, n, h, d_k, n_cp)
+    assert no_gqa == fig["printed_without_gqa_factor"] * b
+    assert round(no_gqa / 50e9 * 1e3) == fig["printed_without_gqa_ms"]
+    assert orc.kv_bytes_recv(3, n, n_kv, d_k, n_cp) == 3 * b
+    for method in (0, 1):
+        assert orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, n_cp, method) == b, "ring == all-gather bytes"
+
+
+def pin_overlap_pages(orc):
+    fig = GOLDEN["overlap_bar_tokens"]
+    F = 989e12                                  # H100 dense bf16 (reading; the page gives none)
+    nvl = orc.overlap_min_tokens(F, 450e9, 1, 1)
+    ib = orc.overlap_min_tokens(F, 50e9, 1, 1)
+    assert abs(nvl - fig["printed_nvlink_tokens"]) / fig["printed_nvlink_tokens"] < 0.01
+    assert abs(ib - fig["printed_ib_tokens"]) / fig["printed_ib_tokens"] < 0.02
+    gqa = orc.overlap_min_tokens(F, 450e9, 64, 8)
+    assert abs(nvl / gqa - fig["printed_gqa_factor"]) < 1e-12
+    assert fig["printed_tokens_per_gpu_128k_cp16"] > nvl and fig["printed_tokens_per_gpu_128k_cp16"] > ib / 8
+
+
+def pin_ulysses(orc):
+    fig = GOLDEN["ulysses_breakeven"]
+    assert orc.ulysses_breakeven(16, 16) == fig["printed_mha_group_larger_than"]
+    assert orc.ulysses_breakeven(64, 8) == fig["printed_gqa8_group_larger_than"]
+    T, d_k, h, n_kv = 4096, 128, 64, 8
+    n_eq = orc.ulysses_breakeven(h, n_kv)
+    ring = orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, n_eq, 0)
+    uly = orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, n_eq, 2)
+    assert abs(ring - uly) / ring < 1e-12
+    assert orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 2) < orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 0)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
