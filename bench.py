@@ -1,0 +1,413 @@
+#!/usr/bin/env python3
+"""Benchmark of the context-parallel ring-attention forward on GB300.
+
+One step = one pass of the whole path over the 128K-token Llama-3-70B-shaped causal GQA workload
+(B=1, T=131072, h=64, n_kv=8, d_k=128, n_cp=16, zigzag): token placement (gather of Q, K, V and
+position ids), every virtual rank over every ring step with block skipping and the online
+softmax, and the write-back of O and lse in natural order. Inputs stay resident in HBM; they
+are 2.7 GB, larger than L2, so no flush is needed between steps.
+
+Prints one JSON line. ``--impl reference`` times the fp64 CPU oracle instead (the reference
+arm of this benchmark), on a bounded sample of rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "ring-attn fwd effective TFLOP/s on 1 GB300; % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "llama70b_zigzag_T128k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops_eff(w) -> float:
+    """4*B*h*d per visible pair; causal pairs counted as T^2/2 (a diagonal block as half)."""
+    pairs = w.T * w.T / 2 if w.causal else float(w.T) * w.T
+    return 4.0 * w.B * w.h * w.d * pairs
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# Reference arm and CPU baseline: the fp64 oracle on sampled rows
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample_rate(w, q, k, v, n_rows: int, seed: int):
+    """Time the oracle on n_rows sampled query rows (all heads, whole batch); returns
+    (effective TFLOP/s, seconds, sample description). Work counted as 4*d per visible pair."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.T, size=n_rows, replace=False)).astype(np.int64)
+    pairs = float(np.sum(rows + 1)) if w.causal else float(n_rows) * w.T
+    t0 = time.perf_counter()
+    oracle.get().attention(q, k, v, causal=w.causal, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.d * w.h * w.B * pairs
+    return flops / dt / 1e12, dt, f"{n_rows} uniformly drawn query rows x {w.h} heads x B={w.B} (seed {seed})"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    q, k, v = synth.make_qkv(w)
+    import oracle
+    oracle.build()
+    rows_per_step = args.ref_rows
+    for i in range(args.warmup):
+        oracle_sample_rate(w, q, k, v, rows_per_step, seed=1000 + i)
+    rates, times = [], []
+    for i in range(args.steps):
+        r, dt, desc = oracle_sample_rate(w, q, k, v, rows_per_step, seed=2000 + i)
+        rates.append(r)
+        times.append(dt)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": f"per step: {rows_per_step} query rows x {w.h} heads of the workload"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, args):
+    return {"workload": w.name, "B": w.B, "T": w.T, "h": w.h, "n_kv": w.n_kv, "d_k": w.d, "n_cp": w.n_cp,
+            "layout": synth.LAYOUT_NAMES[args.layout], "causal": w.causal, "path": args.path,
+            "l2": "inputs larger than L2 (no flush)" if w.T >= 65536 else "L2 flushed between steps",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+# ---------------------------------------------------------------------------------------------
+# The GPU arm
+# ---------------------------------------------------------------------------------------------
+
+def run_gpu(args, w):
+    import torch
+    import context_ring_attention_blockwise_gb300 as cp
+    from context_ring_attention_blockwise_gb300 import _build
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    _build.build()
+    dev = torch.device("cuda", local)
+
+    q_h, k_h, v_h = synth.make_qkv(w)
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = to_dev(q_h), to_dev(k_h), to_dev(v_h)
+    plan = cp.Plan(w.T, w.h, w.n_kv, w.d, w.n_cp, args.layout, w.causal)
+    ring = args.path == "ring"
+    ws = cp.alloc_workspace(plan.ring_workspace_size(w.B) if ring else plan.workspace_size(w.B), dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    flush = None
+    if w.T < 65536:   # inputs below L2 size: flush between steps
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if flush is not None:
+            flush.zero_()
+        if evs:
+            evs[0].record(stream)
+        if ring:
+            cp.ring_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream, copy_stream=copy)
+        else:
+            cp.permute(q, k, v, plan, ws, stream=stream)
+            if evs:
+                evs[1].record(stream)
+            cp.attend(plan, w.B, ws, o, lse, stream=stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    cp.check(plan, ws)
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops_eff(w) * world / (ms_per_step * 1e-3) / 1e12
+    if ring:
+        attn_ms = None
+        perm_ms = None
+    else:
+        perm_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+        attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+
+    # e2e through the public API with host buffers: H2D of the inputs from pinned memory and D2H
+    # of O and lse into pinned memory, every step, inside the timed region.
+    qp = torch.from_numpy(q_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    kp = torch.from_numpy(k_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    vp = torch.from_numpy(v_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    op = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lp = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        if ring:
+            cp.ring_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream, copy_stream=copy)
+        else:
+            cp.forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = q_h.nbytes + k_h.nbytes + v_h.nbytes
+    d2h = op.numel() * 2 + lp.numel() * 4
+
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    result = None
+    if rank == 0:
+        kernel_ms = attn_ms if attn_ms is not None else ms_per_step
+        achieved = flops_eff(w) / (kernel_ms * 1e-3) / 1e12
+        launches_per_step = (3 if not ring else 1 + 1 + w.n_cp + 1)
+        result = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, args),
+            "frac_of_peak": value / world / peak_tf,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tf, "traffic": args.traffic,
+                         "kernel": "ring_attention_kernel<128>" if not ring else "whole ring-step path",
+                         "peak_kind": f"bf16 dense, sustained, {peak_src}",
+                         "peak_burst": float(peaks.get("bf16_tflops", 0.0))},
+            "kernels_ms": {"permute_and_placement": perm_ms, "attention": attn_ms},
+            "e2e": {"value": flops_eff(w) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+    del qp, kp, vp, op, lp
+    if rank == 0 and args.extras and not ring:
+        result["extras"] = extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks)
+    if rank == 0 and args.cpu_baseline:
+        rate, dt, desc = oracle_sample_rate(w, q_h, k_h, v_h, args.cpu_rows, seed=7)
+        result["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                                  "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
+    """Secondary measurements: the ring-step path at the same workload, and the HBM-bound
+    kernels (placement, merge) against the measured copy bandwidth."""
+    import torch
+    out = {}
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # placement: reads and writes Q, K, V once
+    moved = 2 * (q.numel() + k.numel() + v.numel()) * 2
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        cp.permute(q, k, v, plan, ws, stream=stream)
+    a.record(stream)
+    for _ in range(5):
+        cp.permute(q, k, v, plan, ws, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / 5
+    out["placement"] = {"ms": ms, "gbs": moved / ms / 1e6, "frac_of_hbm": moved / ms / 1e6 / hbm}
+    # standalone merge of two fp32 partials at the workload's (T, h, d)
+    rows = w.B * w.T
+    S = 2
+    op = torch.randn((S, rows, w.h, w.d), dtype=torch.float32, device=dev)
+    lp = torch.randn((S, w.h, rows), dtype=torch.float32, device=dev)
+    mo = torch.empty((rows, w.h, w.d), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((w.h, rows), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        cp.merge(op, lp, mo, ml, stream=stream)
+    a.record(stream)
+    for _ in range(5):
+        cp.merge(op, lp, mo, ml, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / 5
+    mb = op.numel() * 4 + lp.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
+    out["merge_S2"] = {"ms": ms, "gbs": mb / ms / 1e6, "frac_of_hbm": mb / ms / 1e6 / hbm}
+    del op, lp, mo, ml
+    # the ring-faithful path: permute, n_cp steps with block hops on a copy stream, finalize
+    wsr = cp.alloc_workspace(plan.ring_workspace_size(w.B), dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
+    cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(2):
+        cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsr)
+    ms = a.elapsed_time(b) / 2
+    out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12}
+    del wsr
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.CONFIGS))
+    ap.add_argument("--layout", default=None, help="contiguous|zigzag|striped (default: the workload's first)")
+    ap.add_argument("--path", choices=["fused", "ring"], default="fused")
+    ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per attention launch from ncu, if known")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--cpu-rows", type=int, default=96, help="query rows the CPU baseline computes")
+    ap.add_argument("--ref-rows", type=int, default=8, help="query rows per step of the reference arm")
+    args = ap.parse_args()
+    w = synth.workload(args.workload)
+    args.layout = w.layouts[0] if args.layout is None else synth.LAYOUT_IDS[args.layout]
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

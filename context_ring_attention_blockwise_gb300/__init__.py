@@ -1,0 +1,275 @@
+"""GB300-native (sm_103a) context-parallel ring-attention forward.
+
+A thin Python binding over the C ABI of ``libcpattn.so`` (declared in ``include/cpattn.h``):
+argument marshalling only. Every step of the path (token placement, ring steps with block
+skipping, online softmax, merge, write-back) runs in the library's CUDA kernels. PyTorch is
+used for device memory and streams. There is no CPU fallback: if the library is not built, or
+a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+CONTIGUOUS, ZIGZAG, STRIPED = 0, 1, 2
+LAYOUTS = {"contiguous": CONTIGUOUS, "zigzag": ZIGZAG, "striped": STRIPED}
+FULL, DIAG, SKIP = 0, 1, 2
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_lib = None
+
+SYMBOLS = [
+    "cpattn_plan", "cpattn_plan_destroy", "cpattn_workspace_size", "cpattn_ring_workspace_size", "cpattn_forward",
+    "cpattn_attend",
+    "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
+    "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
+]
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where} failed with status {status}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libcpattn.so (built in-tree by ``_build.build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libcpattn.so is not built ({_build.LIB}); run context_ring_attention_blockwise_gb300."
+                           "_build.build() or __graft_entry__.build() first")
+    L = ctypes.CDLL(_build.LIB)
+    i, u64 = ctypes.c_int, ctypes.c_uint64
+    sz = ctypes.POINTER(ctypes.c_size_t)
+    L.cpattn_plan.argtypes = [_I64, i, i, i, i, i, i, ctypes.POINTER(_P)]
+    L.cpattn_plan_destroy.argtypes = [_P]
+    L.cpattn_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_ring_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_forward.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_permute.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_ring_step.argtypes = [_P, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, _P]
+    L.cpattn_finalize.argtypes = [_P, i, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_merge.argtypes = [i, _I64, i, i, _P, _P, _P, _P, _P]
+    L.cpattn_plan_counts.argtypes = [_P, i, _P, _P, _P, _P, _P, _P]
+    L.cpattn_tile_shape.argtypes = [_P, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.cpattn_tile_counts.argtypes = [_P, i, _P, _P, _P]
+    L.cpattn_check.argtypes = [_P, _P]
+    L.cpattn_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, u64, _P]
+    L.cpattn_last_error.restype = ctypes.c_char_p
+    L.cpattn_last_error.argtypes = []
+    L.cpattn_version.restype = ctypes.c_char_p
+    L.cpattn_version.argtypes = []
+    for name in SYMBOLS:
+        if name not in ("cpattn_last_error", "cpattn_version"):
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise CpattnError(status, where, lib().cpattn_last_error().decode())
+
+
+def _layout_id(layout) -> int:
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+class Plan:
+    """Host-side plan for (T, h, n_kv, d_k, n_cp, layout, causal)."""
+
+    def __init__(self, T: int, h: int, n_kv: int, d_k: int, n_cp: int, layout, causal: bool = True):
+        self.T, self.h, self.n_kv, self.d, self.n_cp = int(T), int(h), int(n_kv), int(d_k), int(n_cp)
+        self.layout, self.causal = _layout_id(layout), bool(causal)
+        self._h = _P()
+        _check(lib().cpattn_plan(self.T, self.h, self.n_kv, self.d, self.n_cp, self.layout, int(self.causal),
+                                 ctypes.byref(self._h)), "cpattn_plan")
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            lib().cpattn_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_workspace_size")
+        return out.value
+
+    def ring_workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_ring_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_ring_workspace_size")
+        return out.value
+
+    def tile_shape(self):
+        bq, bk = ctypes.c_int(), ctypes.c_int()
+        _check(lib().cpattn_tile_shape(self._h, ctypes.byref(bq), ctypes.byref(bk)), "cpattn_tile_shape")
+        return bq.value, bk.value
+
+    def counts(self, B: int = 1):
+        import numpy as np
+        n = self.n_cp
+        full = np.zeros((n, n), dtype=np.int64)
+        diag, skip = np.zeros_like(full), np.zeros_like(full)
+        pairs, kvb, half = (np.zeros(n, dtype=np.int64) for _ in range(3))
+        _check(lib().cpattn_plan_counts(self._h, B, full.ctypes.data, diag.ctypes.data, skip.ctypes.data,
+                                        pairs.ctypes.data, kvb.ctypes.data, half.ctypes.data), "cpattn_plan_counts")
+        return {"full": full, "diag": diag, "skip": skip, "pairs": pairs, "kv_bytes_recv": kvb, "half_units": half}
+
+
+# ---- device calls (torch tensors for memory and streams) ------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev_ptr(t, name):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _P(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return _P(s.cuda_stream)
+
+
+def alloc_workspace(nbytes: int, device=None):
+    """A caller-owned workspace: 1024-byte aligned bytes from the torch caching allocator."""
+    torch = _torch()
+    buf = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device or "cuda")
+    off = (-buf.data_ptr()) % 1024
+    return buf[off:off + nbytes]
+
+
+def _check_inputs(plan: Plan, q, k, v):
+    torch = _torch()
+    B, T, h, d = q.shape
+    if (T, h, d) != (plan.T, plan.h, plan.d) or tuple(k.shape) != (B, T, plan.n_kv, d) or k.shape != v.shape:
+        raise ValueError("q/k/v shapes do not match the plan")
+    for x, nm in ((q, "q"), (k, "k"), (v, "v")):
+        if x.dtype != torch.bfloat16:
+            raise ValueError(f"{nm} must be bfloat16")
+    return B
+
+
+def forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, out=None, lse=None, stream=None):
+    """cpattn_forward: q [B,T,h,d], k/v [B,T,n_kv,d] bf16 CUDA tensors (natural order).
+    Returns (o [B,T,h,d] bf16, lse [B,h,T] fp32)."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if ws is None:
+        ws = alloc_workspace(plan.workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    _check(lib().cpattn_forward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
+                                _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_forward")
+    return out, lse
+
+
+def permute(q, k, v, plan: Plan, ws, pos=None, stream=None):
+    B = _check_inputs(plan, q, k, v)
+    _check(lib().cpattn_permute(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                _dev_ptr(pos, "pos"), _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+           "cpattn_permute")
+
+
+def attend(plan: Plan, B: int, ws, out, lse, scale: float | None = None, stream=None):
+    """cpattn_attend: the attention over a workspace that ``permute`` filled."""
+    _check(lib().cpattn_attend(plan.handle, B, float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
+                               _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_attend")
+
+
+def ring_step(plan: Plan, B: int, step: int, ws, scale: float | None = None, compute=None, copy=None):
+    _check(lib().cpattn_ring_step(plan.handle, B, step, float(scale or 0.0), _dev_ptr(ws, "ws"), ws.numel(),
+                                  _stream_ptr(compute), _stream_ptr(copy)), "cpattn_ring_step")
+
+
+def finalize(plan: Plan, B: int, ws, out, lse, stream=None):
+    _check(lib().cpattn_finalize(plan.handle, B, _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"),
+                                 ws.numel(), _stream_ptr(stream)), "cpattn_finalize")
+
+
+def ring_forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, out=None, lse=None,
+                 stream=None, copy_stream=None):
+    """The ring-faithful path: permute, n_cp ring steps (block hops on a copy stream), finalize."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if ws is None:
+        ws = alloc_workspace(plan.ring_workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    compute = stream if stream is not None else torch.cuda.current_stream()
+    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device)
+    permute(q, k, v, plan, ws, pos=pos, stream=compute)
+    for s in range(plan.n_cp):
+        ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
+    finalize(plan, B, ws, out, lse, stream=compute)
+    return out, lse
+
+
+def merge(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """cpattn_merge: o_parts [S,rows,h,d] fp32, lse_parts [S,h,rows] fp32 -> (o bf16 [rows,h,d], lse [h,rows])."""
+    torch = _torch()
+    S, rows, h, d = o_parts.shape
+    if out is None:
+        out = torch.empty((rows, h, d), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((h, rows), dtype=torch.float32, device=o_parts.device)
+    _check(lib().cpattn_merge(S, rows, h, d, _dev_ptr(o_parts, "o_parts"), _dev_ptr(lse_parts, "lse_parts"),
+                              _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _stream_ptr(stream)), "cpattn_merge")
+    return out, lse
+
+
+def tile_counts(plan: Plan, B: int, ws):
+    """Tiles the kernels computed (all batch elements and heads), by (rank, step): (full, diag)."""
+    import numpy as np
+    full = np.zeros((plan.n_cp, plan.n_cp), dtype=np.int64)
+    diag = np.zeros_like(full)
+    _check(lib().cpattn_tile_counts(plan.handle, B, _dev_ptr(ws, "ws"), full.ctypes.data, diag.ctypes.data),
+           "cpattn_tile_counts")
+    return full, diag
+
+
+def check(plan: Plan | None, ws):
+    """Raise CpattnError if a device-side wait of the kernels that used ``ws`` timed out."""
+    _check(lib().cpattn_check(plan.handle if plan is not None else None, _dev_ptr(ws, "ws")), "cpattn_check")
+
+
+def selftest_wait_timeout(ws, timeout_ns: int, stream=None):
+    _check(lib().cpattn_selftest_wait_timeout(_dev_ptr(ws, "ws"), ws.numel(), int(timeout_ns), _stream_ptr(stream)),
+           "cpattn_selftest_wait_timeout")
+
+
+def version() -> str:
+    return lib().cpattn_version().decode()

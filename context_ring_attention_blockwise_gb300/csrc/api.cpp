@@ -1,0 +1,348 @@
+// api.cpp -- the extern "C" entry points of libcpattn (declared in include/cpattn.h). Host
+// code only: argument checks, workspace layout, stream/event ordering of the ring-step path,
+// and kernel launches. Every compute step runs in the CUDA kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace cpattn {
+std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int layout, int causal);
+}
+
+using cpattn::Plan;
+
+namespace {
+
+thread_local std::string g_err;
+
+cpattn_status_t fail(cpattn_status_t s, const std::string& msg) {
+    g_err = msg;
+    return s;
+}
+
+cpattn_status_t cuda_fail(int e, const char* what) {
+    return fail(CPATTN_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString((cudaError_t)e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+Plan* as_plan(cpattn_plan_t p) { return reinterpret_cast<Plan*>(p); }
+
+float resolve_scale(const Plan& p, float scale) {
+    double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)p.d);
+    return (float)(s * 1.4426950408889634);   // scores are exponentiated with exp2
+}
+
+cpattn_status_t check_ws(const Plan& p, int B, const void* ws, size_t ws_bytes, bool ring) {
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    size_t need = ring ? w.ring_end : w.fwd_end;
+    if (ws_bytes < need)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    return CPATTN_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+// Reset the header, upload the tile order, place tokens and position ids.
+cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
+                         cudaStream_t st) {
+    cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
+    if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
+    e = cudaMemsetAsync(at<char>(ws, w.counts), 0, sizeof(uint64_t) * 2 * (size_t)p.n_cp * p.n_cp, st);
+    if (e) return cuda_fail(e, "cudaMemsetAsync(counts)");
+    e = cudaMemcpyAsync(at<char>(ws, w.order), p.order.data(), sizeof(int32_t) * p.order.size(),
+                        cudaMemcpyHostToDevice, st);
+    if (e) return cuda_fail(e, "cudaMemcpyAsync(order)");
+    cpattn::PermuteArgs a{};
+    a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
+    a.layout = p.layout; a.n_qt = p.n_qt;
+    a.q = q; a.k = k; a.v = v; a.pos = pos;
+    a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL);
+    a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    e = cpattn::launch_permute(a, st);
+    if (e) return cuda_fail(e, "permute kernel");
+    return CPATTN_OK;
+}
+
+cpattn_status_t check_inputs(const Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos) {
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!q || !k || !v) return fail(CPATTN_ERR_INVALID, "q, k and v must be non-NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (pos && !aligned16(pos)))
+        return fail(CPATTN_ERR_INVALID, "q, k, v and pos must be 16-byte aligned");
+    if ((double)B * (double)p.T * p.h > 2.0e9) return fail(CPATTN_ERR_UNSUPPORTED, "B*T*h beyond 2e9 rows");
+    return CPATTN_OK;
+}
+
+cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
+    cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    cpattn::AttnLaunch a{};
+    a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
+    a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt;
+    a.scale_log2 = resolve_scale(p, scale);
+    a.qL = at<char>(ws, w.qL);
+    a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);
+    a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm); a.order = at<int32_t>(ws, w.order);
+    a.counts = at<unsigned long long>(ws, w.counts);
+    a.header = at<uint32_t>(ws, w.header);
+    a.timeout_ns = 2000000000ull;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cpattn_last_error(void) { return g_err.c_str(); }
+
+const char* cpattn_version(void) { return "cpattn 0.1 sm_103a"; }
+
+cpattn_status_t cpattn_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, cpattn_layout_t layout, int causal,
+                            cpattn_plan_t* out) {
+    if (!out) return fail(CPATTN_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d_k != 64 && d_k != 128) return fail(CPATTN_ERR_UNSUPPORTED, "d_k must be 64 or 128");
+    Plan* p = new Plan();
+    std::string why = cpattn::build_plan(*p, T, h, n_kv, d_k, n_cp, (int)layout, causal);
+    if (!why.empty()) {
+        delete p;
+        return fail(CPATTN_ERR_INVALID, why);
+    }
+    *out = reinterpret_cast<cpattn_plan_t>(p);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    for (int i = 0; i < 2; ++i) {
+        if (p->ev_step[i]) cudaEventDestroy(p->ev_step[i]);
+        if (p->ev_copy[i]) cudaEventDestroy(p->ev_copy[i]);
+    }
+    if (p->ev_start) cudaEventDestroy(p->ev_start);
+    delete p;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    *bytes = cpattn::ws_layout(*p, B).fwd_end;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    *bytes = cpattn::ws_layout(*p, B).ring_end;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_tile_shape(cpattn_plan_t plan, int* block_q, int* block_k) {
+    if (!plan) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (block_q) *block_q = cpattn::kBlockQ;
+    if (block_k) *block_k = cpattn::kBlockK;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_counts(cpattn_plan_t plan, int B, int64_t* tiles_full, int64_t* tiles_diag,
+                                   int64_t* tiles_skip, int64_t* pairs, int64_t* kv_bytes_recv,
+                                   int64_t* half_units) {
+    Plan* p = as_plan(plan);
+    if (!p || B <= 0) return fail(CPATTN_ERR_INVALID, "plan and B > 0 required");
+    size_t nn = (size_t)p->n_cp * p->n_cp;
+    if (tiles_full) std::memcpy(tiles_full, p->full.data(), nn * sizeof(int64_t));
+    if (tiles_diag) std::memcpy(tiles_diag, p->diag.data(), nn * sizeof(int64_t));
+    if (tiles_skip) std::memcpy(tiles_skip, p->skip.data(), nn * sizeof(int64_t));
+    if (pairs) std::memcpy(pairs, p->pairs.data(), p->n_cp * sizeof(int64_t));
+    if (half_units) std::memcpy(half_units, p->half_units.data(), p->n_cp * sizeof(int64_t));
+    if (kv_bytes_recv)
+        for (int r = 0; r < p->n_cp; ++r)
+            kv_bytes_recv[r] = (int64_t)4 * B * p->n * p->n_kv * p->d * (p->n_cp - 1);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                               const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                               cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st))) return s;
+    cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.o = o; a.lse = lse;
+    std::string why;
+    int e = cpattn::launch_attention(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                              cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_ws(*p, B, ws, ws_bytes, false);
+    if (s) return s;
+    cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.o = o; a.lse = lse;
+    std::string why;
+    int e = cpattn::launch_attention(a, reinterpret_cast<cudaStream_t>(stream), &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                               const int32_t* pos, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
+    if ((s = prologue(*p, B, q, k, v, pos, ws, reinterpret_cast<cudaStream_t>(stream)))) return s;
+    p->next_step = 0;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
+                                 cpattn_stream_t compute, cpattn_stream_t copy) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    cpattn_status_t s = check_ws(*p, B, ws, ws_bytes, true);
+    if (s) return s;
+    if (step < 0 || step >= p->n_cp) return fail(CPATTN_ERR_INVALID, "step out of range");
+    if (p->next_step != step)
+        return fail(CPATTN_ERR_INVALID, "ring steps must follow cpattn_permute in order 0..n_cp-1 (expected step " +
+                                            std::to_string(p->next_step) + ")");
+    cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute), xst = reinterpret_cast<cudaStream_t>(copy);
+    int e;
+    for (int i = 0; i < 2; ++i) {
+        if (!p->ev_step[i] && (e = cudaEventCreateWithFlags(&p->ev_step[i], cudaEventDisableTiming))) return cuda_fail(e, "cudaEventCreate");
+        if (!p->ev_copy[i] && (e = cudaEventCreateWithFlags(&p->ev_copy[i], cudaEventDisableTiming))) return cuda_fail(e, "cudaEventCreate");
+    }
+    if (!p->ev_start && (e = cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming))) return cuda_fail(e, "cudaEventCreate");
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    const int slot = step & 1, nxt = (step + 1) & 1;
+
+    if (step == 0) {   // the copy stream must see the permuted blocks
+        if ((e = cudaEventRecord(p->ev_start, cst))) return cuda_fail(e, "cudaEventRecord");
+        if ((e = cudaStreamWaitEvent(xst, p->ev_start, 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+    } else if ((e = cudaStreamWaitEvent(cst, p->ev_copy[slot], 0))) {
+        return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
+    a.fused = 0; a.step = step;
+    if (step > 0) { a.kv_k = at<char>(ws, w.stageK[slot]); a.kv_v = at<char>(ws, w.stageV[slot]); }
+    a.kv_by_holder = 1;
+    a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
+    std::string why;
+    if ((e = cpattn::launch_attention(a, cst, &why))) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    if ((e = cudaEventRecord(p->ev_step[slot], cst))) return cuda_fail(e, "cudaEventRecord");
+
+    if (step + 1 < p->n_cp) {
+        // Send right, receive left: slot nxt of rank r <- the block rank r-1 holds now. Blocks
+        // are rank-major, so the hop is two contiguous copies per tensor.
+        if (step >= 1 && (e = cudaStreamWaitEvent(xst, p->ev_step[nxt], 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+        const size_t blk = 2 * (size_t)B * p->n * p->n_kv * p->d;    // one rank's block, bytes
+        const size_t all = blk * p->n_cp;
+        for (int t = 0; t < 2; ++t) {
+            const char* src = (step == 0) ? at<char>(ws, t ? w.vL : w.kL) : at<char>(ws, t ? w.stageV[slot] : w.stageK[slot]);
+            char* dst = at<char>(ws, t ? w.stageV[nxt] : w.stageK[nxt]);
+            if (p->n_cp > 1 && (e = cudaMemcpyAsync(dst + blk, src, all - blk, cudaMemcpyDeviceToDevice, xst)))
+                return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
+            if ((e = cudaMemcpyAsync(dst, src + all - blk, blk, cudaMemcpyDeviceToDevice, xst)))
+                return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
+        }
+        if ((e = cudaEventRecord(p->ev_copy[nxt], xst))) return cuda_fail(e, "cudaEventRecord");
+    }
+    p->next_step = step + 1;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, void* ws, size_t ws_bytes,
+                                cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_ws(*p, B, ws, ws_bytes, true);
+    if (s) return s;
+    if (p->next_step != p->n_cp) return fail(CPATTN_ERR_INVALID, "finalize needs all n_cp ring steps first");
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    cpattn::FinalizeArgs a{};
+    a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.d = p->d; a.n_cp = p->n_cp; a.layout = p->layout;
+    a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run); a.o = o; a.lse = lse;
+    int e = cpattn::launch_finalize(a, stream);
+    if (e) return cuda_fail(e, "finalize kernel");
+    p->next_step = -1;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts,
+                             void* o_bf16, float* lse, cpattn_stream_t stream) {
+    if (S <= 0 || rows <= 0 || h <= 0 || d <= 0 || d % 4) return fail(CPATTN_ERR_INVALID, "S, rows, h > 0 and d a positive multiple of 4 required");
+    if (!o_parts || !lse_parts || !o_bf16 || !lse) return fail(CPATTN_ERR_INVALID, "NULL pointer");
+    if (!aligned16(o_parts) || !aligned16(o_bf16)) return fail(CPATTN_ERR_INVALID, "o_parts and o must be 16-byte aligned");
+    int e = cpattn::launch_merge(S, rows, h, d, o_parts, lse_parts, o_bf16, lse, stream);
+    if (e) return cuda_fail(e, "merge kernel");
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_tile_counts(cpattn_plan_t plan, int B, const void* ws, int64_t* full, int64_t* diag) {
+    Plan* p = as_plan(plan);
+    if (!p || !ws || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, ws and B > 0 required");
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    const size_t nn = (size_t)p->n_cp * p->n_cp;
+    std::vector<unsigned long long> buf(2 * nn);
+    int e = cudaMemcpy(buf.data(), static_cast<const char*>(ws) + w.counts, sizeof(uint64_t) * 2 * nn,
+                       cudaMemcpyDeviceToHost);
+    if (e) return cuda_fail(e, "cudaMemcpy(counts)");
+    for (size_t i = 0; i < nn; ++i) {
+        if (full) full[i] = (int64_t)buf[2 * i];
+        if (diag) diag[i] = (int64_t)buf[2 * i + 1];
+    }
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_check(cpattn_plan_t plan, const void* ws) {
+    (void)plan;
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    uint32_t hdr[2] = {0, 0};
+    int e = cudaMemcpy(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost);
+    if (e) return cuda_fail(e, "cudaMemcpy(header)");
+    if (hdr[cpattn::kErrFlags] & cpattn::kErrTimeoutFlag) {
+        char buf[128];
+        std::snprintf(buf, sizeof buf, "device wait timed out (wait site %u)", hdr[cpattn::kErrWhere]);
+        return fail(CPATTN_ERR_TIMEOUT, buf);
+    }
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns, cpattn_stream_t stream) {
+    if (!ws || ws_bytes < sizeof(uint32_t) * cpattn::kHeaderWords) return fail(CPATTN_ERR_WORKSPACE, "workspace too small");
+    int e = cudaMemsetAsync(ws, 0, sizeof(uint32_t) * cpattn::kHeaderWords, reinterpret_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
+    e = cpattn::launch_wait_selftest(static_cast<uint32_t*>(ws), timeout_ns, stream);
+    if (e) return cuda_fail(e, "wait self-test kernel");
+    return CPATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// internal.h -- plan, workspace layout and launcher declarations shared by the host code and
+// the CUDA kernels of libcpattn. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/cpattn.h"
+
+struct CUevent_st;
+
+namespace cpattn {
+
+constexpr int kBlockQ = 128;   // query rows per tile (the tcgen05 MMA M)
+constexpr int kBlockK = 128;   // keys per tile (the QK^T MMA N, the PV MMA K)
+
+// Workspace header words (uint32), written by kernels, read by cpattn_check.
+enum HeaderWord : int { kErrFlags = 0, kErrWhere = 1, kHeaderWords = 64 };
+enum ErrFlag : uint32_t { kErrTimeoutFlag = 1u };
+
+// Byte offsets of the regions inside the caller's workspace, all 1024-aligned.
+struct WsLayout {
+    size_t header = 0;      // uint32[kHeaderWords]
+    size_t posL = 0;        // int32 [n_cp][n]: position id of (rank, local index)
+    size_t tile_mm = 0;     // int32x2 [n_cp][n_qt]: min and max position of each tile
+    size_t order = 0;       // int32 [n_cp * n_qt]: (rank, q-tile) pairs, longest first
+    size_t counts = 0;      // uint64 [n_cp][n_cp][2]: tiles computed per (rank, step), FULL / DIAG
+    size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
+    size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
+    size_t fwd_end = 0;     // end of what cpattn_forward needs
+    size_t stageK[2] = {0, 0}, stageV[2] = {0, 0};  // ring stage slots, same shape as kL
+    size_t o_run = 0;       // fp32 [n_cp][B][h][n][d] running output (normalised)
+    size_t lse_run = 0;     // fp32 [n_cp][B][h][n] running lse
+    size_t ring_end = 0;
+};
+
+struct Plan {
+    int64_t T = 0, n = 0, m = 0;   // tokens, tokens per rank, zigzag chunk
+    int h = 0, n_kv = 0, d = 0, n_cp = 0, layout = 0, causal = 0;
+    int n_qt = 0;                   // tiles per rank block (query and key tiles have one size)
+    std::vector<int32_t> order;     // (r * n_qt + qt), longest first
+    std::vector<int64_t> full, diag, skip;  // [n_cp][n_cp] by (rank, step), per (b, head)
+    std::vector<int64_t> pairs;             // [n_cp]
+    std::vector<int64_t> half_units;        // [n_cp]
+    // ring-step path state (created on first use)
+    CUevent_st* ev_step[2] = {nullptr, nullptr};
+    CUevent_st* ev_copy[2] = {nullptr, nullptr};
+    CUevent_st* ev_start = nullptr;
+    int next_step = -1;             // step expected next on the ring path (-1: permute first)
+};
+
+WsLayout ws_layout(const Plan& p, int B);
+int64_t token_of(const Plan& p, int r, int64_t j);   // natural token of (rank, local index)
+
+// ---- kernels (enqueue only; return a cudaError_t as int) --------------------------------
+struct PermuteArgs {
+    int B, T_is_int; int64_t T, n, m; int h, n_kv, d, n_cp, layout, n_qt;
+    const void* q; const void* k; const void* v; const int32_t* pos;
+    void* qL; void* kL; void* vL; int32_t* posL; int32_t* tile_mm;
+};
+int launch_permute(const PermuteArgs& a, void* stream);
+
+struct AttnLaunch {
+    int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt;
+    float scale_log2;
+    int fused;        // 1: all ring steps, natural-order bf16 output; 0: one step, merge into running state
+    int step;         // ring step (fused == 0)
+    const void* qL; const void* kv_k; const void* kv_v;   // K/V base: kL/vL or a stage slot
+    int kv_by_holder; // K/V rows indexed by the holder rank r instead of the source rank
+    const int32_t* posL; const int32_t* tile_mm; const int32_t* order;
+    unsigned long long* counts;     // tiles computed per (rank, step, class)
+    void* o; float* lse;            // fused outputs (natural order)
+    float* o_run; float* lse_run;   // ring-step running state
+    uint32_t* header;
+    uint64_t timeout_ns;
+};
+int launch_attention(const AttnLaunch& a, void* stream, std::string* why);
+
+struct FinalizeArgs {
+    int B; int64_t T, n, m; int h, d, n_cp, layout;
+    const float* o_run; const float* lse_run; void* o; float* lse;
+};
+int launch_finalize(const FinalizeArgs& a, void* stream);
+
+int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts, void* o,
+                 float* lse, void* stream);
+
+int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
+
+}  // namespace cpattn

@@ -1,0 +1,216 @@
+// layout_kernels.cu -- the HBM-bound kernels of the path: token placement (gather Q, K, V and
+// position ids into rank-major layout order), the position range of every tile, the final
+// scatter of the ring-step path back to natural order, and the standalone log-sum-exp merge.
+//
+// Placement: "Context and expert parallelism", section "The causal mask unbalances the
+// sequence" (contiguous, zigzag and round-robin stripes) and section "In PyTorch" (every
+// position-indexed tensor is sharded with the sequence, so position ids travel with tokens).
+// Merge: same page, online-softmax paragraph of "Pass them around a ring".
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+// rank and local index of natural token t
+__device__ __forceinline__ void rank_of(int layout, int64_t t, int64_t n, int64_t m, int n_cp, int& r, int64_t& j) {
+    if (layout == CPATTN_CONTIGUOUS) {
+        r = (int)(t / n);
+        j = t - (int64_t)r * n;
+    } else if (layout == CPATTN_ZIGZAG) {
+        int c = (int)(t / m);
+        if (c < n_cp) { r = c; j = t - (int64_t)c * m; }
+        else { r = 2 * n_cp - 1 - c; j = m + (t - (int64_t)c * m); }
+    } else {
+        r = (int)(t % n_cp);
+        j = t / n_cp;
+    }
+}
+
+__device__ __forceinline__ int64_t token_of_dev(int layout, int r, int64_t j, int64_t n, int64_t m, int n_cp) {
+    if (layout == CPATTN_CONTIGUOUS) return (int64_t)r * n + j;
+    if (layout == CPATTN_ZIGZAG) return j < m ? (int64_t)r * m + j : (int64_t)(2 * n_cp - 1 - r) * m + (j - m);
+    return j * n_cp + r;
+}
+
+// One 128-thread block per (rank, tile): position ids in layout order and their min/max.
+__global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restrict__ pos, int32_t* __restrict__ posL,
+                                                        int2* __restrict__ tile_mm, int64_t n, int64_t m, int n_cp,
+                                                        int layout, int n_qt) {
+    const int r = blockIdx.x / n_qt, tile = blockIdx.x % n_qt;
+    const int64_t j = (int64_t)tile * kBlockQ + threadIdx.x;
+    int lo = INT_MAX, hi = INT_MIN;
+    if (j < n) {
+        int64_t t = token_of_dev(layout, r, j, n, m, n_cp);
+        int pv = pos ? pos[t] : (int)t;
+        posL[(int64_t)r * n + j] = pv;
+        lo = hi = pv;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    __shared__ int slo[4], shi[4];
+    if ((threadIdx.x & 31) == 0) { slo[threadIdx.x >> 5] = lo; shi[threadIdx.x >> 5] = hi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 4; ++w) { lo = min(lo, slo[w]); hi = max(hi, shi[w]); }
+        tile_mm[blockIdx.x] = make_int2(lo, hi);
+    }
+}
+
+// Gather rows of d bf16 from natural [B,T,heads,d] into rank-major [n_cp][B][heads][n][d].
+// One thread moves 16 bytes; threads walk the source in order so reads are fully coalesced and
+// every destination row is written as whole 16-byte pieces of one contiguous row.
+__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
+                                                      const uint4* __restrict__ v, uint4* __restrict__ qL,
+                                                      uint4* __restrict__ kL, uint4* __restrict__ vL, int B, int64_t T,
+                                                      int64_t n, int64_t m, int h, int n_kv, int d, int n_cp,
+                                                      int layout) {
+    const int cpr = d / 8;                                  // 16-byte chunks per row
+    const int64_t nq = (int64_t)B * T * h * cpr;
+    const int64_t nk = (int64_t)B * T * n_kv * cpr;
+    const int64_t total = nq + 2 * nk;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4* src;
+        uint4* dst;
+        int64_t e;
+        int heads;
+        if (i < nq) { src = q; dst = qL; e = i; heads = h; }
+        else if (i < nq + nk) { src = k; dst = kL; e = i - nq; heads = n_kv; }
+        else { src = v; dst = vL; e = i - nq - nk; heads = n_kv; }
+        const int c = (int)(e % cpr);
+        int64_t rest = e / cpr;
+        const int hd = (int)(rest % heads);
+        rest /= heads;
+        const int64_t t = rest % T;
+        const int b = (int)(rest / T);
+        int r;
+        int64_t j;
+        rank_of(layout, t, n, m, n_cp, r, j);
+        const int64_t drow = (((int64_t)r * B + b) * heads + hd) * n + j;
+        dst[drow * cpr + c] = __ldg(src + e);
+    }
+}
+
+// Ring-step path: running fp32 state [n_cp][B][h][n][d] -> bf16 natural [B,T,h,d]; lse
+// [n_cp][B][h][n] -> [B,h,T]. One thread per 4 outputs, destination order.
+__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ o_run, const float* __restrict__ lse_run,
+                                                       uint2* __restrict__ o, float* __restrict__ lse, int B, int64_t T,
+                                                       int64_t n, int64_t m, int h, int d, int n_cp, int layout) {
+    const int cpr = d / 4;
+    const int64_t no = (int64_t)B * T * h * cpr;
+    const int64_t nl = (int64_t)B * h * T;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < no + nl; i += (int64_t)gridDim.x * blockDim.x) {
+        if (i < no) {
+            const int c = (int)(i % cpr);
+            int64_t rest = i / cpr;
+            const int hd = (int)(rest % h);
+            rest /= h;
+            const int64_t t = rest % T;
+            const int b = (int)(rest / T);
+            int r;
+            int64_t j;
+            rank_of(layout, t, n, m, n_cp, r, j);
+            const float4 x = o_run[((((int64_t)r * B + b) * h + hd) * n + j) * cpr + c];
+            __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+            uint2 out;
+            out.x = *reinterpret_cast<uint32_t*>(&lo);
+            out.y = *reinterpret_cast<uint32_t*>(&hi);
+            o[i] = out;
+        } else {
+            const int64_t e = i - no;
+            const int64_t t = e % T;
+            const int64_t bh = e / T;
+            const int b = (int)(bh / h), hd = (int)(bh % h);
+            int r;
+            int64_t j;
+            rank_of(layout, t, n, m, n_cp, r, j);
+            lse[e] = lse_run[(((int64_t)r * B + b) * h + hd) * n + j];
+        }
+    }
+}
+
+// S-way merge: o = sum_s exp(lse_s - L) o_s with L = M + ln sum_s exp(lse_s - M), M = max lse_s.
+// One thread per 4 consecutive d of one (row, head).
+__global__ void __launch_bounds__(256) merge_kernel(int S, int64_t rows, int h, int d, const float4* __restrict__ o_parts,
+                                                    const float* __restrict__ lse_parts, uint2* __restrict__ o,
+                                                    float* __restrict__ lse) {
+    const int cpr = d / 4;
+    const int64_t total = rows * h * cpr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % cpr);
+        const int64_t rh = i / cpr;
+        const int hd = (int)(rh % h);
+        const int64_t row = rh / h;
+        float M = -INFINITY;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(lse_parts + ((int64_t)s * h + hd) * rows + row));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = -INFINITY;
+        if (M != -INFINITY) {
+            float sum = 0.f;
+            for (int s = 0; s < S; ++s) sum += expf(__ldg(lse_parts + ((int64_t)s * h + hd) * rows + row) - M);
+            L = M + logf(sum);
+            for (int s = 0; s < S; ++s) {
+                const float ls = __ldg(lse_parts + ((int64_t)s * h + hd) * rows + row);
+                if (ls == -INFINITY) continue;
+                const float w = expf(ls - L);
+                const float4 x = __ldg(o_parts + ((int64_t)s * rows * h + rh) * cpr + c);
+                acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+            }
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t*>(&lo);
+        out.y = *reinterpret_cast<uint32_t*>(&hi);
+        o[i] = out;
+        if (c == 0) lse[(int64_t)hd * rows + row] = L;
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (work + threads - 1) / threads;
+    int64_t cap = (int64_t)sms * 16;
+    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+int launch_permute(const PermuteArgs& a, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int2*>(a.tile_mm), a.n, a.m,
+                                                      a.n_cp, a.layout, a.n_qt);
+    int e = (int)cudaGetLastError();
+    if (e) return e;
+    const int64_t work = (int64_t)a.B * a.T * (a.h + 2 * a.n_kv) * (a.d / 8);
+    permute_kernel<<<grid_for(work, 256), 256, 0, st>>>(
+        static_cast<const uint4*>(a.q), static_cast<const uint4*>(a.k), static_cast<const uint4*>(a.v),
+        static_cast<uint4*>(a.qL), static_cast<uint4*>(a.kL), static_cast<uint4*>(a.vL), a.B, a.T, a.n, a.m, a.h,
+        a.n_kv, a.d, a.n_cp, a.layout);
+    return (int)cudaGetLastError();
+}
+
+int launch_finalize(const FinalizeArgs& a, void* stream) {
+    const int64_t work = (int64_t)a.B * a.T * a.h * (a.d / 4 + 1);
+    finalize_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float4*>(a.o_run), a.lse_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m, a.h,
+        a.d, a.n_cp, a.layout);
+    return (int)cudaGetLastError();
+}
+
+int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts, void* o, float* lse,
+                 void* stream) {
+    const int64_t work = rows * h * (d / 4);
+    merge_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        S, rows, h, d, reinterpret_cast<const float4*>(o_parts), lse_parts, static_cast<uint2*>(o), lse);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace cpattn

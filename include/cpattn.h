@@ -1,0 +1,178 @@
+/*
+ * cpattn.h -- C ABI of the GB300 (sm_103a) context-parallel ring-attention forward.
+ *
+ * The library computes, on one GPU, the forward pass of ring attention over n_cp virtual
+ * context-parallel ranks: every rank's query chunk attends to every key/value block in ring
+ * order with an exact online-softmax merge, under contiguous, zigzag or striped token
+ * placement, with causal block skipping and grouped-query heads.
+ *
+ * Sources, cited by page title and section:
+ *   [CEX] "Context and expert parallelism" (zerotofrontier.app): "Splitting the sequence, and
+ *         the one layer that objects"; "Pass them around a ring" paragraph and the online
+ *         softmax paragraph after it; "What context parallelism communicates"; "The causal
+ *         mask unbalances the sequence"; "In PyTorch" (position ids sharded with the sequence).
+ *   [CPC] "Context Parallelism (CP)" concept page: "Key math / How it works".
+ *   [CPP] "primitive-context-parallel" skill page: "What it does"; "Interface (V1 stub)".
+ *
+ * Conventions for every call:
+ *   - The caller owns all device memory (inputs, outputs, workspace). A plan owns only host
+ *     tables and, once the ring-step path is used, two CUDA events.
+ *   - Device pointers must be 16-byte aligned. bf16 tensors are raw bf16 (uint16 storage).
+ *   - Calls are asynchronous on the given stream(s) and never synchronise the host, except
+ *     cpattn_check, which reads the workspace's error word.
+ *   - Argument errors are found on the host and returned before anything is launched; the
+ *     message is available from cpattn_last_error() on the same thread.
+ *   - Device-side errors (a bounded wait that ran out) are recorded in the workspace header
+ *     and reported by cpattn_check. No call traps, asserts on the device or throws.
+ *   - There is no CPU fallback: without a usable sm_103a device, calls return CPATTN_ERR_CUDA.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Token placement of [CEX] "The causal mask unbalances the sequence":
+ *   CONTIGUOUS: rank r holds tokens [r*n, (r+1)*n), n = T/n_cp ([CPP] "What it does").
+ *   ZIGZAG:     2*n_cp chunks of m = T/(2 n_cp); rank r holds chunk r, then chunk 2n_cp-1-r.
+ *   STRIPED:    round-robin tokens; rank r holds t = j*n_cp + r at local index j. */
+typedef enum { CPATTN_CONTIGUOUS = 0, CPATTN_ZIGZAG = 1, CPATTN_STRIPED = 2 } cpattn_layout_t;
+
+typedef enum {
+    CPATTN_OK = 0,
+    CPATTN_ERR_INVALID = 1,     /* bad argument (null pointer, shape, alignment, step order) */
+    CPATTN_ERR_UNSUPPORTED = 2, /* valid but not built here (d_k not 64 or 128, ...) */
+    CPATTN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+    CPATTN_ERR_CUDA = 4,        /* a CUDA runtime call failed (message has the CUDA error) */
+    CPATTN_ERR_TIMEOUT = 5      /* a device-side bounded wait ran out (from cpattn_check) */
+} cpattn_status_t;
+
+/* Block classes of [CEX] "The causal mask unbalances the sequence". */
+typedef enum { CPATTN_TILE_FULL = 0, CPATTN_TILE_DIAG = 1, CPATTN_TILE_SKIP = 2 } cpattn_tile_class_t;
+
+typedef struct cpattn_plan* cpattn_plan_t;   /* opaque, host-side */
+typedef struct CUstream_st* cpattn_stream_t; /* a cudaStream_t; NULL is the legacy default stream */
+
+/* Build a plan for T tokens, h query heads, n_kv key/value heads (h % n_kv == 0; query head i
+ * reads KV head i / (h/n_kv)), head width d_k (64 or 128), n_cp virtual ranks, a layout and a
+ * causal flag. Requires T % n_cp == 0 (ZIGZAG: T % (2 n_cp) == 0). The plan computes, for the
+ * default positions 0..T-1, the block class of every (rank, ring step, query tile, key tile),
+ * the per-rank work and byte counters and a longest-first order of the query tiles. Host only;
+ * no CUDA call. *out is set on success. */
+cpattn_status_t cpattn_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, cpattn_layout_t layout, int causal,
+                            cpattn_plan_t* out);
+cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan);
+
+/* Workspace bytes for cpattn_forward / cpattn_permute with batch B. */
+cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+/* Workspace bytes for the ring-step path (permute + ring_step + finalize): the forward
+ * workspace plus the two-slot key/value stage and the fp32 running (O, lse) state. */
+cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+
+/* The whole forward pass ([CEX] "Pass them around a ring" and the online-softmax paragraph;
+ * [CPC] "Key math / How it works"): place tokens, run every virtual rank over every ring step
+ * with causal block skipping, normalise and write the result back in natural token order.
+ *   q   [B, T, h, d_k]    bf16, natural token order          (device, read)
+ *   k,v [B, T, n_kv, d_k] bf16, natural token order          (device, read)
+ *   pos [T] int32 position id of each natural token, or NULL for 0..T-1 (device, read). The
+ *       causal mask shows key u to query t iff pos[u] <= pos[t]; positions travel with the
+ *       tokens ([CEX] "In PyTorch").
+ *   scale: softmax scale; <= 0 means 1/sqrt(d_k).
+ *   o   [B, T, h, d_k] bf16 output, natural order            (device, written)
+ *   lse [B, h, T] fp32 natural-log log-sum-exp of the scaled visible scores (device, written;
+ *       -inf for a row that sees no key, whose o row is then 0)
+ *   ws, ws_bytes: workspace of at least cpattn_workspace_size bytes (device, scratch).
+ * Enqueued on `stream`. */
+cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                               const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                               cpattn_stream_t stream);
+
+/* cpattn_forward without the placement step: every virtual rank over every ring step on a
+ * workspace that cpattn_permute has filled, writing o and lse as cpattn_forward does. Lets a
+ * caller place tokens once and run the attention (or time the two kernels) separately. */
+cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                              cpattn_stream_t stream);
+
+/* Ring-faithful path, step 1: gather Q, K, V and the position ids into layout order inside the
+ * workspace (rank-major blocks) and reset the workspace header. Same arguments as
+ * cpattn_forward's inputs; ws must hold cpattn_ring_workspace_size bytes to be usable by
+ * cpattn_ring_step (cpattn_workspace_size is enough for the permute alone). */
+cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                               const int32_t* pos, void* ws, size_t ws_bytes, cpattn_stream_t stream);
+
+/* Ring-faithful path, step 2 ([CEX] "Pass them around a ring"): ring step `step` of n_cp for
+ * every virtual rank at once. Rank r attends to the key/value block it holds, that of rank
+ * (r - step) mod n_cp, read from the stage slot step % 2 (step 0: its own block in place), and
+ * merges the partial (O_s, lse_s) into the fp32 running state in the workspace. On `copy` it
+ * enqueues the hop to the next step: every rank's slot (step+1) % 2 receives the block its left
+ * neighbour holds now (send right, receive left), ordered against the compute stream with
+ * events so that a slot is overwritten only after the step that read it has finished. Steps
+ * must be issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan. */
+cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
+                                 cpattn_stream_t compute, cpattn_stream_t copy);
+
+/* Ring-faithful path, step 3: the running state after the last step, rounded to bf16 and
+ * written back in natural token order: o [B,T,h,d_k] bf16, lse [B,h,T] fp32. */
+cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, void* ws, size_t ws_bytes,
+                                cpattn_stream_t stream);
+
+/* S-way log-sum-exp merge of partial attention results ([CEX] online-softmax paragraph: old
+ * totals rescaled to a common maximum). For every row and head:
+ *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).
+ *   o_parts   [S][rows][h][d] fp32 (device, read)      lse_parts [S][h][rows] fp32 (device, read)
+ *   o_bf16    [rows][h][d] bf16 (device, written)      lse       [h][rows] fp32 (device, written)
+ * d must be a multiple of 4. */
+cpattn_status_t cpattn_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts,
+                             void* o_bf16, float* lse, cpattn_stream_t stream);
+
+/* The plan's block decisions and work counters (host memory, written by the call):
+ *   tiles_full/diag/skip [n_cp * n_cp], index r * n_cp + step: tile counts of one (batch
+ *       element, query head) for rank r at ring step `step`, tiles of block_q x block_k tokens
+ *       over each rank's local order (the last tile of a block may be short);
+ *   pairs [n_cp]: exact visible (query, key) pairs of rank r for one (batch element, head);
+ *   kv_bytes_recv [n_cp]: bytes of K and V rank r receives around the ring for the batch:
+ *       4 * B * n * n_kv * d_k * (n_cp - 1) ([CEX] "What context parallelism communicates");
+ *   half_units [n_cp]: chunk-level work, FULL chunk pairs count 2 and partly visible ones 1
+ *       ([CEX] "The causal mask unbalances the sequence").
+ * Any output pointer may be NULL. Positions are 0..T-1. */
+cpattn_status_t cpattn_plan_counts(cpattn_plan_t plan, int B, int64_t* tiles_full, int64_t* tiles_diag,
+                                   int64_t* tiles_skip, int64_t* pairs, int64_t* kv_bytes_recv,
+                                   int64_t* half_units);
+
+/* After the stream has been synchronised: the key tiles the kernels actually computed since the
+ * last cpattn_forward / cpattn_permute on this workspace, summed over batch elements and query
+ * heads, by (rank r, ring step): full[r * n_cp + step] tiles computed without a mask (every
+ * pair visible) and diag[r * n_cp + step] partly visible tiles computed with the element mask.
+ * Skipped tiles are not computed. With positions 0..T-1 these equal B * h times the plan's
+ * tiles_full and tiles_diag. Host arrays of n_cp * n_cp; either may be NULL. */
+cpattn_status_t cpattn_tile_counts(cpattn_plan_t plan, int B, const void* ws, int64_t* full, int64_t* diag);
+
+/* Query and key tile sizes the plan classifies and the kernels compute with. */
+cpattn_status_t cpattn_tile_shape(cpattn_plan_t plan, int* block_q, int* block_k);
+
+/* After the stream that ran the calls has been synchronised: reads the workspace header and
+ * returns CPATTN_OK, or CPATTN_ERR_TIMEOUT if a device-side wait ran out (the message names the
+ * wait). ws is the device workspace. */
+cpattn_status_t cpattn_check(cpattn_plan_t plan, const void* ws);
+
+/* Failure-detection self test: launches one block that waits on a barrier nothing completes,
+ * with a limit of timeout_ns nanoseconds, and records the timeout in the workspace header
+ * exactly as the attention kernels do. cpattn_check then reports CPATTN_ERR_TIMEOUT. */
+cpattn_status_t cpattn_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t timeout_ns,
+                                             cpattn_stream_t stream);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char* cpattn_last_error(void);
+
+/* Library version, e.g. "cpattn 0.1 sm_103a". */
+const char* cpattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */
