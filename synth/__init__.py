@@ -14,7 +14,7 @@ import tempfile
 
 import numpy as np
 
-from .configs import CONFIGS, Workload, workload  # noqa: F401
+from .configs import CONFIGS, LAYOUT_IDS, LAYOUT_NAMES, ORDER, Workload, workload  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
