@@ -271,7 +271,9 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, co
     const int64_t jl = (int64_t)qt * 128 + row;          // local index on rank r
     const bool row_valid = jl < P.n;
     const int qpos = row_valid ? __ldg(P.posL + (int64_t)r * P.n + jl) : 0;
-    float m_used = -INFINITY, l = 0.f;
+    // l: sum of the fp32 exponentials (for lse); lr: sum of the same values rounded to bf16 as the
+    // PV product sees them (for the normalisation of O, so its weights sum to one exactly).
+    float m_used = -INFINITY, l = 0.f, lr = 0.f;
     TileWalk w;
     w.init(P, r, qmm);
     int j = 0;
@@ -325,16 +327,24 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, co
         if (resc) {
             alpha = ex2(m_used - m_new);
             l *= alpha;
+            lr *= alpha;
             m_used = m_new;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float rs = 0.f;
+        // P is rounded to bf16 for the PV product; the row sum adds the same rounded values, so
+        // the weights O / l applies are exactly the ones the tensor core multiplied.
+        uint32_t pk[64];
+        float rs = 0.f, rsr = 0.f;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-            x[c] = ex2(fmaf(x[c], P.scale_log2, -msub));
-            rs += x[c];
+        for (int c = 0; c < 64; ++c) {
+            const float p0 = ex2(fmaf(x[2 * c], P.scale_log2, -msub));
+            const float p1 = ex2(fmaf(x[2 * c + 1], P.scale_log2, -msub));
+            pk[c] = pack_bf16(p0, p1);
+            rs += p0 + p1;
+            rsr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
         }
         l += rs;
+        lr += rsr;
         if (j > 0) {   // PV of the previous tile done: the P buffer is free and O is stable
             ok = __all_sync(0xffffffffu, wait(bars.pv_done, (j - 1) & 1, kSitePvDone));
             if (!ok) break;
@@ -357,8 +367,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, co
         for (int g8 = 0; g8 < 16; ++g8) {
             const int pn = g8 >> 3, cc = g8 & 7;
             const uint32_t addr = sP + pn * C::PANEL_BYTES + row * 128 + (((cc ^ (row & 7)) & 7) << 4);
-            st_shared_v4(addr, pack_bf16(x[8 * g8 + 0], x[8 * g8 + 1]), pack_bf16(x[8 * g8 + 2], x[8 * g8 + 3]),
-                         pack_bf16(x[8 * g8 + 4], x[8 * g8 + 5]), pack_bf16(x[8 * g8 + 6], x[8 * g8 + 7]));
+            st_shared_v4(addr, pk[4 * g8 + 0], pk[4 * g8 + 1], pk[4 * g8 + 2], pk[4 * g8 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -374,7 +383,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, co
     } else if (!P.fused && P.step > 0) {
         return;   // nothing visible at this step: the running state is unchanged
     }
-    const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+    const float inv_l = lr > 0.f ? 1.0f / lr : 0.f;
     const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
     if (P.fused) {
         int64_t tn = 0;

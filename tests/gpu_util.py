@@ -13,6 +13,15 @@ O_TOL = 1e-2      # max-abs error on O (bf16 output from bf16 inputs, fp32 accum
 LSE_TOL = 1e-3    # max-abs error on lse (fp32)
 
 
+def o_tolerance(ref_o: np.ndarray) -> np.ndarray:
+    """Per-element bound on |O - O_exact|: 1e-2, except where |O_exact| >= 4. There the spacing
+    of the bf16 grid (2^-5 in [4, 8)) is wider than twice 1e-2, so no bf16 value need lie within
+    1e-2 of the exact one; such elements must instead be within one bf16 ulp of it."""
+    a = np.abs(ref_o)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(a, 1e-30))) - 7)
+    return np.where(a >= 4.0, ulp, O_TOL)
+
+
 def to_device_bf16(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
@@ -52,7 +61,12 @@ def compare(o, lse, ref_o, ref_lse, rows=None, what=""):
     assert np.all(np.isfinite(o)), f"{what}: non-finite O"
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(lse), fin), f"{what}: -inf pattern of lse differs"
-    eo = float(np.max(np.abs(o - ref_o))) if o.size else 0.0
+    err = np.abs(o - ref_o)
+    eo = float(np.max(err)) if o.size else 0.0
     el = float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0
-    assert eo <= O_TOL and el <= LSE_TOL, f"{what}: max|dO| = {eo:.3e} (tol {O_TOL}), max|dlse| = {el:.3e} (tol {LSE_TOL})"
+    over = err > o_tolerance(ref_o)
+    if over.any() or el > LSE_TOL:
+        idx = np.unravel_index(int(np.argmax(err - o_tolerance(ref_o))), err.shape)
+        raise AssertionError(f"{what}: max|dO| = {eo:.3e} ({int(over.sum())} elements over tolerance; worst at "
+                             f"{idx}: got {o[idx]:.6f}, exact {ref_o[idx]:.6f}), max|dlse| = {el:.3e} (tol {LSE_TOL})")
     return eo, el
