@@ -23,7 +23,7 @@ _lib = None
 
 SYMBOLS = [
     "cpattn_plan", "cpattn_plan_destroy", "cpattn_workspace_size", "cpattn_ring_workspace_size", "cpattn_forward",
-    "cpattn_attend",
+    "cpattn_attend", "cpattn_forward_noalloc",
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
 ]
@@ -56,6 +56,7 @@ def lib():
     L.cpattn_ring_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_forward.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_forward_noalloc.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]
     L.cpattn_permute.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_ring_step.argtypes = [_P, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, _P]
     L.cpattn_finalize.argtypes = [_P, i, _P, _P, _P, ctypes.c_size_t, _P]
@@ -192,6 +193,21 @@ def forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, 
     _check(lib().cpattn_forward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
                                 _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
                                 _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_forward")
+    return out, lse
+
+
+def forward_noalloc(q, k, v, plan: Plan, pos=None, scale: float | None = None, out=None, lse=None, stream=None):
+    """cpattn_forward_noalloc: the forward with the library's built-in 64 MiB device scratch, for
+    callers that cannot allocate a workspace (outputs may still come from the caller)."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    _check(lib().cpattn_forward_noalloc(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                        _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"),
+                                        _dev_ptr(lse, "lse"), _stream_ptr(stream)), "cpattn_forward_noalloc")
     return out, lse
 
 

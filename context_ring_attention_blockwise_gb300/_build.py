@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcpattn.so")
-SOURCES = ["api.cpp", "plan.cpp", "layout_kernels.cu", "attention.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "layout_kernels.cu", "attention.cu", "noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -18,8 +18,15 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
 using cpattn::Plan;
 
 namespace {
-
 thread_local std::string g_err;
+}
+
+namespace cpattn {
+// Record the message cpattn_last_error returns on this thread (for entry points in other files).
+void set_last_error(const std::string& msg) { g_err = msg; }
+}  // namespace cpattn
+
+namespace {
 
 cpattn_status_t fail(cpattn_status_t s, const std::string& msg) {
     g_err = msg;

@@ -52,6 +52,7 @@ struct Plan {
 };
 
 WsLayout ws_layout(const Plan& p, int B);
+void set_last_error(const std::string& msg);
 int64_t token_of(const Plan& p, int r, int64_t j);   // natural token of (rank, local index)
 
 // ---- kernels (enqueue only; return a cudaError_t as int) --------------------------------

@@ -97,6 +97,22 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
 cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                               cpattn_stream_t stream);
 
+/* cpattn_forward for callers that cannot allocate device memory. The paper has no counterpart:
+ * this call exists for code that may not call cudaMalloc or any allocating routine, such as a
+ * host callback, an allocator hook or a plug-in that must leave the process's memory pools alone.
+ * Same arguments as cpattn_forward minus the workspace: the scratch is a 64 MiB device array
+ * built into the library, which every GPU that loads the library holds until the process
+ * exits. The call itself allocates nothing. A problem whose cpattn_workspace_size exceeds
+ * 64 MiB is rejected with CPATTN_ERR_WORKSPACE and a message saying so.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before capturing a stream.
+ *   - All calls share the array and it keeps the last call's contents; each call clears what
+ *     must start at zero. Calls that overlap on the GPU (other streams, other threads) race on
+ *     it: issue them one after another on one stream. */
+cpattn_status_t cpattn_forward_noalloc(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const int32_t* pos, float scale, void* o, float* lse,
+                                       cpattn_stream_t stream);
+
 /* Ring-faithful path, step 1: gather Q, K, V and the position ids into layout order inside the
  * workspace (rank-major blocks) and reset the workspace header. Same arguments as
  * cpattn_forward's inputs; ws must hold cpattn_ring_workspace_size bytes to be usable by
