@@ -66,7 +66,7 @@ cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const voi
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
-    e = cudaMemsetAsync(at<char>(ws, w.counts), 0, sizeof(uint64_t) * 2 * (size_t)p.n_cp * p.n_cp, st);
+    e = cudaMemsetAsync(at<char>(ws, w.counts), 0, w.sched + sizeof(uint32_t) * (1 + (size_t)p.n_cp) - w.counts, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(counts)");
     e = cudaMemcpyAsync(at<char>(ws, w.order), p.order.data(), sizeof(int32_t) * p.order.size(),
                         cudaMemcpyHostToDevice, st);
@@ -95,7 +95,8 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     cpattn::AttnLaunch a{};
     a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
-    a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt;
+    a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt; a.pair_heads = p.pair_heads; a.n_grp = p.n_grp;
+    a.sched = at<uint32_t>(ws, w.sched);
     a.scale_log2 = resolve_scale(p, scale);
     a.qL = at<char>(ws, w.qL);
     a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);
@@ -104,6 +105,13 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
     return a;
+}
+
+// Zero the launch's work counter, then enqueue the persistent attention kernel.
+int launch_attn(const cpattn::AttnLaunch& a, cudaStream_t st, std::string* why) {
+    int e = cudaMemsetAsync(a.sched, 0, sizeof(uint32_t), st);
+    if (e) return e;
+    return cpattn::launch_attention(a, st, why);
 }
 
 }  // namespace
@@ -194,7 +202,7 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
     a.o = o; a.lse = lse;
     std::string why;
-    int e = cpattn::launch_attention(a, st, &why);
+    int e = launch_attn(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
@@ -211,7 +219,7 @@ cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, f
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
     a.o = o; a.lse = lse;
     std::string why;
-    int e = cpattn::launch_attention(a, reinterpret_cast<cudaStream_t>(stream), &why);
+    int e = launch_attn(a, reinterpret_cast<cudaStream_t>(stream), &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
@@ -257,11 +265,12 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
     }
     cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
     a.fused = 0; a.step = step;
+    a.sched = at<uint32_t>(ws, w.sched) + 1 + step;
     if (step > 0) { a.kv_k = at<char>(ws, w.stageK[slot]); a.kv_v = at<char>(ws, w.stageV[slot]); }
     a.kv_by_holder = 1;
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
     std::string why;
-    if ((e = cpattn::launch_attention(a, cst, &why))) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    if ((e = launch_attn(a, cst, &why))) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     if ((e = cudaEventRecord(p->ev_step[slot], cst))) return cuda_fail(e, "cudaEventRecord");
 
     if (step + 1 < p->n_cp) {

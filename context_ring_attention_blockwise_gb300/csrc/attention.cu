@@ -1,30 +1,41 @@
 // attention.cu -- the ring-step attention kernel for sm_103a.
 //
-// One CTA owns one work unit: 128 query rows of one (batch element, query head) on one virtual
-// rank r. It walks the key/value blocks in ring order ("Context and expert parallelism",
-// "Pass them around a ring": at step s rank r holds the block of rank (r - s) mod n_cp), skips
-// key tiles that no query of the unit can see and masks the partly visible ones ("The causal
-// mask unbalances the sequence"), and keeps the online-softmax state of the paragraph after it
-// (running max, running sum of exponentials, running weighted sum of values, rescaled when a
-// larger score arrives) on chip across every step.
+// A persistent kernel. Each CTA repeatedly takes a work unit from a global counter, in the
+// longest-first order the plan computed. A unit is two 128-row query tiles on one virtual rank r
+// that share every key/value tile: two heads of one KV group (the group size is even), or two
+// adjacent query tiles of one head (otherwise). The unit walks the key/value blocks in ring order
+// ("Context and expert parallelism", "Pass them around a ring": at step s rank r holds the block
+// of rank (r - s) mod n_cp). It skips key tiles no query of the unit can see and masks the partly
+// visible ones ("The causal mask unbalances the sequence"). It keeps the online-softmax state of
+// the paragraph after the ring one on chip across every step: running max, running sum of
+// exponentials, running weighted sum of values, rescaled when a larger score arrives.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: Q tile once, then K and V tiles through an NS-deep stage ring.
-//   warp 1      owns tensor memory; one lane issues tcgen05.mma: S = Q K^T into one of two
-//               TMEM score buffers, O += P V into the TMEM output accumulator.
-//   warps 2..5  one thread per query row: read S from TMEM, mask, row max, exp2, row sum,
-//               write P (bf16) to shared memory, rescale O lazily, and the epilogue.
-// Tensor memory (512 columns): S0 at 0, S1 at 128, O at 256 (d_k columns of fp32).
+// Warp roles (384 threads; registers move from warpgroup 0 to the softmax warpgroups with
+// setmaxnreg: 128 x 56 + 256 x 224 = the 384 x 168 the block is launched with):
+//   warp 0      scheduler + TMA producer: the next unit index into a 2-slot ring; both Q tiles
+//               once per unit; K and V tiles through an NS-deep stage ring, V one tile behind K.
+//   warp 1      owns tensor memory; one lane issues tcgen05.mma. S_i = Q_i K^T (SS form), then
+//               O_i += P_i V with P_i read from tensor memory (TS form).
+//   warps 2, 3  idle.
+//   warps 4..7  softmax warpgroup 0 (query tile 0), one thread per row.
+//   warps 8..11 softmax warpgroup 1 (query tile 1). Each thread reads its row of S from TMEM,
+//               masks, takes the max, exponentiates with exp2, sums, writes P (bf16) back over
+//               S in TMEM, rescales O lazily, and writes the unit's output.
+// Tensor memory (512 columns): S0 at 0, S1 at 128 (P_i packed bf16x2 over the first 64 columns
+// of S_i), O0 at 256, O1 at 256 + d_k.
 //
-// Rescaling is lazy: the row keeps using a stale maximum m_used until a tile raises the row
-// maximum by more than 8 (in log2 units), so P stays below 2^8 and the final O / l is unchanged.
-// Every wait is bounded by a global-timer limit; on expiry the kernel records the wait site in
-// the workspace header, lets every role leave its loop, waits for its own copies and MMAs, and
-// frees tensor memory before returning.
+// MMAs from the issuing thread execute in order. So QK_i of the next tile, which overwrites
+// S_i / P_i, is issued only after PV_i of this tile, which reads P_i.
+//
+// Rescaling is lazy: a row keeps a stale maximum until a tile raises it by more than 8 (log2
+// units). P then stays below 2^8 and the final O / l is unchanged. Every wait is bounded by a
+// global-timer limit. On expiry the kernel records the wait site in the workspace header, every
+// role leaves its loop, the kernel waits for its own copies and MMAs, and frees tensor memory.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 #include <string>
 
@@ -36,14 +47,19 @@ namespace {
 
 using namespace ptx;
 
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 96, kRegsHigh = 200;   // 128 * low + 256 * high <= 384 * 168
+
 struct Params {
-    int B, h, n_kv, g, n_cp, n_qt, causal, fused, step, kv_by_holder, layout;
+    int B, h, n_kv, g, n_cp, n_qt, n_grp, pair_heads, causal, fused, step, kv_by_holder, layout;
+    int num_units;
     int64_t n, m, T;
     float scale_log2;
     const int32_t* posL;
     const int2* tile_mm;
     const int32_t* order;
     unsigned long long* counts;
+    uint32_t* sched;
     uint16_t* o;
     float* lse;
     float* o_run;
@@ -54,57 +70,64 @@ struct Params {
 
 template <int D>
 struct Cfg {
-    static constexpr int NS = (D == 128) ? 2 : 3;         // K/V stage depth
+    static constexpr int NS = (D == 128) ? 2 : 4;         // K/V stage depth
     static constexpr int PANELS = D / 64;                 // 64-column (128-byte) swizzle panels
     static constexpr int PANEL_BYTES = 128 * 128;         // 128 rows x 128 bytes
-    static constexpr int Q_BYTES = 128 * D * 2;
-    static constexpr int KV_BYTES = 128 * D * 2;
-    static constexpr int P_BYTES = 128 * 128 * 2;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int Q_BYTES = 128 * D * 2;           // one query tile
+    static constexpr int KV_BYTES = 128 * D * 2;          // one key (or value) tile
+    static constexpr int OFF_Q = 0;                       // two query tiles
+    static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int NBAR = 1 + 4 * NS + 2 + 2 + 1 + 1 + 1;
+    static constexpr int OFF_BAR = OFF_V + NS * KV_BYTES;
+    static constexpr int NBAR = 15 + 4 * NS;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+    static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 256;
+    static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
 };
 
-// Barrier addresses in shared memory.
+// Barrier addresses are computed from the base on use (fixed offsets), so no role keeps a
+// register per barrier.
 template <int D>
 struct Bars {
-    uint32_t q_full, k_full[Cfg<D>::NS], v_full[Cfg<D>::NS], k_empty[Cfg<D>::NS], v_empty[Cfg<D>::NS];
-    uint32_t s_full[2], s_free[2], p_full, pv_done, mma_done;
-    __device__ void setup(uint32_t base) {
-        uint32_t a = base;
-        auto next = [&]() { uint32_t r = a; a += 8; return r; };
-        q_full = next();
-        for (int i = 0; i < Cfg<D>::NS; ++i) k_full[i] = next();
-        for (int i = 0; i < Cfg<D>::NS; ++i) v_full[i] = next();
-        for (int i = 0; i < Cfg<D>::NS; ++i) k_empty[i] = next();
-        for (int i = 0; i < Cfg<D>::NS; ++i) v_empty[i] = next();
-        s_full[0] = next(); s_full[1] = next();
-        s_free[0] = next(); s_free[1] = next();
-        p_full = next(); pv_done = next(); mma_done = next();
-    }
-    __device__ void init() {
-        mbar_init(q_full, 1);
-        for (int i = 0; i < Cfg<D>::NS; ++i) {
-            mbar_init(k_full[i], 1); mbar_init(v_full[i], 1);
-            mbar_init(k_empty[i], 1); mbar_init(v_empty[i], 1);
+    static constexpr int NS = Cfg<D>::NS;
+    uint32_t base;
+    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
+    __device__ uint32_t unit_full(int s) const { return at(s); }
+    __device__ uint32_t unit_empty(int s) const { return at(2 + s); }
+    __device__ uint32_t q_full() const { return at(4); }
+    __device__ uint32_t q_empty() const { return at(5); }
+    __device__ uint32_t k_full(int st) const { return at(6 + st); }
+    __device__ uint32_t v_full(int st) const { return at(6 + NS + st); }
+    __device__ uint32_t k_empty(int st) const { return at(6 + 2 * NS + st); }
+    __device__ uint32_t v_empty(int st) const { return at(6 + 3 * NS + st); }
+    __device__ uint32_t s_full(int i) const { return at(6 + 4 * NS + i); }
+    __device__ uint32_t p_full(int i) const { return at(8 + 4 * NS + i); }
+    __device__ uint32_t pv_done(int i) const { return at(10 + 4 * NS + i); }
+    __device__ uint32_t o_free(int i) const { return at(12 + 4 * NS + i); }
+    __device__ uint32_t mma_done() const { return at(14 + 4 * NS); }
+    static constexpr int kCount = 15 + 4 * NS;
+    __device__ void init() const {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(unit_full(i), 1);
+            mbar_init(unit_empty(i), 1 + 8);          // the MMA lane and one lane per softmax warp
+            mbar_init(s_full(i), 1);
+            mbar_init(p_full(i), 128);
+            mbar_init(pv_done(i), 1);
+            mbar_init(o_free(i), 128);
         }
-        for (int i = 0; i < 2; ++i) { mbar_init(s_full[i], 1); mbar_init(s_free[i], 128); }
-        mbar_init(p_full, 128);
-        mbar_init(pv_done, 1);
-        mbar_init(mma_done, 1);
+        mbar_init(q_full(), 1);
+        mbar_init(q_empty(), 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full(i), 1); mbar_init(v_full(i), 1);
+            mbar_init(k_empty(i), 1); mbar_init(v_empty(i), 1);
+        }
+        mbar_init(mma_done(), 1);
     }
 };
 
-// Wait sites reported through the header on a timeout.
-enum Site : int { kSiteQ = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty, kSiteSFull, kSiteSFree,
-                  kSitePFull, kSitePvDone, kSiteDrain, kSiteSelfTest };
+enum Site : int { kSiteQ = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty, kSiteSFull, kSiteQEmpty,
+                  kSitePFull, kSitePvDone, kSiteDrain, kSiteSelfTest, kSiteUnitFull, kSiteUnitEmpty, kSiteOFree };
 
 struct Waiter {
     volatile int* abort_flag;
@@ -132,13 +155,59 @@ struct Waiter {
     }
 };
 
-// The key tiles one unit visits, in ring order, with SKIP tiles left out. Every role walks the
-// same sequence. mask = 1 when the tile is partly visible or shorter than 128 keys.
+// One work unit: rank r, batch element b, and two query tiles (head_i, qt_i) sharing KV head kvh.
+struct Unit {
+    int r, b, kvh;
+    int head[2], qt[2], valid[2];
+    int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
+    Unit U;
+    if (P.pair_heads) {
+        const int hp = P.h / 2, per = P.B * hp;
+        const int rg = __ldg(P.order + u / per);
+        U.r = rg / P.n_grp;
+        const int qt = rg % P.n_grp;
+        const int rem = u % per;
+        U.b = rem / hp;
+        U.head[0] = 2 * (rem % hp);
+        U.head[1] = U.head[0] + 1;
+        U.qt[0] = U.qt[1] = qt;
+        U.valid[0] = U.valid[1] = 1;
+    } else {
+        const int per = P.B * P.h;
+        const int rg = __ldg(P.order + u / per);
+        U.r = rg / P.n_grp;
+        const int grp = rg % P.n_grp;
+        const int rem = u % per;
+        U.b = rem / P.h;
+        U.head[0] = U.head[1] = rem % P.h;
+        U.qt[0] = 2 * grp;
+        U.qt[1] = 2 * grp + 1;
+        U.valid[0] = 1;
+        U.valid[1] = U.qt[1] < P.n_qt;
+    }
+    U.kvh = U.head[0] / P.g;
+    for (int i = 0; i < 2; ++i)
+        U.qmm[i] = U.valid[i] ? __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]) : make_int2(INT_MAX, INT_MIN);
+    return U;
+}
+
+// The key tiles a unit visits, in ring order, leaving out tiles that both query tiles skip.
+// cls[i]: FULL / DIAG / SKIP for query tile i; mask[i]: the tile needs the element mask for
+// query tile i (partly visible, skipped by this tile only, or shorter than 128 keys).
 struct TileWalk {
     const Params* p;
-    int r, qmin, qmax, s, s_end, kt, src, mask, diag;
-    __device__ void init(const Params& P, int r_, int2 qmm) {
-        p = &P; r = r_; qmin = qmm.x; qmax = qmm.y;
+    int r, s, s_end, kt, src;
+    int qmin0, qmax0, qmin1, qmax1, cls0, cls1, mask0, mask1;
+    __device__ int cls(int i) const { return i ? cls1 : cls0; }
+    __device__ int mask(int i) const { return i ? mask1 : mask0; }
+    __device__ void init(const Params& P, const Unit& U) {
+        p = &P;
+        r = U.r;
+        qmin0 = U.qmm[0].x; qmax0 = U.qmm[0].y;
+        qmin1 = U.qmm[1].x; qmax1 = U.qmm[1].y;
         s = P.fused ? 0 : P.step;
         s_end = P.fused ? P.n_cp : P.step + 1;
         kt = -1;
@@ -152,295 +221,384 @@ struct TileWalk {
             }
             src = r - s;
             if (src < 0) src += P.n_cp;
-            const bool short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
-            if (!P.causal) { diag = 0; mask = short_tile; return true; }
+            const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
+            if (!P.causal) {
+                cls0 = cls1 = CPATTN_TILE_FULL;
+                mask0 = mask1 = short_tile;
+                return true;
+            }
             const int2 kmm = __ldg(P.tile_mm + src * P.n_qt + kt);
-            if (kmm.x > qmax) continue;                 // every key after every query: skip
-            diag = kmm.y > qmin;                        // some key after some query
-            mask = diag || short_tile;                  // partly visible: element mask
+            cls0 = (kmm.x > qmax0) ? CPATTN_TILE_SKIP : (kmm.y > qmin0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            cls1 = (kmm.x > qmax1) ? CPATTN_TILE_SKIP : (kmm.y > qmin1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
+            mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
+            mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
             return true;
         }
     }
 };
 
+// ---------------------------------------------------------------------------------------------
+// warp 0: scheduler and TMA producer
+// ---------------------------------------------------------------------------------------------
 template <int D>
 __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                         uint32_t sQ, uint32_t sK, uint32_t sV, const Bars<D>& bars, const Waiter& wait, int r,
-                         int qt, int b, int head, int kvh, int2 qmm) {
+                         uint32_t sQ, uint32_t sK, uint32_t sV, volatile int* unit_slot, const Bars<D>& bars,
+                         const Waiter& wait) {
     using C = Cfg<D>;
-    TileWalk w;
-    w.init(P, r, qmm);
-    const int qrow = (int)((((int64_t)r * P.B + b) * P.h + head) * P.n + (int64_t)qt * 128);
-    int nk = 0, nv = 0;            // K and V tiles issued
-    int prev_row = 0;
-    bool ok = true, q_issued = false;
-    auto load_v = [&](int i, int row) -> bool {
-        const int st = i % C::NS;
-        if (i >= C::NS && !wait(bars.v_empty[st], ((i / C::NS) - 1) & 1, kSiteVEmpty)) return false;
-        mbar_arrive_expect_tx(bars.v_full[st], C::KV_BYTES);
+    int nk = 0, nv = 0, nq = 0;   // K tiles, V tiles, Q pairs issued by this CTA
+    bool ok = true;
+    auto load_v = [&](int row) -> bool {
+        const int st = nv % C::NS;
+        if (nv >= C::NS && !wait(bars.v_empty(st), ((nv / C::NS) - 1) & 1, kSiteVEmpty)) return false;
+        mbar_arrive_expect_tx(bars.v_full(st), C::KV_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_2d(sV + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmV, bars.v_full[st], pn * 64, row);
+            tma_load_2d(sV + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmV, bars.v_full(st), pn * 64, row);
         ++nv;
         return true;
     };
-    while (w.next()) {
-        const int holder = P.kv_by_holder ? r : w.src;
-        const int krow = (int)((((int64_t)holder * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)w.kt * 128);
-        if (!q_issued) {
-            mbar_arrive_expect_tx(bars.q_full, C::Q_BYTES);
-            for (int pn = 0; pn < C::PANELS; ++pn) tma_load_2d(sQ + pn * C::PANEL_BYTES, tmQ, bars.q_full, pn * 64, qrow);
-            q_issued = true;
+    for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        const int u = (int)atomicAdd(P.sched, 1u);
+        if (it >= 2 && !wait(bars.unit_empty(slot), ((it >> 1) - 1) & 1, kSiteUnitEmpty)) { ok = false; break; }
+        unit_slot[slot] = (u < P.num_units) ? u : -1;
+        mbar_arrive(bars.unit_full(slot));
+        if (u >= P.num_units) break;
+        const Unit U = decode_unit(P, u);
+        TileWalk w;
+        w.init(P, U);
+        int j = 0, prev_row = 0;
+        while (w.next()) {
+            const int holder = P.kv_by_holder ? U.r : w.src;
+            const int krow = (int)((((int64_t)holder * P.B + U.b) * P.n_kv + U.kvh) * P.n + (int64_t)w.kt * 128);
+            if (j == 0) {
+                if (nq >= 1 && !wait(bars.q_empty(), (nq - 1) & 1, kSiteQEmpty)) { ok = false; break; }
+                mbar_arrive_expect_tx(bars.q_full(), 2 * C::Q_BYTES);
+                for (int i = 0; i < 2; ++i) {
+                    const int qrow = (int)((((int64_t)U.r * P.B + U.b) * P.h + U.head[i]) * P.n + (int64_t)U.qt[i] * 128);
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_2d(sQ + i * C::Q_BYTES + pn * C::PANEL_BYTES, tmQ, bars.q_full(), pn * 64, qrow);
+                }
+                ++nq;
+            }
+            const int st = nk % C::NS;
+            if (nk >= C::NS && !wait(bars.k_empty(st), ((nk / C::NS) - 1) & 1, kSiteKEmpty)) { ok = false; break; }
+            mbar_arrive_expect_tx(bars.k_full(st), C::KV_BYTES);
+            for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_2d(sK + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmK, bars.k_full(st), pn * 64, krow);
+            ++nk;
+            if (j >= 1 && !load_v(prev_row)) { ok = false; break; }     // V runs one tile behind K
+            prev_row = krow;
+            ++j;
         }
-        const int st = nk % C::NS;
-        if (nk >= C::NS && !wait(bars.k_empty[st], ((nk / C::NS) - 1) & 1, kSiteKEmpty)) { ok = false; break; }
-        mbar_arrive_expect_tx(bars.k_full[st], C::KV_BYTES);
-        for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_2d(sK + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmK, bars.k_full[st], pn * 64, krow);
-        ++nk;
-        if (nk >= 2 && !load_v(nk - 2, prev_row)) { ok = false; break; }   // V runs one tile behind K
-        prev_row = krow;
+        if (ok && j >= 1) ok = load_v(prev_row);
     }
-    if (ok && nk >= 1) ok = load_v(nk - 1, prev_row);
     if (ok) {
-        // Normal tail: the last arrivals of the tensor core on the stage barriers have landed.
-        for (int i = (nk > C::NS ? nk - C::NS : 0); i < nk; ++i) wait(bars.k_empty[i % C::NS], (i / C::NS) & 1, kSiteKEmpty);
-        for (int i = (nv > C::NS ? nv - C::NS : 0); i < nv; ++i) wait(bars.v_empty[i % C::NS], (i / C::NS) & 1, kSiteVEmpty);
+        // The tensor core's last arrivals on the stage barriers have landed before the CTA exits.
+        for (int i = (nk > C::NS ? nk - C::NS : 0); i < nk; ++i) wait(bars.k_empty(i % C::NS), (i / C::NS) & 1, kSiteKEmpty);
+        for (int i = (nv > C::NS ? nv - C::NS : 0); i < nv; ++i) wait(bars.v_empty(i % C::NS), (i / C::NS) & 1, kSiteVEmpty);
+        if (nq >= 1) wait(bars.q_empty(), (nq - 1) & 1, kSiteQEmpty);
     } else {
         // Aborted: still wait (bounded) until our own copies in flight have landed.
-        if (q_issued) wait(bars.q_full, 0, kSiteQ, false);
-        for (int i = (nk > C::NS ? nk - C::NS : 0); i < nk; ++i) wait(bars.k_full[i % C::NS], (i / C::NS) & 1, kSiteKFull, false);
-        for (int i = (nv > C::NS ? nv - C::NS : 0); i < nv; ++i) wait(bars.v_full[i % C::NS], (i / C::NS) & 1, kSiteVFull, false);
+        if (nq >= 1) wait(bars.q_full(), (nq - 1) & 1, kSiteQ, false);
+        for (int i = (nk > C::NS ? nk - C::NS : 0); i < nk; ++i) wait(bars.k_full(i % C::NS), (i / C::NS) & 1, kSiteKFull, false);
+        for (int i = (nv > C::NS ? nv - C::NS : 0); i < nv; ++i) wait(bars.v_full(i % C::NS), (i / C::NS) & 1, kSiteVFull, false);
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// warp 1, lane 0: MMA issue
+// ---------------------------------------------------------------------------------------------
 template <int D>
-__device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV, uint32_t sP,
-                           const Bars<D>& bars, const Waiter& wait, int r, int2 qmm) {
+__device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t sK, uint32_t sV,
+                           volatile int* unit_slot, const Bars<D>& bars, const Waiter& wait) {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);   // A = Q (K-major), B = K (K-major)
-    constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);     // A = P (K-major), B = V (MN-major)
-    TileWalk w;
-    w.init(P, r, qmm);
-    auto issue_pv = [&](int i) -> bool {
-        const int st = i % C::NS;
-        if (!wait(bars.p_full, i & 1, kSitePFull)) return false;
-        if (!wait(bars.v_full[st], (i / C::NS) & 1, kSiteVFull)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {      // 128 keys, 16 per MMA
-            const uint64_t a = desc_sw128(sP + (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = desc_sw128(sV + st * C::KV_BYTES + kk * 2048, C::PANEL_BYTES, 1024);
-            mma_bf16_ss(tmem + C::O_COL, a, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bars.v_empty[st]);
-        mma_commit(bars.pv_done);
-        return true;
-    };
-    int j = 0;
+    constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);     // A = P (TMEM), B = V (MN-major)
+    int nk = 0, nv = 0, nq = 0, npv = 0, nunits = 0;   // K, V, Q consumed; PV tiles; units with tiles
     bool ok = true;
-    while (w.next()) {
-        if (j == 0 && !wait(bars.q_full, 0, kSiteQ)) { ok = false; break; }
-        const int st = j % C::NS, sb = j & 1;
-        if (!wait(bars.k_full[st], (j / C::NS) & 1, kSiteKFull)) { ok = false; break; }
-        if (j >= 2 && !wait(bars.s_free[sb], ((j >> 1) - 1) & 1, kSiteSFree)) { ok = false; break; }
-        tc_fence_after();
+    auto issue_qk = [&](int i, int kst) {
+        const uint32_t qb = sQ + i * C::Q_BYTES, kb = sK + kst * C::KV_BYTES;
+        const uint32_t d = tmem + (i ? C::S_COL1 : C::S_COL0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-            mma_bf16_ss(tmem + (sb ? 128u : 0u), desc_sw128(sQ + off, 16, 1024),
-                        desc_sw128(sK + st * C::KV_BYTES + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+            mma_bf16_ss(d, desc_sw128(qb + off, 16, 1024), desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bars.s_full[sb]);
-        mma_commit(bars.k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
-        ++j;
+        mma_commit(bars.s_full(i));
+    };
+    auto issue_pv = [&](int i, int vst, bool first) {
+        const uint32_t vb = sV + vst * C::KV_BYTES;
+        const uint32_t d = tmem + (i ? C::O_COL1 : C::O_COL0), a = tmem + (i ? C::S_COL1 : C::S_COL0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)       // 128 keys, 16 per MMA; P_i packs 2 keys per column
+            mma_bf16_ts(d, a + kk * 8, desc_sw128(vb + kk * 2048, C::PANEL_BYTES, 1024), kIdescPV,
+                        (!first || kk > 0) ? 1u : 0u);
+        mma_commit(bars.pv_done(i));
+    };
+    for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        if (!wait(bars.unit_full(slot), (it >> 1) & 1, kSiteUnitFull)) { ok = false; break; }
+        const int u = unit_slot[slot];
+        mbar_arrive(bars.unit_empty(slot));
+        if (u < 0) break;
+        const Unit U = decode_unit(P, u);
+        TileWalk w;
+        w.init(P, U);
+        if (!w.next()) continue;                       // nothing visible for this unit
+        if (!wait(bars.q_full(), nq & 1, kSiteQ)) { ok = false; break; }
+        int kst = nk % C::NS;
+        if (!wait(bars.k_full(kst), (nk / C::NS) & 1, kSiteKFull)) { ok = false; break; }
+        tc_fence_after();
+        issue_qk(0, kst);
+        issue_qk(1, kst);
+        mma_commit(bars.k_empty(kst));
+        ++nk;
+        for (int j = 0; ok; ++j) {
+            const bool nxt = w.next();
+            const int vst = nv % C::NS;
+            // query tile 0: PV_0(j), then QK_0(j+1)
+            if (!wait(bars.p_full(0), npv & 1, kSitePFull)) { ok = false; break; }
+            if (j == 0 && nunits >= 1 && !wait(bars.o_free(0), (nunits - 1) & 1, kSiteOFree)) { ok = false; break; }
+            if (!wait(bars.v_full(vst), (nv / C::NS) & 1, kSiteVFull)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(0, vst, j == 0);
+            if (nxt) {
+                kst = nk % C::NS;
+                if (!wait(bars.k_full(kst), (nk / C::NS) & 1, kSiteKFull)) { ok = false; break; }
+                tc_fence_after();
+                issue_qk(0, kst);
+            }
+            // query tile 1: PV_1(j), then QK_1(j+1)
+            if (!wait(bars.p_full(1), npv & 1, kSitePFull)) { ok = false; break; }
+            if (j == 0 && nunits >= 1 && !wait(bars.o_free(1), (nunits - 1) & 1, kSiteOFree)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(1, vst, j == 0);
+            mma_commit(bars.v_empty(vst));
+            ++nv;
+            if (nxt) {
+                issue_qk(1, kst);
+                mma_commit(bars.k_empty(kst));
+                ++nk;
+            }
+            ++npv;
+            if (!nxt) break;
+        }
+        if (!ok) break;
+        mma_commit(bars.q_empty());        // every QK of this unit has been issued
+        ++nq;
+        ++nunits;
     }
-    if (ok && j >= 1) issue_pv(j - 1);
     // Drain: every MMA this thread issued has completed before tensor memory is freed.
-    mma_commit(bars.mma_done);
-    wait(bars.mma_done, 0, kSiteDrain, false);
+    mma_commit(bars.mma_done());
+    wait(bars.mma_done(), 0, kSiteDrain, false);
 }
 
+// ---------------------------------------------------------------------------------------------
+// warps 4..11: softmax and epilogue, warpgroup i for query tile i, one thread per row
+// ---------------------------------------------------------------------------------------------
 template <int D>
-__device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, const Bars<D>& bars,
-                                 const Waiter& wait, int r, int qt, int b, int head, int2 qmm) {
+__device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* unit_slot, const Bars<D>& bars,
+                                 const Waiter& wait) {
     using C = Cfg<D>;
+    const int wg = (threadIdx.x >> 5) >= 8 ? 1 : 0;
     const int quarter = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-    const int row = quarter * 32 + lane;                 // TMEM lane = query row of the tile
+    const int row = quarter * 32 + lane;                        // TMEM lane = query row of the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int64_t jl = (int64_t)qt * 128 + row;          // local index on rank r
-    const bool row_valid = jl < P.n;
-    const int qpos = row_valid ? __ldg(P.posL + (int64_t)r * P.n + jl) : 0;
-    // l: sum of the fp32 exponentials (for lse); lr: sum of the same values rounded to bf16 as the
-    // PV product sees them (for the normalisation of O, so its weights sum to one exactly).
-    float m_used = -INFINITY, l = 0.f, lr = 0.f;
-    TileWalk w;
-    w.init(P, r, qmm);
-    int j = 0;
+    const uint32_t s_col = wg ? C::S_COL1 : C::S_COL0, o_col = wg ? C::O_COL1 : C::O_COL0;
+    const uint64_t scale2 = f2_pack(P.scale_log2, P.scale_log2);
+    int ntile = 0;   // tiles processed by this warpgroup
     bool ok = true;
-    float x[128];
-    const bool counter = (row == 0);                    // one thread tallies computed tiles
-    int cnt_s = -1;
-    unsigned long long cnt_full = 0, cnt_diag = 0;
-    auto flush = [&]() {
-        if (counter && cnt_s >= 0) {
-            unsigned long long* c = P.counts + ((size_t)r * P.n_cp + cnt_s) * 2;
-            if (cnt_full) atomicAdd(c, cnt_full);
-            if (cnt_diag) atomicAdd(c + 1, cnt_diag);
-        }
-        cnt_full = cnt_diag = 0;
-    };
-    while (w.next()) {
-        const int sb = j & 1;
-        if (w.s != cnt_s) { flush(); cnt_s = w.s; }
-        if (w.diag) ++cnt_diag; else ++cnt_full;
-        ok = __all_sync(0xffffffffu, wait(bars.s_full[sb], (j >> 1) & 1, kSiteSFull));
+    for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        ok = __all_sync(0xffffffffu, wait(bars.unit_full(slot), (it >> 1) & 1, kSiteUnitFull));
         if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t t[32];
-            tmem_ld32(tmem + lane_base + (sb ? 128u : 0u) + c * 32, t);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(t[i]);
-        }
-        tc_fence_before();
-        mbar_arrive(bars.s_free[sb]);
-        if (w.mask) {
-            const int64_t kbase = (int64_t)w.src * P.n + (int64_t)w.kt * 128;
-            const int64_t left = P.n - (int64_t)w.kt * 128;
-            const int kvalid = left < 128 ? (int)left : 128;
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                bool vis = row_valid && c < kvalid;
-                if (vis && P.causal) vis = __ldg(P.posL + kbase + c) <= qpos;
-                if (!vis) x[c] = -INFINITY;
+        const int u = unit_slot[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.unit_empty(slot));
+        if (u < 0) break;
+        const Unit U = decode_unit(P, u);
+        const int head = wg ? U.head[1] : U.head[0];
+        const int qt = wg ? U.qt[1] : U.qt[0];
+        const int member_valid = wg ? U.valid[1] : U.valid[0];
+        const int64_t jl = (int64_t)qt * 128 + row;             // local index on rank r
+        const bool row_valid = member_valid && jl < P.n;
+        const int qpos = row_valid ? __ldg(P.posL + (int64_t)U.r * P.n + jl) : 0;
+        // l: sum of the fp32 exponentials (for lse); lr: the same values rounded to bf16 as the PV
+        // product sees them (normalises O, so the weights applied to V sum to one exactly).
+        float m_used = -INFINITY, l = 0.f, lr = 0.f;
+        const bool counter = (row == 0) && member_valid;       // one thread tallies computed tiles
+        int cnt_s = -1;
+        unsigned long long cnt_full = 0, cnt_diag = 0;
+        auto flush = [&]() {
+            if (counter && cnt_s >= 0) {
+                unsigned long long* c = P.counts + ((size_t)U.r * P.n_cp + cnt_s) * 2;
+                if (cnt_full) atomicAdd(c, cnt_full);
+                if (cnt_diag) atomicAdd(c + 1, cnt_diag);
             }
-        }
-        float mx = x[0];
-#pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-        const float mt = (mx == -INFINITY) ? -INFINITY : mx * P.scale_log2;
-        const float m_new = fmaxf(m_used, mt);
-        const bool resc = m_new > m_used + 8.0f;
-        float alpha = 1.0f;
-        if (resc) {
-            alpha = ex2(m_used - m_new);
-            l *= alpha;
-            lr *= alpha;
-            m_used = m_new;
-        }
-        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        // P is rounded to bf16 for the PV product; the row sum adds the same rounded values, so
-        // the weights O / l applies are exactly the ones the tensor core multiplied.
-        uint32_t pk[64];
-        float rs = 0.f, rsr = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const float p0 = ex2(fmaf(x[2 * c], P.scale_log2, -msub));
-            const float p1 = ex2(fmaf(x[2 * c + 1], P.scale_log2, -msub));
-            pk[c] = pack_bf16(p0, p1);
-            rs += p0 + p1;
-            rsr += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
-        }
-        l += rs;
-        lr += rsr;
-        if (j > 0) {   // PV of the previous tile done: the P buffer is free and O is stable
-            ok = __all_sync(0xffffffffu, wait(bars.pv_done, (j - 1) & 1, kSitePvDone));
+            cnt_full = cnt_diag = 0;
+        };
+        TileWalk w;
+        w.init(P, U);
+        int j = 0;
+        while (w.next()) {
+            if (w.s != cnt_s) { flush(); cnt_s = w.s; }
+            const int cls = w.cls(wg);
+            if (cls == CPATTN_TILE_DIAG) ++cnt_diag;
+            else if (cls == CPATTN_TILE_FULL) ++cnt_full;
+            ok = __all_sync(0xffffffffu, wait(bars.s_full(wg), ntile & 1, kSiteSFull));
             if (!ok) break;
             tc_fence_after();
-            if (__any_sync(0xffffffffu, resc)) {
+            uint32_t sr[128];
+            tmem_ld128(tmem + lane_base + s_col, sr);
+            float x[128];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+            if (w.mask(wg)) {
+                const int64_t kbase = (int64_t)w.src * P.n + (int64_t)w.kt * 128;
+                const int64_t left = P.n - (int64_t)w.kt * 128;
+                const int kvalid = (cls == CPATTN_TILE_SKIP) ? 0 : (left < 128 ? (int)left : 128);
+                // 16 keys at a time; the empty asm keeps the position loads of later chunks from
+                // being hoisted (128 live loads would double the register footprint).
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 16) {
+                    int kp[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.posL + kbase + c0 + c) : INT_MIN;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos;
+                        if (!vis) x[c0 + c] = -INFINITY;
+                    }
+                    asm volatile("" ::: "memory");
+                }
+            }
+            float mx = max3(x[0], x[1], x[2]);
+#pragma unroll
+            for (int c = 3; c < 127; c += 2) mx = max3(mx, x[c], x[c + 1]);
+            mx = fmaxf(mx, x[127]);
+            const float mt = (mx == -INFINITY) ? -INFINITY : mx * P.scale_log2;
+            const float m_new = fmaxf(m_used, mt);
+            const bool resc = m_new > m_used + 8.0f;
+            float alpha = 1.0f;
+            if (resc) {
+                alpha = ex2(m_used - m_new);
+                l *= alpha;
+                lr *= alpha;
+                m_used = m_new;
+            }
+            const float msub = (m_used == -INFINITY) ? 0.f : -m_used;
+            const uint64_t neg_m2 = f2_pack(msub, msub);
+            uint32_t pk[64];
+            uint64_t sum2 = 0, sumr2 = 0;   // packed pairs of +0.0f
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                float a0, a1;
+                f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), scale2, neg_m2), a0, a1);
+                const float p0 = ex2(a0), p1 = ex2(a1);
+                pk[c] = pack_bf16(p0, p1);
+                sum2 = f2_add(sum2, f2_pack(p0, p1));
+                sumr2 = f2_add(sumr2, f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
+            }
+            float s0, s1, r0, r1;
+            f2_unpack(sum2, s0, s1);
+            f2_unpack(sumr2, r0, r1);
+            l += s0 + s1;
+            lr += r0 + r1;
+            // P_i over the first 64 columns of S_i: column c holds keys 2c (low half) and 2c + 1.
+            tmem_st64(tmem + lane_base + s_col, pk);
+            if (j > 0 && __any_sync(0xffffffffu, resc)) {
+                // O_i holds the PVs of earlier tiles: wait for the last one, then rescale in place.
+                ok = __all_sync(0xffffffffu, wait(bars.pv_done(wg), (ntile - 1) & 1, kSitePvDone));
+                if (!ok) {
+                    tmem_st_wait();
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t t[32];
-                    const uint32_t ta = tmem + lane_base + C::O_COL + c * 32;
+                    const uint32_t ta = tmem + lane_base + o_col + c * 32;
                     tmem_ld32(ta, t);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+                    for (int q = 0; q < 32; ++q) t[q] = __float_as_uint(__uint_as_float(t[q]) * alpha);
                     tmem_st32(ta, t);
                 }
-                tmem_st_wait();
             }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.p_full(wg));
+            ++ntile;
+            ++j;
         }
-        // P as bf16, K-major with the 128-byte swizzle: two panels of 64 keys, row = 128 bytes.
-#pragma unroll
-        for (int g8 = 0; g8 < 16; ++g8) {
-            const int pn = g8 >> 3, cc = g8 & 7;
-            const uint32_t addr = sP + pn * C::PANEL_BYTES + row * 128 + (((cc ^ (row & 7)) & 7) << 4);
-            st_shared_v4(addr, pk[4 * g8 + 0], pk[4 * g8 + 1], pk[4 * g8 + 2], pk[4 * g8 + 3]);
+        flush();
+        if (!ok) break;
+        if (j == 0 && !P.fused && P.step > 0) continue;    // nothing visible at this step
+        if (j > 0) {
+            ok = __all_sync(0xffffffffu, wait(bars.pv_done(wg), (ntile - 1) & 1, kSitePvDone));
+            if (!ok) break;
+            tc_fence_after();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bars.p_full);
-        ++j;
-    }
-    flush();
-    if (!ok) return;
-    if (j > 0) {
-        ok = __all_sync(0xffffffffu, wait(bars.pv_done, (j - 1) & 1, kSitePvDone));
-        if (!ok) return;
-        tc_fence_after();
-    } else if (!P.fused && P.step > 0) {
-        return;   // nothing visible at this step: the running state is unchanged
-    }
-    const float inv_l = lr > 0.f ? 1.0f / lr : 0.f;
-    const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    if (P.fused) {
-        int64_t tn = 0;
-        if (P.layout == CPATTN_CONTIGUOUS) tn = (int64_t)r * P.n + jl;
-        else if (P.layout == CPATTN_ZIGZAG) tn = jl < P.m ? (int64_t)r * P.m + jl : (int64_t)(2 * P.n_cp - 1 - r) * P.m + (jl - P.m);
-        else tn = jl * P.n_cp + r;
-        uint4* dst = reinterpret_cast<uint4*>(P.o + (((int64_t)b * P.T + tn) * P.h + head) * D);
+        const float inv_l = lr > 0.f ? 1.0f / lr : 0.f;
+        const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        // Output in 32-column chunks of O_i (bounded register use while loading and storing).
+        uint4* dst = nullptr;                 // fused: bf16 row in natural order
+        float4* orun = nullptr;               // ring step: fp32 running row in layout order
+        int64_t base = 0;
+        float wa = 0.f, wb = inv_l, L = lse_v;
+        const bool first = (P.step == 0);
+        if (P.fused) {
+            int64_t tn;
+            if (P.layout == CPATTN_CONTIGUOUS) tn = (int64_t)U.r * P.n + jl;
+            else if (P.layout == CPATTN_ZIGZAG)
+                tn = jl < P.m ? (int64_t)U.r * P.m + jl : (int64_t)(2 * P.n_cp - 1 - U.r) * P.m + (jl - P.m);
+            else tn = jl * P.n_cp + U.r;
+            if (row_valid) {
+                dst = reinterpret_cast<uint4*>(P.o + (((int64_t)U.b * P.T + tn) * P.h + head) * D);
+                P.lse[((int64_t)U.b * P.h + head) * P.T + tn] = lse_v;
+            }
+        } else if (row_valid) {
+            base = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n + jl;
+            orun = reinterpret_cast<float4*>(P.o_run + base * D);
+            if (!first) {
+                const float la = P.lse_run[base];
+                const float M = fmaxf(la, lse_v);
+                if (M == -INFINITY) {
+                    wb = 0.f;
+                    L = -INFINITY;
+                } else {
+                    L = M + logf(expf(la - M) + expf(lse_v - M));
+                    wa = expf(la - L);
+                    wb = expf(lse_v - L) * inv_l;
+                }
+            }
+            P.lse_run[base] = L;
+        }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-            uint32_t t[32];
-            if (j > 0) tmem_ld32(tmem + lane_base + C::O_COL + c * 32, t);
-            else {
+            uint32_t ot[32];
+            if (j > 0) {
+                tmem_ld32(tmem + lane_base + o_col + c * 32, ot);
+            } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) t[i] = 0u;
+                for (int q = 0; q < 32; ++q) ot[q] = 0u;
             }
-            if (row_valid) {
+            if (dst) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint4 v;
-                    v.x = pack_bf16(__uint_as_float(t[8 * q4 + 0]) * inv_l, __uint_as_float(t[8 * q4 + 1]) * inv_l);
-                    v.y = pack_bf16(__uint_as_float(t[8 * q4 + 2]) * inv_l, __uint_as_float(t[8 * q4 + 3]) * inv_l);
-                    v.z = pack_bf16(__uint_as_float(t[8 * q4 + 4]) * inv_l, __uint_as_float(t[8 * q4 + 5]) * inv_l);
-                    v.w = pack_bf16(__uint_as_float(t[8 * q4 + 6]) * inv_l, __uint_as_float(t[8 * q4 + 7]) * inv_l);
+                    v.x = pack_bf16(__uint_as_float(ot[8 * q4 + 0]) * inv_l, __uint_as_float(ot[8 * q4 + 1]) * inv_l);
+                    v.y = pack_bf16(__uint_as_float(ot[8 * q4 + 2]) * inv_l, __uint_as_float(ot[8 * q4 + 3]) * inv_l);
+                    v.z = pack_bf16(__uint_as_float(ot[8 * q4 + 4]) * inv_l, __uint_as_float(ot[8 * q4 + 5]) * inv_l);
+                    v.w = pack_bf16(__uint_as_float(ot[8 * q4 + 6]) * inv_l, __uint_as_float(ot[8 * q4 + 7]) * inv_l);
                     dst[c * 4 + q4] = v;
                 }
-            }
-        }
-        if (row_valid) P.lse[((int64_t)b * P.h + head) * P.T + tn] = lse_v;
-    } else {
-        const int64_t base = (((int64_t)r * P.B + b) * P.h + head) * P.n + jl;
-        float4* orun = reinterpret_cast<float4*>(P.o_run + base * D);
-        float wa = 0.f, wb = 1.f, L = lse_v;
-        const bool first = (P.step == 0);
-        if (row_valid && !first) {
-            const float la = P.lse_run[base];
-            const float M = fmaxf(la, lse_v);
-            if (M == -INFINITY) { wa = 0.f; wb = 0.f; L = -INFINITY; }
-            else {
-                L = M + logf(expf(la - M) + expf(lse_v - M));
-                wa = expf(la - L);
-                wb = expf(lse_v - L);
-            }
-        }
-        wb *= inv_l;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t t[32];
-            if (j > 0) tmem_ld32(tmem + lane_base + C::O_COL + c * 32, t);
-            else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) t[i] = 0u;
-            }
-            if (row_valid) {
+            } else if (orun) {
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
-                    float4 ob = make_float4(__uint_as_float(t[4 * q4]) * wb, __uint_as_float(t[4 * q4 + 1]) * wb,
-                                            __uint_as_float(t[4 * q4 + 2]) * wb, __uint_as_float(t[4 * q4 + 3]) * wb);
+                    float4 ob = make_float4(__uint_as_float(ot[4 * q4]) * wb, __uint_as_float(ot[4 * q4 + 1]) * wb,
+                                            __uint_as_float(ot[4 * q4 + 2]) * wb, __uint_as_float(ot[4 * q4 + 3]) * wb);
                     if (!first) {
                         const float4 oa = orun[c * 8 + q4];
                         ob.x += wa * oa.x; ob.y += wa * oa.y; ob.z += wa * oa.z; ob.w += wa * oa.w;
@@ -449,33 +607,31 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, uint32_t sP, co
                 }
             }
         }
-        if (row_valid) P.lse_run[base] = L;
+        if (j > 0) {
+            tc_fence_before();
+            mbar_arrive(bars.o_free(wg));                 // O_i has been read: the next unit may overwrite it
+        }
     }
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     ring_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params P) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V, sP = sbase + C::OFF_P;
+    const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-    Bars<D> bars;
-    bars.setup(sbase + C::OFF_BAR);
+    volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 16);   // [2]
+    const Bars<D> bars{sbase + C::OFF_BAR};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int bhn = P.B * P.h;
-    const int rq = __ldg(P.order + blockIdx.x / bhn);
-    const int r = rq / P.n_qt, qt = rq % P.n_qt;
-    const int bh = blockIdx.x % bhn, b = bh / P.h, head = bh % P.h, kvh = head / P.g;
-    const int2 qmm = __ldg(P.tile_mm + rq);
-    // A unit that starts after another one recorded a device error does no work (the decision
-    // is taken by one thread and shared, so the whole block leaves together).
-    volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    // A CTA that starts after a device error was recorded does no work (one thread decides for
+    // the whole block).
     if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
     __syncthreads();
     if (*skip_flag) return;
@@ -500,12 +656,13 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tmem = *tmem_slot;
     const Waiter wait{abort_flag, P.header, P.timeout_ns};
 
-    if (warp == 0) {
-        if (lane == 0) producer<D>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, bars, wait, r, qt, b, head, kvh, qmm);
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer<D>(P, tmem, sQ, sK, sV, sP, bars, wait, r, qmm);
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) producer<D>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
+        if (warp == 1 && lane == 0) mma_issuer<D>(P, tmem, sQ, sK, sV, unit_slot, bars, wait);
     } else {
-        softmax_epilogue<D>(P, tmem, sP, bars, wait, r, qt, b, head, qmm);
+        setmaxnreg_inc<kRegsHigh>();
+        softmax_epilogue<D>(P, tmem, unit_slot, bars, wait);
     }
     tc_fence_before();
     __syncthreads();
@@ -563,13 +720,17 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int d) {
 template <int D>
 int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     using C = Cfg<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
-        attr_set = true;
+        attr_dev = dev;
     }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     CUtensorMap tq, tk, tv;
     const uint64_t qrows = (uint64_t)a.n_cp * a.B * a.h * a.n, kvrows = (uint64_t)a.n_cp * a.B * a.n_kv * a.n;
     if (!make_map(&tq, a.qL, qrows, D) || !make_map(&tk, a.kv_k, kvrows, D) || !make_map(&tv, a.kv_v, kvrows, D)) {
@@ -577,15 +738,22 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
         return (int)cudaErrorInvalidValue;
     }
     Params P{};
-    P.B = a.B; P.h = a.h; P.n_kv = a.n_kv; P.g = a.h / a.n_kv; P.n_cp = a.n_cp; P.n_qt = a.n_qt; P.causal = a.causal;
+    P.B = a.B; P.h = a.h; P.n_kv = a.n_kv; P.g = a.h / a.n_kv; P.n_cp = a.n_cp; P.n_qt = a.n_qt;
+    P.n_grp = a.n_grp; P.pair_heads = a.pair_heads; P.causal = a.causal;
     P.fused = a.fused; P.step = a.step; P.kv_by_holder = a.kv_by_holder; P.layout = a.layout;
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int2*>(a.tile_mm); P.order = a.order;
-    P.counts = a.counts;
+    P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
     P.header = a.header; P.timeout_ns = a.timeout_ns;
-    const int64_t units = (int64_t)a.n_cp * a.n_qt * a.B * a.h;
-    ring_attention_kernel<D><<<(unsigned)units, 192, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
+    const int64_t units = (int64_t)a.n_cp * a.n_grp * a.B * (a.pair_heads ? a.h / 2 : a.h);
+    if (units > INT_MAX) {
+        *why = "too many work units";
+        return (int)cudaErrorInvalidValue;
+    }
+    P.num_units = (int)units;
+    const int grid = (int)(units < sms ? units : sms);
+    ring_attention_kernel<D><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ struct WsLayout {
     size_t tile_mm = 0;     // int32x2 [n_cp][n_qt]: min and max position of each tile
     size_t order = 0;       // int32 [n_cp * n_qt]: (rank, q-tile) pairs, longest first
     size_t counts = 0;      // uint64 [n_cp][n_cp][2]: tiles computed per (rank, step), FULL / DIAG
+    size_t sched = 0;       // uint32 [1 + n_cp]: work counters of the persistent kernel (fused, each step)
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
@@ -40,7 +41,9 @@ struct Plan {
     int64_t T = 0, n = 0, m = 0;   // tokens, tokens per rank, zigzag chunk
     int h = 0, n_kv = 0, d = 0, n_cp = 0, layout = 0, causal = 0;
     int n_qt = 0;                   // tiles per rank block (query and key tiles have one size)
-    std::vector<int32_t> order;     // (r * n_qt + qt), longest first
+    int pair_heads = 0;             // a CTA pairs two heads of one KV group (else two adjacent q-tiles)
+    int n_grp = 0;                  // row groups per rank: n_qt when pairing heads, ceil(n_qt / 2) otherwise
+    std::vector<int32_t> order;     // (r * n_grp + group), longest first
     std::vector<int64_t> full, diag, skip;  // [n_cp][n_cp] by (rank, step), per (b, head)
     std::vector<int64_t> pairs;             // [n_cp]
     std::vector<int64_t> half_units;        // [n_cp]
@@ -64,7 +67,8 @@ struct PermuteArgs {
 int launch_permute(const PermuteArgs& a, void* stream);
 
 struct AttnLaunch {
-    int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt;
+    int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt, pair_heads, n_grp;
+    uint32_t* sched;  // work counter of this launch (zeroed before the launch)
     float scale_log2;
     int fused;        // 1: all ring steps, natural-order bf16 output; 0: one step, merge into running state
     int step;         // ring step (fused == 0)

@@ -34,6 +34,7 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.tile_mm = take(sizeof(int32_t) * 2 * (size_t)p.n_cp * p.n_qt);
     w.order = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
     w.counts = take(sizeof(uint64_t) * 2 * (size_t)p.n_cp * p.n_cp);
+    w.sched = take(sizeof(uint32_t) * (1 + (size_t)p.n_cp));
     w.qL = take(2 * (size_t)B * T * p.h * d);
     w.kL = take(2 * (size_t)B * T * p.n_kv * d);
     w.vL = take(2 * (size_t)B * T * p.n_kv * d);
@@ -83,7 +84,11 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
     p.full.assign((size_t)n_cp * n_cp, 0);
     p.diag.assign((size_t)n_cp * n_cp, 0);
     p.skip.assign((size_t)n_cp * n_cp, 0);
-    std::vector<int64_t> work((size_t)n_cp * p.n_qt, 0);   // computed tiles per (rank, q-tile)
+    // A CTA computes two 128-row query tiles against each key tile: two heads of one KV group
+    // when the group size is even, else two adjacent query tiles of one head.
+    p.pair_heads = ((h / n_kv) % 2 == 0) ? 1 : 0;
+    p.n_grp = p.pair_heads ? p.n_qt : (p.n_qt + 1) / 2;
+    std::vector<int64_t> work((size_t)n_cp * p.n_grp, 0);  // key tiles a row group computes
     for (int r = 0; r < n_cp; ++r)
         for (int s = 0; s < n_cp; ++s) {
             int src = ((r - s) % n_cp + n_cp) % n_cp;
@@ -96,7 +101,18 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
                     if (c == CPATTN_TILE_FULL) ++p.full[rs];
                     else if (c == CPATTN_TILE_DIAG) ++p.diag[rs];
                     else ++p.skip[rs];
-                    if (c != CPATTN_TILE_SKIP) ++work[qi];
+                }
+            }
+            for (int grp = 0; grp < p.n_grp; ++grp) {
+                const int q0 = p.pair_heads ? grp : 2 * grp;
+                const int q1 = p.pair_heads ? grp : std::min(2 * grp + 1, p.n_qt - 1);
+                for (int kt = 0; kt < p.n_qt; ++kt) {
+                    size_t ki = (size_t)src * p.n_qt + kt;
+                    int c0 = classify(p.causal, tmin[(size_t)r * p.n_qt + q0], tmax[(size_t)r * p.n_qt + q0],
+                                      tmin[ki], tmax[ki]);
+                    int c1 = classify(p.causal, tmin[(size_t)r * p.n_qt + q1], tmax[(size_t)r * p.n_qt + q1],
+                                      tmin[ki], tmax[ki]);
+                    if (c0 != CPATTN_TILE_SKIP || c1 != CPATTN_TILE_SKIP) ++work[(size_t)r * p.n_grp + grp];
                 }
             }
         }
@@ -134,7 +150,7 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
         }
     }
     // longest-first order of (rank, q-tile): the block scheduler starts the heaviest units first
-    p.order.resize((size_t)n_cp * p.n_qt);
+    p.order.resize((size_t)n_cp * p.n_grp);
     std::iota(p.order.begin(), p.order.end(), 0);
     std::stable_sort(p.order.begin(), p.order.end(), [&](int32_t a, int32_t b) { return work[a] > work[b]; });
     return "";
