@@ -56,7 +56,7 @@ struct Params {
     int64_t n, m, T;
     float scale_log2;
     const int32_t* posL;
-    const int2* tile_mm;
+    const int4* tile_mm;
     const int32_t* order;
     unsigned long long* counts;
     uint32_t* sched;
@@ -162,45 +162,54 @@ struct Unit {
     int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
 };
 
+// Units are numbered KV-head-major: all units of one (batch element, KV head) come before the
+// next, so the CTAs running at any moment read the keys and values of one or two KV heads and
+// those stay in L2. Within a KV head, (rank, row group) follow the plan's longest-first order,
+// then the query heads of the group.
 __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
     Unit U;
+    const int per = P.pair_heads ? P.g / 2 : P.g;        // units per (b, kvh, row group)
+    const int n_rg = P.n_cp * P.n_grp;
+    const int pp = u % per;
+    const int t = u / per;
+    const int rgi = t % n_rg;
+    const int bk = t / n_rg;
+    U.kvh = bk % P.n_kv;
+    U.b = bk / P.n_kv;
+    const int rg = __ldg(P.order + rgi);
+    U.r = rg / P.n_grp;
+    const int grp = rg % P.n_grp;
     if (P.pair_heads) {
-        const int hp = P.h / 2, per = P.B * hp;
-        const int rg = __ldg(P.order + u / per);
-        U.r = rg / P.n_grp;
-        const int qt = rg % P.n_grp;
-        const int rem = u % per;
-        U.b = rem / hp;
-        U.head[0] = 2 * (rem % hp);
+        U.head[0] = U.kvh * P.g + 2 * pp;
         U.head[1] = U.head[0] + 1;
-        U.qt[0] = U.qt[1] = qt;
+        U.qt[0] = U.qt[1] = grp;
         U.valid[0] = U.valid[1] = 1;
     } else {
-        const int per = P.B * P.h;
-        const int rg = __ldg(P.order + u / per);
-        U.r = rg / P.n_grp;
-        const int grp = rg % P.n_grp;
-        const int rem = u % per;
-        U.b = rem / P.h;
-        U.head[0] = U.head[1] = rem % P.h;
+        U.head[0] = U.head[1] = U.kvh * P.g + pp;
         U.qt[0] = 2 * grp;
         U.qt[1] = 2 * grp + 1;
         U.valid[0] = 1;
         U.valid[1] = U.qt[1] < P.n_qt;
     }
-    U.kvh = U.head[0] / P.g;
-    for (int i = 0; i < 2; ++i)
-        U.qmm[i] = U.valid[i] ? __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]) : make_int2(INT_MAX, INT_MIN);
+    for (int i = 0; i < 2; ++i) {
+        if (U.valid[i]) {
+            const int4 t4 = __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]);
+            U.qmm[i] = make_int2(t4.x, t4.y);
+        } else {
+            U.qmm[i] = make_int2(INT_MAX, INT_MIN);
+        }
+    }
     return U;
 }
 
 // The key tiles a unit visits, in ring order, leaving out tiles that both query tiles skip.
-// cls[i]: FULL / DIAG / SKIP for query tile i; mask[i]: the tile needs the element mask for
-// query tile i (partly visible, skipped by this tile only, or shorter than 128 keys).
+// cls(i): FULL / DIAG / SKIP for query tile i; mask(i): the tile needs the element mask for
+// query tile i (partly visible, skipped by this tile only, or shorter than 128 keys). A block
+// whose remaining tiles all start after every query of the unit is left in one step.
 struct TileWalk {
     const Params* p;
     int r, s, s_end, kt, src;
-    int qmin0, qmax0, qmin1, qmax1, cls0, cls1, mask0, mask1;
+    int qmin0, qmax0, qmin1, qmax1, qmax, cls0, cls1, mask0, mask1;
     __device__ int cls(int i) const { return i ? cls1 : cls0; }
     __device__ int mask(int i) const { return i ? mask1 : mask0; }
     __device__ void init(const Params& P, const Unit& U) {
@@ -208,6 +217,7 @@ struct TileWalk {
         r = U.r;
         qmin0 = U.qmm[0].x; qmax0 = U.qmm[0].y;
         qmin1 = U.qmm[1].x; qmax1 = U.qmm[1].y;
+        qmax = max(qmax0, qmax1);
         s = P.fused ? 0 : P.step;
         s_end = P.fused ? P.n_cp : P.step + 1;
         kt = -1;
@@ -227,9 +237,13 @@ struct TileWalk {
                 mask0 = mask1 = short_tile;
                 return true;
             }
-            const int2 kmm = __ldg(P.tile_mm + src * P.n_qt + kt);
-            cls0 = (kmm.x > qmax0) ? CPATTN_TILE_SKIP : (kmm.y > qmin0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
-            cls1 = (kmm.x > qmax1) ? CPATTN_TILE_SKIP : (kmm.y > qmin1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            const int4 t4 = __ldg(P.tile_mm + src * P.n_qt + kt);
+            if (t4.z > qmax) {           // this tile and every later one of the block: skipped
+                kt = P.n_qt - 1;
+                continue;
+            }
+            cls0 = (t4.x > qmax0) ? CPATTN_TILE_SKIP : (t4.y > qmin0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            cls1 = (t4.x > qmax1) ? CPATTN_TILE_SKIP : (t4.y > qmin1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
             if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
             mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
             mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
@@ -441,11 +455,15 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         TileWalk w;
         w.init(P, U);
         int j = 0;
-        while (w.next()) {
+        bool have = w.next();
+        while (have) {
+            // This tile's walk state; the walk moves on to the next tile right away so its table
+            // load overlaps the work below.
+            const int cls = w.cls(wg), tmask = w.mask(wg), tsrc = w.src, tkt = w.kt;
             if (w.s != cnt_s) { flush(); cnt_s = w.s; }
-            const int cls = w.cls(wg);
             if (cls == CPATTN_TILE_DIAG) ++cnt_diag;
             else if (cls == CPATTN_TILE_FULL) ++cnt_full;
+            have = w.next();
             ok = __all_sync(0xffffffffu, wait(bars.s_full(wg), ntile & 1, kSiteSFull));
             if (!ok) break;
             tc_fence_after();
@@ -454,9 +472,9 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             float x[128];
 #pragma unroll
             for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-            if (w.mask(wg)) {
-                const int64_t kbase = (int64_t)w.src * P.n + (int64_t)w.kt * 128;
-                const int64_t left = P.n - (int64_t)w.kt * 128;
+            if (tmask) {
+                const int64_t kbase = (int64_t)tsrc * P.n + (int64_t)tkt * 128;
+                const int64_t left = P.n - (int64_t)tkt * 128;
                 const int kvalid = (cls == CPATTN_TILE_SKIP) ? 0 : (left < 128 ? (int)left : 128);
                 // 16 keys at a time; the empty asm keeps the position loads of later chunks from
                 // being hoisted (128 live loads would double the register footprint).
@@ -474,10 +492,18 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                     asm volatile("" ::: "memory");
                 }
             }
-            float mx = max3(x[0], x[1], x[2]);
+            // Row max over four independent chains (short dependency chains).
+            float mq[4];
 #pragma unroll
-            for (int c = 3; c < 127; c += 2) mx = max3(mx, x[c], x[c + 1]);
-            mx = fmaxf(mx, x[127]);
+            for (int q = 0; q < 4; ++q) mq[q] = x[q];
+#pragma unroll
+            for (int c = 4; c < 124; c += 8) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mq[q] = max3(mq[q], x[c + 2 * q], x[c + 2 * q + 1]);
+            }
+            mq[0] = max3(mq[0], x[124], x[125]);
+            mq[1] = max3(mq[1], x[126], x[127]);
+            const float mx = max3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
             const float mt = (mx == -INFINITY) ? -INFINITY : mx * P.scale_log2;
             const float m_new = fmaxf(m_used, mt);
             const bool resc = m_new > m_used + 8.0f;
@@ -491,19 +517,20 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             const float msub = (m_used == -INFINITY) ? 0.f : -m_used;
             const uint64_t neg_m2 = f2_pack(msub, msub);
             uint32_t pk[64];
-            uint64_t sum2 = 0, sumr2 = 0;   // packed pairs of +0.0f
+            uint64_t sum2[4] = {0, 0, 0, 0}, sumr2[4] = {0, 0, 0, 0};   // packed pairs of +0.0f
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 float a0, a1;
                 f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), scale2, neg_m2), a0, a1);
                 const float p0 = ex2(a0), p1 = ex2(a1);
                 pk[c] = pack_bf16(p0, p1);
-                sum2 = f2_add(sum2, f2_pack(p0, p1));
-                sumr2 = f2_add(sumr2, f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
+                sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
+                sumr2[c & 3] =
+                    f2_add(sumr2[c & 3], f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
             }
             float s0, s1, r0, r1;
-            f2_unpack(sum2, s0, s1);
-            f2_unpack(sumr2, r0, r1);
+            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s0, s1);
+            f2_unpack(f2_add(f2_add(sumr2[0], sumr2[1]), f2_add(sumr2[2], sumr2[3])), r0, r1);
             l += s0 + s1;
             lr += r0 + r1;
             // P_i over the first 64 columns of S_i: column c holds keys 2c (low half) and 2c + 1.
@@ -742,7 +769,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.n_grp = a.n_grp; P.pair_heads = a.pair_heads; P.causal = a.causal;
     P.fused = a.fused; P.step = a.step; P.kv_by_holder = a.kv_by_holder; P.layout = a.layout;
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
-    P.posL = a.posL; P.tile_mm = reinterpret_cast<const int2*>(a.tile_mm); P.order = a.order;
+    P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm); P.order = a.order;
     P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
     P.header = a.header; P.timeout_ns = a.timeout_ns;

@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "internal.h"
@@ -39,7 +40,7 @@ __device__ __forceinline__ int64_t token_of_dev(int layout, int r, int64_t j, in
 
 // One 128-thread block per (rank, tile): position ids in layout order and their min/max.
 __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restrict__ pos, int32_t* __restrict__ posL,
-                                                        int2* __restrict__ tile_mm, int64_t n, int64_t m, int n_cp,
+                                                        int4* __restrict__ tile_mm, int64_t n, int64_t m, int n_cp,
                                                         int layout, int n_qt) {
     const int r = blockIdx.x / n_qt, tile = blockIdx.x % n_qt;
     const int64_t j = (int64_t)tile * kBlockQ + threadIdx.x;
@@ -59,7 +60,21 @@ __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restric
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < 4; ++w) { lo = min(lo, slo[w]); hi = max(hi, shi[w]); }
-        tile_mm[blockIdx.x] = make_int2(lo, hi);
+        tile_mm[blockIdx.x] = make_int4(lo, hi, lo, 0);
+    }
+}
+
+// Per rank block, the minimum position over tiles kt..n_qt-1 (a backward scan): a key walk that
+// finds it above every query position skips the rest of the block in one step.
+__global__ void tile_suffix_kernel(int4* __restrict__ tile_mm, int n_cp, int n_qt) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= n_cp) return;
+    int run = INT_MAX;
+    for (int kt = n_qt - 1; kt >= 0; --kt) {
+        int4 t = tile_mm[(int64_t)r * n_qt + kt];
+        run = min(run, t.x);
+        t.z = run;
+        tile_mm[(int64_t)r * n_qt + kt] = t;
     }
 }
 
@@ -185,9 +200,12 @@ int grid_for(int64_t work, int threads) {
 
 int launch_permute(const PermuteArgs& a, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int2*>(a.tile_mm), a.n, a.m,
+    pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int4*>(a.tile_mm), a.n, a.m,
                                                       a.n_cp, a.layout, a.n_qt);
     int e = (int)cudaGetLastError();
+    if (e) return e;
+    tile_suffix_kernel<<<(a.n_cp + 127) / 128, 128, 0, st>>>(reinterpret_cast<int4*>(a.tile_mm), a.n_cp, a.n_qt);
+    e = (int)cudaGetLastError();
     if (e) return e;
     const int64_t work = (int64_t)a.B * a.T * (a.h + 2 * a.n_kv) * (a.d / 8);
     permute_kernel<<<grid_for(work, 256), 256, 0, st>>>(

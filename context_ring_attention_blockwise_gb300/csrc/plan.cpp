@@ -31,7 +31,7 @@ WsLayout ws_layout(const Plan& p, int B) {
     const size_t T = (size_t)p.T, d = (size_t)p.d;
     w.header = take(sizeof(uint32_t) * kHeaderWords);
     w.posL = take(sizeof(int32_t) * T);
-    w.tile_mm = take(sizeof(int32_t) * 2 * (size_t)p.n_cp * p.n_qt);
+    w.tile_mm = take(sizeof(int32_t) * 4 * (size_t)p.n_cp * p.n_qt);
     w.order = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
     w.counts = take(sizeof(uint64_t) * 2 * (size_t)p.n_cp * p.n_cp);
     w.sched = take(sizeof(uint32_t) * (1 + (size_t)p.n_cp));
