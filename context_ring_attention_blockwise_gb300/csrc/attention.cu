@@ -11,7 +11,8 @@
 // exponentials, running weighted sum of values, rescaled when a larger score arrives.
 //
 // Warp roles (384 threads; registers move from warpgroup 0 to the softmax warpgroups with
-// setmaxnreg: 128 x 56 + 256 x 224 = the 384 x 168 the block is launched with):
+// setmaxnreg: 128 x 112 + 256 x 192 <= the 384 x 168 the block is launched with, checked on the
+// host before the first launch):
 //   warp 0      scheduler + TMA producer: the next unit index into a 2-slot ring; both Q tiles
 //               once per unit; K and V tiles through an NS-deep stage ring, V one tile behind K.
 //   warp 1      owns tensor memory; one lane issues tcgen05.mma. S_i = Q_i K^T (SS form), then
@@ -48,7 +49,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 384;
-constexpr int kRegsLow = 96, kRegsHigh = 200;   // 128 * low + 256 * high <= 384 * 168
+constexpr int kRegsLow = 112, kRegsHigh = 192;   // 128 * 112 + 256 * 192 = 63488 <= 384 * 168
 
 struct Params {
     int B, h, n_kv, g, n_cp, n_qt, n_grp, pair_heads, causal, fused, step, kv_by_holder, layout;
@@ -754,6 +755,16 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
         cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
+        // setmaxnreg.inc waits until enough registers are free in the block's allocation: the
+        // split must fit in what the block is launched with, or the kernel would never proceed.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, ring_attention_kernel<D>);
+        if (e != cudaSuccess) return (int)e;
+        if ((long)fa.numRegs * kThreads < 128L * kRegsLow + 256L * kRegsHigh) {
+            *why = "attention kernel built with " + std::to_string(fa.numRegs) +
+                   " registers per thread, too few for its warpgroup register split";
+            return (int)cudaErrorInvalidConfiguration;
+        }
         attr_dev = dev;
     }
     int sms = 0;

@@ -67,6 +67,9 @@ def compare(o, lse, ref_o, ref_lse, rows=None, what=""):
     over = err > o_tolerance(ref_o)
     if over.any() or el > LSE_TOL:
         idx = np.unravel_index(int(np.argmax(err - o_tolerance(ref_o))), err.shape)
+        le = np.where(fin, np.abs(np.where(fin, lse, 0) - np.where(fin, ref_lse, 0)), 0)
+        li = np.unravel_index(int(np.argmax(le)), le.shape)
+        what += f" [worst lse at (b, head, row) {li}: got {lse[li]:.6f}, exact {ref_lse[li]:.6f}]"
         raise AssertionError(f"{what}: max|dO| = {eo:.3e} ({int(over.sum())} elements over tolerance; worst at "
                              f"{idx}: got {o[idx]:.6f}, exact {ref_o[idx]:.6f}), max|dlse| = {el:.3e} (tol {LSE_TOL})")
     return eo, el
