@@ -32,6 +32,37 @@ METRIC = "ring-attn fwd effective TFLOP/s on 1 GB300; % of dense BF16 tensor pea
 DEFAULT_WORKLOAD = "llama70b_zigzag_T128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) of one attention launch on a workload, from a one-pass ncu capture of
+# dram__bytes_read.sum and dram__bytes_write.sum, keyed by the sha256 prefix of the attention kernel
+# source it was measured on: a changed kernel reports null until it is measured again.
+MEASURED_TRAFFIC = {"c23e79a650b5fd4c": {"llama70b_zigzag_T128k": 5.20e9 + 2.15e9}}
+
+
+def attention_source_hash() -> str:
+    import hashlib
+    path = os.path.join(ROOT, "context_ring_attention_blockwise_gb300", "csrc", "attention.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(workload_name: str):
+    return MEASURED_TRAFFIC.get(attention_source_hash(), {}).get(workload_name)
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """The maximum of `value` over all ranks (the slowest rank sets the job's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank: float, world: int, max_ms_per_step: float) -> float:
+    """Aggregate throughput: the work every rank did in one step over the slowest rank's step time."""
+    return work_per_rank * world / (max_ms_per_step * 1e-3)
+
 
 def flops_eff(w) -> float:
     """4*B*h*d per visible pair; causal pairs counted as T^2/2 (a diagonal block as half)."""
@@ -241,13 +272,9 @@ def run_gpu(args, w):
     if dist is not None:
         dist.barrier()
     cp.check(plan, ws)
-    total_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(t_start.elapsed_time(t_end), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = flops_eff(w) * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(flops_eff(w), world, ms_per_step) / 1e12
     if ring:
         attn_ms = None
         perm_ms = None
@@ -285,11 +312,7 @@ def run_gpu(args, w):
         e2e_step()
     b.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dist, dev)
     h2d = q_h.nbytes + k_h.nbytes + v_h.nbytes
     d2h = op.numel() * 2 + lp.numel() * 4
 
@@ -306,12 +329,13 @@ def run_gpu(args, w):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, args),
             "frac_of_peak": value / world / peak_tf,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": achieved / peak_tf, "traffic": args.traffic,
+                         "frac": achieved / peak_tf,
+                         "traffic": args.traffic if args.traffic is not None else (None if ring else measured_traffic(w.name)),
                          "kernel": "ring_attention_kernel<128>" if not ring else "whole ring-step path",
                          "peak_kind": f"bf16 dense, sustained, {peak_src}",
                          "peak_burst": float(peaks.get("bf16_tflops", 0.0))},
             "kernels_ms": {"permute_and_placement": perm_ms, "attention": attn_ms},
-            "e2e": {"value": flops_eff(w) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_rate(flops_eff(w), world, e2e_ms) / 1e12, "unit": "TFLOP/s",
                     "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
