@@ -97,6 +97,7 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
     a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt; a.pair_heads = p.pair_heads; a.n_grp = p.n_grp;
     a.sched = at<uint32_t>(ws, w.sched);
+    a.unit_tiles = at<int32_t>(ws, w.unit_tiles);
     a.scale_log2 = resolve_scale(p, scale);
     a.qL = at<char>(ws, w.qL);
     a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);
@@ -314,7 +315,7 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
 
 cpattn_status_t cpattn_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts,
                              void* o_bf16, float* lse, cpattn_stream_t stream) {
-    if (S <= 0 || rows <= 0 || h <= 0 || d <= 0 || d % 4) return fail(CPATTN_ERR_INVALID, "S, rows, h > 0 and d a positive multiple of 4 required");
+    if (S <= 0 || rows <= 0 || h <= 0 || d <= 0 || d % 8) return fail(CPATTN_ERR_INVALID, "S, rows, h > 0 and d a positive multiple of 8 required");
     if (!o_parts || !lse_parts || !o_bf16 || !lse) return fail(CPATTN_ERR_INVALID, "NULL pointer");
     if (!aligned16(o_parts) || !aligned16(o_bf16)) return fail(CPATTN_ERR_INVALID, "o_parts and o must be 16-byte aligned");
     int e = cpattn::launch_merge(S, rows, h, d, o_parts, lse_parts, o_bf16, lse, stream);

@@ -16,7 +16,9 @@
 //   warp 0      scheduler + TMA producer: the next unit index into a 2-slot ring; both Q tiles
 //               once per unit; K and V tiles through an NS-deep stage ring, V one tile behind K.
 //   warp 1      owns tensor memory; one lane issues tcgen05.mma. S_i = Q_i K^T (SS form), then
-//               O_i += P_i V with P_i read from tensor memory (TS form).
+//               O_i += P_i V with P_i read from tensor memory (TS form). It takes the number of
+//               key tiles of each unit from a table a small kernel writes before the launch, so
+//               no table lookup of the key walk sits between two of its MMA groups.
 //   warps 2, 3  idle.
 //   warps 4..7  softmax warpgroup 0 (query tile 0), one thread per row.
 //   warps 8..11 softmax warpgroup 1 (query tile 1). Each thread reads its row of S from TMEM,
@@ -59,6 +61,7 @@ struct Params {
     const int32_t* posL;
     const int4* tile_mm;
     const int32_t* order;
+    int32_t* unit_tiles;   // [n_cp * n_grp]: key tiles of a unit of row group r * n_grp + group
     unsigned long long* counts;
     uint32_t* sched;
     uint16_t* o;
@@ -113,9 +116,9 @@ struct Bars {
             mbar_init(unit_full(i), 1);
             mbar_init(unit_empty(i), 1 + 8);          // the MMA lane and one lane per softmax warp
             mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), 128);
+            mbar_init(p_full(i), 4);                  // one lane per softmax warp
             mbar_init(pv_done(i), 1);
-            mbar_init(o_free(i), 128);
+            mbar_init(o_free(i), 4);
         }
         mbar_init(q_full(), 1);
         mbar_init(q_empty(), 1);
@@ -158,7 +161,7 @@ struct Waiter {
 
 // One work unit: rank r, batch element b, and two query tiles (head_i, qt_i) sharing KV head kvh.
 struct Unit {
-    int r, b, kvh;
+    int r, b, kvh, rg;   // rank, batch element, KV head, row group r * n_grp + group
     int head[2], qt[2], valid[2];
     int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
 };
@@ -178,6 +181,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
     U.kvh = bk % P.n_kv;
     U.b = bk / P.n_kv;
     const int rg = __ldg(P.order + rgi);
+    U.rg = rg;
     U.r = rg / P.n_grp;
     const int grp = rg % P.n_grp;
     if (P.pair_heads) {
@@ -358,9 +362,8 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
         mbar_arrive(bars.unit_empty(slot));
         if (u < 0) break;
         const Unit U = decode_unit(P, u);
-        TileWalk w;
-        w.init(P, U);
-        if (!w.next()) continue;                       // nothing visible for this unit
+        const int n_tiles = __ldg(P.unit_tiles + U.rg);
+        if (n_tiles == 0) continue;                    // nothing visible for this unit
         if (!wait(bars.q_full(), nq & 1, kSiteQ)) { ok = false; break; }
         int kst = nk % C::NS;
         if (!wait(bars.k_full(kst), (nk / C::NS) & 1, kSiteKFull)) { ok = false; break; }
@@ -370,7 +373,7 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
         mma_commit(bars.k_empty(kst));
         ++nk;
         for (int j = 0; ok; ++j) {
-            const bool nxt = w.next();
+            const bool nxt = j + 1 < n_tiles;
             const int vst = nv % C::NS;
             // query tile 0: PV_0(j), then QK_0(j+1)
             if (!wait(bars.p_full(0), npv & 1, kSitePFull)) { ok = false; break; }
@@ -518,7 +521,8 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             const float msub = (m_used == -INFINITY) ? 0.f : -m_used;
             const uint64_t neg_m2 = f2_pack(msub, msub);
             uint32_t pk[64];
-            uint64_t sum2[4] = {0, 0, 0, 0}, sumr2[4] = {0, 0, 0, 0};   // packed pairs of +0.0f
+            uint64_t sum2[4] = {0, 0, 0, 0};                          // packed pairs of +0.0f
+            float rlo[4] = {0.f, 0.f, 0.f, 0.f}, rhi[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 float a0, a1;
@@ -526,12 +530,12 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                 const float p0 = ex2(a0), p1 = ex2(a1);
                 pk[c] = pack_bf16(p0, p1);
                 sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
-                sumr2[c & 3] =
-                    f2_add(sumr2[c & 3], f2_pack(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xFFFF0000u)));
+                add_bf16x2_f32(rlo[c & 3], rhi[c & 3], pk[c]);
             }
             float s0, s1, r0, r1;
             f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s0, s1);
-            f2_unpack(f2_add(f2_add(sumr2[0], sumr2[1]), f2_add(sumr2[2], sumr2[3])), r0, r1);
+            r0 = (rlo[0] + rlo[1]) + (rlo[2] + rlo[3]);
+            r1 = (rhi[0] + rhi[1]) + (rhi[2] + rhi[3]);
             l += s0 + s1;
             lr += r0 + r1;
             // P_i over the first 64 columns of S_i: column c holds keys 2c (low half) and 2c + 1.
@@ -556,7 +560,8 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.p_full(wg));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full(wg));
             ++ntile;
             ++j;
         }
@@ -637,7 +642,8 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         }
         if (j > 0) {
             tc_fence_before();
-            mbar_arrive(bars.o_free(wg));                 // O_i has been read: the next unit may overwrite it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.o_free(wg));  // O_i has been read: the next unit may overwrite it
         }
     }
 }
@@ -714,6 +720,43 @@ __global__ void wait_selftest_kernel(uint32_t* header, uint64_t timeout_ns) {
     wait(b, 0, kSiteSelfTest);
 }
 
+// One thread per row group (rank r, group): the number of key tiles a unit of that row group
+// visits in this launch, by the same walk the producer and the softmax warps take. Units of one
+// row group differ only in batch element and heads, which do not change the walk.
+__global__ void unit_tiles_kernel(const Params P) {
+    const int rg = blockIdx.x * blockDim.x + threadIdx.x;
+    if (rg >= P.n_cp * P.n_grp) return;
+    Unit U;
+    U.rg = rg;
+    U.r = rg / P.n_grp;
+    U.b = 0;
+    U.kvh = 0;
+    const int grp = rg % P.n_grp;
+    if (P.pair_heads) {
+        U.qt[0] = U.qt[1] = grp;
+        U.valid[0] = U.valid[1] = 1;
+    } else {
+        U.qt[0] = 2 * grp;
+        U.qt[1] = 2 * grp + 1;
+        U.valid[0] = 1;
+        U.valid[1] = U.qt[1] < P.n_qt;
+    }
+    for (int i = 0; i < 2; ++i) {
+        if (U.valid[i]) {
+            const int4 t4 = P.tile_mm[U.r * P.n_qt + U.qt[i]];
+            U.qmm[i] = make_int2(t4.x, t4.y);
+        } else {
+            U.qmm[i] = make_int2(INT_MAX, INT_MIN);
+        }
+        U.head[i] = 0;
+    }
+    TileWalk w;
+    w.init(P, U);
+    int c = 0;
+    while (w.next()) ++c;
+    P.unit_tiles[rg] = c;
+}
+
 // ---- host side -------------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -781,6 +824,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.fused = a.fused; P.step = a.step; P.kv_by_holder = a.kv_by_holder; P.layout = a.layout;
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm); P.order = a.order;
+    P.unit_tiles = a.unit_tiles;
     P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
     P.header = a.header; P.timeout_ns = a.timeout_ns;
@@ -791,6 +835,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     }
     P.num_units = (int)units;
     const int grid = (int)(units < sms ? units : sms);
+    const int n_rg = a.n_cp * a.n_grp;
+    unit_tiles_kernel<<<(n_rg + 127) / 128, 128, 0, st>>>(P);
     ring_attention_kernel<D><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }

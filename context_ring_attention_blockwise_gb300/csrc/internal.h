@@ -29,6 +29,8 @@ struct WsLayout {
     size_t order = 0;       // int32 [n_cp * n_qt]: (rank, q-tile) pairs, longest first
     size_t counts = 0;      // uint64 [n_cp][n_cp][2]: tiles computed per (rank, step), FULL / DIAG
     size_t sched = 0;       // uint32 [1 + n_cp]: work counters of the persistent kernel (fused, each step)
+    size_t unit_tiles = 0;  // int32 [n_cp * n_qt]: key tiles a unit of row group (r, group) visits in
+                            // the current launch (written by the attention launch itself)
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
@@ -70,6 +72,7 @@ int launch_permute(const PermuteArgs& a, void* stream);
 struct AttnLaunch {
     int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt, pair_heads, n_grp;
     uint32_t* sched;  // work counter of this launch (zeroed before the launch)
+    int32_t* unit_tiles;  // [n_cp * n_grp] scratch: key tiles per row group for this launch
     float scale_log2;
     int fused;        // 1: all ring steps, natural-order bf16 output; 0: one step, merge into running state
     int step;         // ring step (fused == 0)

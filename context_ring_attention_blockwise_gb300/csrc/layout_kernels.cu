@@ -79,36 +79,51 @@ __global__ void tile_suffix_kernel(int4* __restrict__ tile_mm, int n_cp, int n_q
 }
 
 // Gather rows of d bf16 from natural [B,T,heads,d] into rank-major [n_cp][B][heads][n][d].
-// One thread moves 16 bytes; threads walk the source in order so reads are fully coalesced and
-// every destination row is written as whole 16-byte pieces of one contiguous row.
-__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
+// A block takes one natural token row (b, t) at a time: its h query heads and n_kv key and value
+// heads, (h + 2 n_kv) * d / 8 pieces of 16 bytes, contiguous in each source. The rank and local
+// index are worked out once per row; each thread then issues up to kUnroll loads before its
+// stores, so enough bytes are in flight to keep HBM busy.
+constexpr int kPermuteUnroll = 8;
+
+__global__ void __launch_bounds__(256, 4) permute_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
                                                       const uint4* __restrict__ v, uint4* __restrict__ qL,
                                                       uint4* __restrict__ kL, uint4* __restrict__ vL, int B, int64_t T,
                                                       int64_t n, int64_t m, int h, int n_kv, int d, int n_cp,
                                                       int layout) {
-    const int cpr = d / 8;                                  // 16-byte chunks per row
-    const int64_t nq = (int64_t)B * T * h * cpr;
-    const int64_t nk = (int64_t)B * T * n_kv * cpr;
-    const int64_t total = nq + 2 * nk;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const uint4* src;
-        uint4* dst;
-        int64_t e;
-        int heads;
-        if (i < nq) { src = q; dst = qL; e = i; heads = h; }
-        else if (i < nq + nk) { src = k; dst = kL; e = i - nq; heads = n_kv; }
-        else { src = v; dst = vL; e = i - nq - nk; heads = n_kv; }
-        const int c = (int)(e % cpr);
-        int64_t rest = e / cpr;
-        const int hd = (int)(rest % heads);
-        rest /= heads;
-        const int64_t t = rest % T;
-        const int b = (int)(rest / T);
+    const int lg = (d == 128) ? 4 : 3;                      // log2 of the 16-byte pieces per head row
+    const int cpr = 1 << lg;
+    const int per_row = (h + 2 * n_kv) * cpr;
+    const int64_t rows = (int64_t)B * T;
+    for (int64_t rw = blockIdx.x; rw < rows; rw += gridDim.x) {
+        const int64_t t = rw % T;
+        const int b = (int)(rw / T);
         int r;
         int64_t j;
         rank_of(layout, t, n, m, n_cp, r, j);
-        const int64_t drow = (((int64_t)r * B + b) * heads + hd) * n + j;
-        dst[drow * cpr + c] = __ldg(src + e);
+        const int64_t rb = (int64_t)r * B + b;
+        for (int e0 = threadIdx.x; e0 < per_row; e0 += kPermuteUnroll * blockDim.x) {
+            uint4 x[kPermuteUnroll];
+            uint4* dp[kPermuteUnroll];
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u) {
+                const int e = e0 + u * blockDim.x;
+                dp[u] = nullptr;
+                if (e < per_row) {
+                    const int hh = e >> lg, c = e & (cpr - 1);
+                    const uint4* src;
+                    uint4* dst;
+                    int heads, hd;
+                    if (hh < h) { src = q; dst = qL; heads = h; hd = hh; }
+                    else if (hh < h + n_kv) { src = k; dst = kL; heads = n_kv; hd = hh - h; }
+                    else { src = v; dst = vL; heads = n_kv; hd = hh - h - n_kv; }
+                    x[u] = __ldg(src + (rw * heads + hd) * cpr + c);
+                    dp[u] = dst + ((rb * heads + hd) * n + j) * cpr + c;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u)
+                if (dp[u]) *dp[u] = x[u];
+        }
     }
 }
 
@@ -151,48 +166,78 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
 }
 
 // S-way merge: o = sum_s exp(lse_s - L) o_s with L = M + ln sum_s exp(lse_s - M), M = max lse_s.
-// One thread per 4 consecutive d of one (row, head).
-__global__ void __launch_bounds__(256) merge_kernel(int S, int64_t rows, int h, int d, const float4* __restrict__ o_parts,
-                                                    const float* __restrict__ lse_parts, uint2* __restrict__ o,
-                                                    float* __restrict__ lse) {
-    const int cpr = d / 4;
+// One thread per 8 consecutive d of one (row, head). One pass over the partials, four at a time:
+// the chunk's loads are issued together, then a running maximum, sum and weighted sum are
+// updated (rescaled when the maximum rises). An empty partial (lse = -inf) is skipped, whatever
+// its O holds.
+__global__ void __launch_bounds__(256, 4) merge_kernel(int S, int64_t rows, int h, int d,
+                                                       const float4* __restrict__ o_parts,
+                                                       const float* __restrict__ lse_parts, uint4* __restrict__ o,
+                                                       float* __restrict__ lse) {
+    const int cpr = d / 8;
     const int64_t total = rows * h * cpr;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(i % cpr);
         const int64_t rh = i / cpr;
         const int hd = (int)(rh % h);
         const int64_t row = rh / h;
-        float M = -INFINITY;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, __ldg(lse_parts + ((int64_t)s * h + hd) * rows + row));
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = -INFINITY;
-        if (M != -INFINITY) {
-            float sum = 0.f;
-            for (int s = 0; s < S; ++s) sum += expf(__ldg(lse_parts + ((int64_t)s * h + hd) * rows + row) - M);
-            L = M + logf(sum);
-            for (int s = 0; s < S; ++s) {
-                const float ls = __ldg(lse_parts + ((int64_t)s * h + hd) * rows + row);
-                if (ls == -INFINITY) continue;
-                const float w = expf(ls - L);
-                const float4 x = __ldg(o_parts + ((int64_t)s * rows * h + rh) * cpr + c);
-                acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+        float M = -INFINITY, sum = 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            float ls[4];
+            float4 x[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s = s0 + u;
+                ls[u] = -INFINITY;
+                x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (s < S) {
+                    ls[u] = __ldg(lse_parts + ((int64_t)s * h + hd) * rows + row);
+                    const float4* src = o_parts + ((int64_t)s * total + i) * 2;
+                    x[u][0] = __ldg(src);
+                    x[u][1] = __ldg(src + 1);
+                }
             }
+            const float mc = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
+            if (mc == -INFINITY) continue;
+            const float Mn = fmaxf(M, mc);
+            const float a = expf(M - Mn);                 // 0 while nothing has been merged
+            sum *= a;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] *= a;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (ls[u] == -INFINITY) continue;
+                const float w = expf(ls[u] - Mn);
+                sum += w;
+                acc[0] += w * x[u][0].x; acc[1] += w * x[u][0].y; acc[2] += w * x[u][0].z; acc[3] += w * x[u][0].w;
+                acc[4] += w * x[u][1].x; acc[5] += w * x[u][1].y; acc[6] += w * x[u][1].z; acc[7] += w * x[u][1].w;
+            }
+            M = Mn;
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 out;
-        out.x = *reinterpret_cast<uint32_t*>(&lo);
-        out.y = *reinterpret_cast<uint32_t*>(&hi);
-        o[i] = out;
+        const float inv = (M == -INFINITY) ? 0.f : 1.0f / sum;
+        const float L = (M == -INFINITY) ? -INFINITY : M + logf(sum);
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+            pk[e] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        o[i] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         if (c == 0) lse[(int64_t)hd * rows + row] = L;
     }
 }
 
-int grid_for(int64_t work, int threads) {
+int sm_count() {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+int grid_for(int64_t work, int threads) {
     int64_t blocks = (work + threads - 1) / threads;
-    int64_t cap = (int64_t)sms * 16;
+    int64_t cap = (int64_t)sm_count() * 16;
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
@@ -207,8 +252,9 @@ int launch_permute(const PermuteArgs& a, void* stream) {
     tile_suffix_kernel<<<(a.n_cp + 127) / 128, 128, 0, st>>>(reinterpret_cast<int4*>(a.tile_mm), a.n_cp, a.n_qt);
     e = (int)cudaGetLastError();
     if (e) return e;
-    const int64_t work = (int64_t)a.B * a.T * (a.h + 2 * a.n_kv) * (a.d / 8);
-    permute_kernel<<<grid_for(work, 256), 256, 0, st>>>(
+    // one token row per block iteration; four resident 256-thread blocks per SM
+    const int64_t rows = (int64_t)a.B * a.T, cap = (int64_t)sm_count() * 4;
+    permute_kernel<<<(int)(rows < cap ? rows : cap), 256, 0, st>>>(
         static_cast<const uint4*>(a.q), static_cast<const uint4*>(a.k), static_cast<const uint4*>(a.v),
         static_cast<uint4*>(a.qL), static_cast<uint4*>(a.kL), static_cast<uint4*>(a.vL), a.B, a.T, a.n, a.m, a.h,
         a.n_kv, a.d, a.n_cp, a.layout);
@@ -225,9 +271,11 @@ int launch_finalize(const FinalizeArgs& a, void* stream) {
 
 int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts, void* o, float* lse,
                  void* stream) {
-    const int64_t work = rows * h * (d / 4);
-    merge_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        S, rows, h, d, reinterpret_cast<const float4*>(o_parts), lse_parts, static_cast<uint2*>(o), lse);
+    // four resident 256-thread blocks per SM, grid-stride over (row, head, 8 columns)
+    const int64_t work = rows * h * (d / 8), cap = (int64_t)sm_count() * 4;
+    const int64_t blocks = (work + 255) / 256;
+    merge_kernel<<<(int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        S, rows, h, d, reinterpret_cast<const float4*>(o_parts), lse_parts, static_cast<uint4*>(o), lse);
     return (int)cudaGetLastError();
 }
 

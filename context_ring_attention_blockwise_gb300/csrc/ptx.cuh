@@ -45,6 +45,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// acc_lo += low bf16 of pk, acc_hi += high bf16 of pk: each bf16 is widened exactly and added in
+// fp32 (round to nearest), with no integer unpacking of the pair.
+__device__ __forceinline__ void add_bf16x2_f32(float& acc_lo, float& acc_hi, uint32_t pk) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(pk));
+}
+
 // ---- TMA -----------------------------------------------------------------------------------
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -141,7 +141,7 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
  *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).
  *   o_parts   [S][rows][h][d] fp32 (device, read)      lse_parts [S][h][rows] fp32 (device, read)
  *   o_bf16    [rows][h][d] bf16 (device, written)      lse       [h][rows] fp32 (device, written)
- * d must be a multiple of 4. */
+ * d must be a multiple of 8 (each thread of the kernel merges 8 consecutive values). */
 cpattn_status_t cpattn_merge(int S, int64_t rows, int h, int d, const float* o_parts, const float* lse_parts,
                              void* o_bf16, float* lse, cpattn_stream_t stream);
 

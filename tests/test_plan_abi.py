@@ -78,6 +78,7 @@ def test_calls_fail_before_launch_on_bad_arguments():
     assert L.cpattn_forward(p.handle, 1, fake, fake, fake, None, 0.0, fake, fake, odd, ws_ok, None) == 3
     assert L.cpattn_forward(p.handle, 0, fake, fake, fake, None, 0.0, fake, fake, fake, ws_ok, None) == 1
     assert L.cpattn_merge(2, 10, 2, 6, fake, fake, fake, fake, None) == 1
+    assert L.cpattn_merge(2, 10, 2, 12, fake, fake, fake, fake, None) == 1     # d must be a multiple of 8
     assert L.cpattn_ring_step(p.handle, 1, 0, 0.0, fake, p.ring_workspace_size(1), None, None) == 1   # permute first
     assert "permute" in L.cpattn_last_error().decode()
     assert L.cpattn_finalize(p.handle, 1, fake, fake, fake, p.ring_workspace_size(1), None) == 1
