@@ -72,6 +72,13 @@ def bind(path: str):
     lib.oracle_overlap_min_tokens.restype = ctypes.c_double
     lib.oracle_kv_bytes_recv.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.oracle_kv_bytes_recv.restype = _I64
+    lib.oracle_attention_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                                              _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _I64, _P, _P, _P, _P]
+    lib.oracle_ring_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P,
+                                         _P, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         _P, _P, _P]
+    lib.oracle_bwd_bytes_recv.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.oracle_bwd_bytes_recv.restype = _I64
     return lib
 
 
@@ -149,6 +156,60 @@ class Oracle:
         if rc:
             raise ValueError("oracle_ring failed")
         return o, lse
+
+    # -- gradients ----------------------------------------------------------------------
+    def backward(self, q, k, v, dout, causal=True, scale=None, pos=None, rows=None, keys=None):
+        """Gradients of L = sum(O * dO) for bf16-bit inputs (dout [B,T,h,d] bf16 bits too).
+
+        Returns (dq [B,R,h,d] for the query rows `rows`, dk [B,K,n_kv,d], dv [B,K,n_kv,d] for the
+        keys `keys`), fp64; rows/keys default to all T."""
+        B, T, h, d = q.shape
+        n_kv = k.shape[2]
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, dout))
+        posp = None
+        if pos is not None:
+            pos = np.ascontiguousarray(pos, dtype=np.int32)
+            posp = pos.ctypes.data
+        rowsp, R = None, T
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            rowsp, R = rows.ctypes.data, rows.size
+        keysp, K = None, T
+        if keys is not None:
+            keys = np.ascontiguousarray(keys, dtype=np.int64)
+            keysp, K = keys.ctypes.data, keys.size
+        dq = np.empty((B, R, h, d), dtype=np.float64)
+        dk = np.empty((B, K, n_kv, d), dtype=np.float64)
+        dv = np.empty((B, K, n_kv, d), dtype=np.float64)
+        rc = self.lib.oracle_attention_backward(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                dout.ctypes.data, posp, int(causal), scale, R, rowsp, K, keysp,
+                                                dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+        if rc:
+            raise ValueError("oracle_attention_backward failed")
+        return dq, dk, dv
+
+    def ring_backward(self, q, k, v, dout, n_cp, layout, causal=True, scale=None, pos=None, block=16):
+        B, T, h, d = q.shape
+        n_kv = k.shape[2]
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v, dout))
+        posp = None
+        if pos is not None:
+            pos = np.ascontiguousarray(pos, dtype=np.int32)
+            posp = pos.ctypes.data
+        dq = np.empty((B, T, h, d), dtype=np.float64)
+        dk = np.empty((B, T, n_kv, d), dtype=np.float64)
+        dv = np.empty((B, T, n_kv, d), dtype=np.float64)
+        rc = self.lib.oracle_ring_backward(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                           dout.ctypes.data, posp, int(causal), scale, n_cp, layout, block,
+                                           dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+        if rc:
+            raise ValueError("oracle_ring_backward failed")
+        return dq, dk, dv
+
+    def bwd_bytes_recv(self, B, n, n_kv, d_k, n_cp, grad_bytes) -> int:
+        return int(self.lib.oracle_bwd_bytes_recv(B, n, n_kv, d_k, n_cp, grad_bytes))
 
     def merge(self, o_parts, lse_parts):
         """o_parts [S,rows,h,d], lse_parts [S,h,rows] (fp64). Returns (o [rows,h,d], lse [h,rows])."""

@@ -22,7 +22,9 @@
  *
  * Parity status: every function below is pinned by the CPU tests (closed forms, the pages'
  * printed figures, brute force on small inputs, agreement of the ring simulation with the
- * definition, and a library softmax-attention routine). Nothing here is "parity unpinned".
+ * definition, and a library softmax-attention routine; for the gradients also central finite
+ * differences of the forward definition and a library's automatic differentiation). Nothing
+ * here is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -429,4 +431,298 @@ double oracle_overlap_min_tokens(double flops_per_s, double bytes_per_s, double 
  * foreign block, skipped or not, for B sequences and all n_kv heads of width d_k. */
 int64_t oracle_kv_bytes_recv(int B, int64_t n, int n_kv, int d_k, int n_cp) {
     return (int64_t)(n_cp - 1) * 2 /* K and V */ * (int64_t)B * n * n_kv * d_k * 2 /* bytes */;
+}
+
+/* ------------------------------------------------------------------------------------- */
+/* Gradients. [CEX] "Splitting the sequence, and the one layer that objects" and "What    */
+/* context parallelism communicates": the backward pass of the ring computes the same     */
+/* gradients as plain attention; each rank keeps the gradient of its queries, and the key  */
+/* and value gradients travel with the blocks back to their owners. The pages print no     */
+/* gradient formulas; these are the derivatives of the forward definition above, for the   */
+/* loss L = sum_{b,t,i} <O[b,t,i,:], dO[b,t,i,:]>:                                          */
+/*   P_tu  = exp(s_tu - lse_t) for visible u, else 0                                        */
+/*   dP_tu = <dO_t, v_u>,  D_t = sum_u P_tu dP_tu = <dO_t, O_t>                              */
+/*   dS_tu = P_tu (dP_tu - D_t)                                                              */
+/*   dQ_t  = scale sum_u dS_tu k_u                                                           */
+/*   dK_u  = scale sum_{i in group} sum_t dS_tu q_t,  dV_u = sum_{i in group} sum_t P_tu dO_t */
+/* (the KV head of a group receives the sum over the group's query heads).                 */
+/* ------------------------------------------------------------------------------------- */
+
+/* lse and D = <dO_t, O_t> of one (b, t, head i) row from the definition (two passes). */
+static void row_stats(int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      const uint16_t* dout, const int32_t* pos, int causal, double scale, int b, int64_t t, int i,
+                      double* acc, double* lse_out, double* d_out) {
+    int kv = i / (h / n_kv);
+    const uint16_t* qrow = q + (((int64_t)b * T + t) * h + i) * d;
+    double mx = -INFINITY;
+    for (int64_t u = 0; u < T; ++u) {
+        if (!visible(pos, u, t, causal)) continue;
+        const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_value(qrow[c]) * bf16_value(krow[c]);
+        if (scale * dot > mx) mx = scale * dot;
+    }
+    if (mx == -INFINITY) { *lse_out = -INFINITY; *d_out = 0.0; return; }
+    double sum = 0.0;
+    for (int c = 0; c < d; ++c) acc[c] = 0.0;
+    for (int64_t u = 0; u < T; ++u) {
+        if (!visible(pos, u, t, causal)) continue;
+        const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
+        const uint16_t* vrow = v + (((int64_t)b * T + u) * n_kv + kv) * d;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += bf16_value(qrow[c]) * bf16_value(krow[c]);
+        double e = exp(scale * dot - mx);
+        sum += e;
+        for (int c = 0; c < d; ++c) acc[c] += e * bf16_value(vrow[c]);
+    }
+    const uint16_t* grow = dout + (((int64_t)b * T + t) * h + i) * d;
+    double dd = 0.0;
+    for (int c = 0; c < d; ++c) dd += bf16_value(grow[c]) * (acc[c] / sum);
+    *lse_out = mx + log(sum);
+    *d_out = dd;
+}
+
+/* The contribution of the pair (query t of head i, key u): P_tu and dS_tu. */
+static void pair_terms(int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                       const uint16_t* dout, double scale, int b, int64_t t, int i, int64_t u, double lse_t,
+                       double d_t, double* p_out, double* ds_out) {
+    int kv = i / (h / n_kv);
+    const uint16_t* qrow = q + (((int64_t)b * T + t) * h + i) * d;
+    const uint16_t* grow = dout + (((int64_t)b * T + t) * h + i) * d;
+    const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
+    const uint16_t* vrow = v + (((int64_t)b * T + u) * n_kv + kv) * d;
+    double dot = 0.0, dp = 0.0;
+    for (int c = 0; c < d; ++c) {
+        dot += bf16_value(qrow[c]) * bf16_value(krow[c]);
+        dp += bf16_value(grow[c]) * bf16_value(vrow[c]);
+    }
+    double p = exp(scale * dot - lse_t);
+    *p_out = p;
+    *ds_out = p * (dp - d_t);
+}
+
+/* q [B,T,h,d], k/v [B,T,n_kv,d], dout [B,T,h,d] bf16 bits, natural order.
+ * dq [B,n_rows,h,d] for the query rows `rows` (NULL: all T, n_rows = T; dq may be NULL);
+ * dk, dv [B,n_keys,n_kv,d] for the keys `keys` (NULL: all T, n_keys = T; dk/dv may be NULL).
+ * fp64 outputs. Returns 0 on success. */
+int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                              const uint16_t* v, const uint16_t* dout, const int32_t* pos, int causal, double scale,
+                              int64_t n_rows, const int64_t* rows, int64_t n_keys, const int64_t* keys, double* dq,
+                              double* dk, double* dv) {
+    if (B <= 0 || T <= 0 || h <= 0 || n_kv <= 0 || d <= 0 || h % n_kv) return 1;
+    if (!rows) n_rows = T;
+    if (!keys) n_keys = T;
+    int g = h / n_kv;
+    int err = 0;
+    /* dQ: every row is self-contained (its own lse and D, then one more pass over its keys) */
+    if (dq) {
+        int64_t total = (int64_t)B * n_rows * h;
+#pragma omp parallel
+        {
+            double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+            if (!acc) {
+#pragma omp atomic write
+                err = 1;
+            }
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t w = 0; w < total; ++w) {
+                if (!acc) continue;
+                int i = (int)(w % h);
+                int64_t ri = (w / h) % n_rows;
+                int b = (int)(w / ((int64_t)h * n_rows));
+                int64_t t = rows ? rows[ri] : ri;
+                int kv = i / g;
+                double lse_t, d_t;
+                row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc, &lse_t, &d_t);
+                double* out = dq + (((int64_t)b * n_rows + ri) * h + i) * d;
+                for (int c = 0; c < d; ++c) out[c] = 0.0;
+                if (lse_t == -INFINITY) continue;
+                for (int64_t u = 0; u < T; ++u) {
+                    if (!visible(pos, u, t, causal)) continue;
+                    double p, ds;
+                    pair_terms(T, h, n_kv, d, q, k, v, dout, scale, b, t, i, u, lse_t, d_t, &p, &ds);
+                    const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
+                    for (int c = 0; c < d; ++c) out[c] += scale * ds * bf16_value(krow[c]);
+                }
+            }
+            free(acc);
+        }
+        if (err) return err;
+    }
+    if (!dk && !dv) return 0;
+    /* dK, dV: first lse and D of every row that sees one of the keys, then per key the sum
+     * over those rows (and the query heads of its group). */
+    double* lse = (double*)malloc(sizeof(double) * (size_t)B * h * T);
+    double* dd = (double*)malloc(sizeof(double) * (size_t)B * h * T);
+    unsigned char* need = (unsigned char*)calloc((size_t)B * T, 1);
+    if (!lse || !dd || !need) { free(lse); free(dd); free(need); return 1; }
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t ki = 0; ki < n_keys; ++ki) {
+            int64_t u = keys ? keys[ki] : ki;
+            if (visible(pos, u, t, causal)) { for (int b = 0; b < B; ++b) need[(int64_t)b * T + t] = 1; break; }
+        }
+    int64_t total = (int64_t)B * T * h;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t w = 0; w < total; ++w) {
+            if (!acc) continue;
+            int i = (int)(w % h);
+            int64_t t = (w / h) % T;
+            int b = (int)(w / ((int64_t)h * T));
+            if (!need[(int64_t)b * T + t]) continue;
+            row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc,
+                      &lse[((int64_t)b * h + i) * T + t], &dd[((int64_t)b * h + i) * T + t]);
+        }
+        free(acc);
+    }
+    if (err) { free(lse); free(dd); free(need); return err; }
+    int64_t kt = (int64_t)B * n_keys * n_kv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < kt; ++w) {
+        int kvh = (int)(w % n_kv);
+        int64_t ki = (w / n_kv) % n_keys;
+        int b = (int)(w / ((int64_t)n_kv * n_keys));
+        int64_t u = keys ? keys[ki] : ki;
+        double* gk = dk ? dk + (((int64_t)b * n_keys + ki) * n_kv + kvh) * d : NULL;
+        double* gv = dv ? dv + (((int64_t)b * n_keys + ki) * n_kv + kvh) * d : NULL;
+        for (int c = 0; c < d; ++c) { if (gk) gk[c] = 0.0; if (gv) gv[c] = 0.0; }
+        for (int i = kvh * g; i < (kvh + 1) * g; ++i)
+            for (int64_t t = 0; t < T; ++t) {
+                if (!visible(pos, u, t, causal)) continue;
+                double lse_t = lse[((int64_t)b * h + i) * T + t];
+                if (lse_t == -INFINITY) continue;
+                double p, ds;
+                pair_terms(T, h, n_kv, d, q, k, v, dout, scale, b, t, i, u, lse_t, dd[((int64_t)b * h + i) * T + t], &p, &ds);
+                const uint16_t* qrow = q + (((int64_t)b * T + t) * h + i) * d;
+                const uint16_t* grow = dout + (((int64_t)b * T + t) * h + i) * d;
+                for (int c = 0; c < d; ++c) {
+                    if (gk) gk[c] += scale * ds * bf16_value(qrow[c]);
+                    if (gv) gv[c] += p * bf16_value(grow[c]);
+                }
+            }
+    }
+    free(lse);
+    free(dd);
+    free(need);
+    return 0;
+}
+
+/* The ring backward, simulated literally. [CEX] "What context parallelism communicates":   */
+/* the key and value gradients travel back to their owners "as a second circulating block  */
+/* in the ring". At step s rank r holds the key/value block of src = (r - s) mod n_cp and   */
+/* that block's gradient accumulator; it adds the contribution of its own queries, tile by  */
+/* tile (`block` keys), keeps its query gradient, and passes both blocks right. After n_cp  */
+/* steps the accumulator has visited every rank and one more hop returns it to src. lse and */
+/* D of every row come from the forward definition. Outputs in natural order, all rows.     */
+int oracle_ring_backward(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, const uint16_t* dout, const int32_t* pos, int causal, double scale,
+                         int n_cp, int layout, int block, double* dq, double* dk, double* dv) {
+    if (B <= 0 || T <= 0 || h <= 0 || n_kv <= 0 || d <= 0 || h % n_kv || n_cp <= 0 || T % n_cp || block <= 0)
+        return 1;
+    if (layout == LAYOUT_ZIGZAG && T % (2 * n_cp)) return 1;
+    int64_t n = T / n_cp;
+    int g = h / n_kv;
+    int64_t* map = (int64_t*)malloc(sizeof(int64_t) * (size_t)T);
+    double* lse = (double*)malloc(sizeof(double) * (size_t)B * h * T);
+    double* dd = (double*)malloc(sizeof(double) * (size_t)B * h * T);
+    if (!map || !lse || !dd || oracle_layout_map(T, n_cp, layout, map)) { free(map); free(lse); free(dd); return 1; }
+    int err = 0;
+    int64_t total = (int64_t)B * T * h;
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t w = 0; w < total; ++w) {
+            if (!acc) continue;
+            int i = (int)(w % h);
+            int64_t t = (w / h) % T;
+            int b = (int)(w / ((int64_t)h * T));
+            row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc,
+                      &lse[((int64_t)b * h + i) * T + t], &dd[((int64_t)b * h + i) * T + t]);
+        }
+        free(acc);
+    }
+    if (err) { free(map); free(lse); free(dd); return err; }
+    memset(dq, 0, sizeof(double) * (size_t)B * T * h * d);
+    /* one independent ring per (batch element, KV head): its query heads and its KV blocks */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < (int64_t)B * n_kv; ++w) {
+        int kvh = (int)(w % n_kv), b = (int)(w / n_kv);
+        double* acc_k = (double*)calloc((size_t)T * d, sizeof(double));   /* [block src][n][d] */
+        double* acc_v = (double*)calloc((size_t)T * d, sizeof(double));
+        if (!acc_k || !acc_v) {
+            free(acc_k); free(acc_v);
+#pragma omp atomic write
+            err = 1;
+            continue;
+        }
+        for (int s = 0; s < n_cp; ++s)
+            for (int r = 0; r < n_cp; ++r) {
+                int src = ((r - s) % n_cp + n_cp) % n_cp;     /* block rank r holds at step s */
+                for (int64_t j = 0; j < n; ++j) {
+                    int64_t t = map[(int64_t)r * n + j];
+                    for (int i = kvh * g; i < (kvh + 1) * g; ++i) {
+                        double lse_t = lse[((int64_t)b * h + i) * T + t], d_t = dd[((int64_t)b * h + i) * T + t];
+                        if (lse_t == -INFINITY) continue;
+                        const uint16_t* qrow = q + (((int64_t)b * T + t) * h + i) * d;
+                        const uint16_t* grow = dout + (((int64_t)b * T + t) * h + i) * d;
+                        double* dqrow = dq + (((int64_t)b * T + t) * h + i) * d;
+                        for (int64_t k0 = 0; k0 < n; k0 += block) {
+                            int64_t kn = (n - k0 < block) ? n - k0 : block;
+                            for (int64_t jj = 0; jj < kn; ++jj) {
+                                int64_t u = map[(int64_t)src * n + k0 + jj];
+                                if (!visible(pos, u, t, causal)) continue;
+                                double p, ds;
+                                pair_terms(T, h, n_kv, d, q, k, v, dout, scale, b, t, i, u, lse_t, d_t, &p, &ds);
+                                const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kvh) * d;
+                                double* ak = acc_k + ((int64_t)src * n + k0 + jj) * d;
+                                double* av = acc_v + ((int64_t)src * n + k0 + jj) * d;
+                                for (int c = 0; c < d; ++c) {
+                                    dqrow[c] += scale * ds * bf16_value(krow[c]);
+                                    ak[c] += scale * ds * bf16_value(qrow[c]);
+                                    av[c] += p * bf16_value(grow[c]);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        /* the accumulator of block src has made n_cp - 1 hops; the last returns it to src */
+        for (int src = 0; src < n_cp; ++src)
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t u = map[(int64_t)src * n + j];
+                double* gk = dk + (((int64_t)b * T + u) * n_kv + kvh) * d;
+                double* gv = dv + (((int64_t)b * T + u) * n_kv + kvh) * d;
+                for (int c = 0; c < d; ++c) {
+                    gk[c] = acc_k[((int64_t)src * n + j) * d + c];
+                    gv[c] = acc_v[((int64_t)src * n + j) * d + c];
+                }
+            }
+        free(acc_k);
+        free(acc_v);
+    }
+    free(map);
+    free(lse);
+    free(dd);
+    return err;
+}
+
+/* Bytes one rank receives in the backward ring: the key/value blocks of the n_cp - 1 other
+ * ranks (as in the forward) plus the circulating key/value gradient blocks, which arrive
+ * n_cp times (the last hop brings a rank its own block back). Gradient elements of
+ * grad_bytes each. [CEX] "What context parallelism communicates": the backward roughly
+ * doubles the traffic. */
+int64_t oracle_bwd_bytes_recv(int B, int64_t n, int n_kv, int d_k, int n_cp, int grad_bytes) {
+    int64_t blk = (int64_t)B * n * n_kv * d_k;
+    return (int64_t)(n_cp - 1) * 2 * blk * 2 + (int64_t)n_cp * 2 * blk * grad_bytes;
 }

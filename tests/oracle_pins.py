@@ -292,4 +292,132 @@ def pin_ulysses(orc):
     assert orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 2) < orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 0)
 
 
+# --------------------------------------------------------------------------------------
+# Gradients: a library's automatic differentiation, finite differences of the forward
+# definition, closed forms, an invariant, and the ring simulation
+# --------------------------------------------------------------------------------------
+
+def _dout(seed, B, T, h, d):
+    return synth.normal_bf16(seed, 4, (B, T, h, d))
+
+
+def _autograd(q, k, v, dout, causal, scale=None, mask=None):
+    """torch float64 autograd of SDPA (K/V heads repeat-interleaved) for L = sum(O * dO)."""
+    Q, K, V = (_f64(x).permute(0, 2, 1, 3).clone().requires_grad_(True) for x in (q, k, v))
+    g = Q.shape[1] // K.shape[1]
+    out = torch.nn.functional.scaled_dot_product_attention(Q, K.repeat_interleave(g, dim=1),
+                                                           V.repeat_interleave(g, dim=1), attn_mask=mask,
+                                                           is_causal=causal and mask is None, scale=scale)
+    (out * _f64(dout).permute(0, 2, 1, 3)).sum().backward()
+    return tuple(x.grad.permute(0, 2, 1, 3).numpy() for x in (Q, K, V))
+
+
+def pin_backward_autograd(orc):
+    for (B, T, h, n_kv, d, causal) in ((1, 41, 4, 2, 16, True), (2, 23, 2, 2, 8, False), (1, 30, 6, 1, 8, True)):
+        q, k, v = _qkv(31, B, T, h, n_kv, d)
+        do = _dout(31, B, T, h, d)
+        dq, dk, dv = orc.backward(q, k, v, do, causal=causal)
+        rq, rk, rv = _autograd(q, k, v, do, causal)
+        assert _maxabs(dq, rq) < 1e-11 and _maxabs(dk, rk) < 1e-11 and _maxabs(dv, rv) < 1e-11, \
+            f"gradients differ from autograd (B={B} T={T} h={h} n_kv={n_kv} causal={causal})"
+    # explicit scale and a mask from position ids
+    q, k, v = _qkv(32, 1, 20, 2, 1, 8)
+    do = _dout(32, 1, 20, 2, 8)
+    pos = np.array([3, 1, 4, 1, 5, 9, 2, 6, 5, 3, 5, 8, 9, 7, 9, 3, 2, 3, 8, 4], dtype=np.int32)
+    mask = torch.from_numpy(pos[None, :] <= pos[:, None])
+    dq, dk, dv = orc.backward(q, k, v, do, causal=True, scale=0.3, pos=pos)
+    rq, rk, rv = _autograd(q, k, v, do, False, scale=0.3, mask=mask)
+    assert _maxabs(dq, rq) < 1e-11 and _maxabs(dk, rk) < 1e-11 and _maxabs(dv, rv) < 1e-11, \
+        "gradients with position ids and an explicit scale differ from autograd"
+
+
+def _loss(orc, q, k, v, do, causal):
+    o, _ = orc.attention(q, k, v, causal=causal)
+    return float(np.sum(o * synth.bf16_bits_to_f32(do).astype(np.float64)))
+
+
+def _bf16_bits(x):
+    return (np.array([x], dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)[0]
+
+
+def pin_backward_finite_differences(orc):
+    """Central differences of the forward definition. The probed element is set to 0.5, and
+    0.5 +- 2^-7 are exact in bf16, so the perturbed inputs are representable exactly."""
+    B, T, h, n_kv, d = 1, 12, 2, 1, 8
+    q, k, v = _qkv(33, B, T, h, n_kv, d)
+    do = _dout(33, B, T, h, d)
+    eps = 2.0 ** -7
+    for causal in (True, False):
+        for name, arr, idx in (("q", q, (0, 7, 1, 3)), ("k", k, (0, 2, 0, 5)), ("v", v, (0, 4, 0, 1))):
+            base = arr.copy()
+            base[idx] = _bf16_bits(0.5)
+            args = {"q": q, "k": k, "v": v}
+            args[name] = base
+            dq, dk, dv = orc.backward(args["q"], args["k"], args["v"], do, causal=causal)
+            grad = {"q": dq, "k": dk, "v": dv}[name][idx]
+            plus, minus = base.copy(), base.copy()
+            plus[idx] = _bf16_bits(0.5 + eps)
+            minus[idx] = _bf16_bits(0.5 - eps)
+            a = dict(args); a[name] = plus
+            lp = _loss(orc, a["q"], a["k"], a["v"], do, causal)
+            a[name] = minus
+            lm = _loss(orc, a["q"], a["k"], a["v"], do, causal)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad) < 2e-3 * max(1.0, abs(grad)), f"d{name} {grad} vs finite difference {fd}"
+
+
+def pin_backward_closed_forms(orc):
+    """Q = 0: every visible key has weight 1/|V(t)|, so dK = 0 exactly and
+    dV_u = sum over the queries t that see u of dO_t / |V(t)|."""
+    B, T, h, n_kv, d = 1, 19, 2, 2, 8
+    _, k, v = _qkv(34, B, T, h, n_kv, d)
+    q = np.zeros((B, T, h, d), dtype=np.uint16)
+    do = _dout(34, B, T, h, d)
+    g = synth.bf16_bits_to_f32(do).astype(np.float64)
+    for causal in (True, False):
+        dq, dk, dv = orc.backward(q, k, v, do, causal=causal)
+        assert _maxabs(dk, 0.0) < 1e-14, "dK must vanish when Q = 0"
+        want = np.zeros_like(dv)
+        for u in range(T):
+            for t in range(T):
+                if causal and u > t:
+                    continue
+                want[0, u] += g[0, t] / ((t + 1) if causal else T)
+        assert _maxabs(dv, want) < 1e-12, "dV closed form for Q = 0"
+
+
+def pin_backward_invariants(orc):
+    """sum_u dS_tu = 0 for every query, hence sum_u dK_u = 0 for every KV head and column; and
+    the rows/keys subsets agree with the full computation."""
+    q, k, v = _qkv(35, 2, 33, 4, 2, 16)
+    do = _dout(35, 2, 33, 4, 16)
+    dq, dk, dv = orc.backward(q, k, v, do, causal=True)
+    assert _maxabs(dk.sum(axis=1), 0.0) < 1e-12, "key gradients must sum to zero over the keys"
+    rows = np.array([0, 5, 32, 17])
+    keys = np.array([32, 0, 9])
+    sq, sk, sv = orc.backward(q, k, v, do, causal=True, rows=rows, keys=keys)
+    assert _maxabs(sq, dq[:, rows]) < 1e-13 and _maxabs(sk, dk[:, keys]) < 1e-13 and _maxabs(sv, dv[:, keys]) < 1e-13, \
+        "row/key subsets differ from the full gradients"
+
+
+def pin_ring_backward_equals_definition(orc):
+    for layout in (CONTIGUOUS, ZIGZAG, STRIPED):
+        for causal in (True, False):
+            q, k, v = _qkv(36 + layout, 1, 48, 4, 2, 8)
+            do = _dout(36 + layout, 1, 48, 4, 8)
+            full = orc.backward(q, k, v, do, causal=causal)
+            ring = orc.ring_backward(q, k, v, do, 4, layout, causal=causal, block=5)
+            for a, b in zip(full, ring):
+                assert _maxabs(a, b) < 1e-12, f"ring backward differs (layout {layout}, causal {causal})"
+
+
+def pin_backward_bytes(orc):
+    """The pages: the backward ring roughly doubles the forward's traffic. With bf16 gradients
+    the gradient blocks add n_cp/(n_cp - 1) of the forward bytes: 2 + 1/15 times at n_cp = 16."""
+    fwd = orc.kv_bytes_recv(1, 8192, 1, 128, 16)
+    bwd = orc.bwd_bytes_recv(1, 8192, 1, 128, 16, 2)
+    assert fwd == 62914560 and bwd == 62914560 + 16 * 2 * 8192 * 128 * 2, "backward ring bytes"
+    assert abs(bwd / fwd - (2 + 1 / 15)) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

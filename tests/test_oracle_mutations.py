@@ -48,6 +48,20 @@ MUTANTS = [
      "return flops_per_s / bytes_per_s * (h / n_kv);", None),
     ("ulysses_keeps_all", "return 4.0 * n * (d + d_kv) * (n_cp - 1.0) / n_cp;",
      "return 4.0 * n * (d + d_kv) * (n_cp - 1.0);", None),
+    # gradients
+    ("bwd_drops_D", "*ds_out = p * (dp - d_t);", "*ds_out = p * dp;", None),
+    ("bwd_ds_sign", "*ds_out = p * (dp - d_t);", "*ds_out = p * (d_t - dp);", None),
+    ("bwd_D_unnormalised", "dd += bf16_value(grow[c]) * (acc[c] / sum);", "dd += bf16_value(grow[c]) * acc[c];", None),
+    ("bwd_lse_drops_max", "*lse_out = mx + log(sum);", "*lse_out = log(sum);", None),
+    ("bwd_dq_no_scale", "out[c] += scale * ds * bf16_value(krow[c]);", "out[c] += ds * bf16_value(krow[c]);", None),
+    ("bwd_dk_no_scale", "if (gk) gk[c] += scale * ds * bf16_value(qrow[c]);", "if (gk) gk[c] += ds * bf16_value(qrow[c]);",
+     None),
+    ("bwd_dv_uses_ds", "if (gv) gv[c] += p * bf16_value(grow[c]);", "if (gv) gv[c] += ds * bf16_value(grow[c]);", None),
+    ("bwd_first_head_only", "for (int i = kvh * g; i < (kvh + 1) * g; ++i)\n            for (int64_t t = 0; t < T; ++t) {",
+     "for (int i = kvh * g; i < kvh * g + 1; ++i)\n            for (int64_t t = 0; t < T; ++t) {", None),
+    ("ring_bwd_own_block", "int src = ((r - s) % n_cp + n_cp) % n_cp;     /* block rank r holds at step s */",
+     "int src = r;", None),
+    ("bwd_bytes_grad_hops", "(int64_t)n_cp * 2 * blk * grad_bytes", "(int64_t)(n_cp - 1) * 2 * blk * grad_bytes", None),
 ]
 
 
