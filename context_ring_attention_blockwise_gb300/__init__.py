@@ -26,6 +26,7 @@ SYMBOLS = [
     "cpattn_attend", "cpattn_forward_noalloc",
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
+    "cpattn_backward_workspace_size", "cpattn_backward",
 ]
 
 
@@ -66,6 +67,8 @@ def lib():
     L.cpattn_tile_counts.argtypes = [_P, i, _P, _P, _P]
     L.cpattn_check.argtypes = [_P, _P]
     L.cpattn_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, u64, _P]
+    L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_last_error.restype = ctypes.c_char_p
     L.cpattn_last_error.argtypes = []
     L.cpattn_version.restype = ctypes.c_char_p
@@ -119,6 +122,11 @@ class Plan:
     def ring_workspace_size(self, B: int) -> int:
         out = ctypes.c_size_t()
         _check(lib().cpattn_ring_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_ring_workspace_size")
+        return out.value
+
+    def backward_workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_backward_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_backward_workspace_size")
         return out.value
 
     def tile_shape(self):
@@ -194,6 +202,30 @@ def forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, 
                                 _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
                                 _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_forward")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = None, ws=None, dq=None, dk=None,
+             dv=None, stream=None):
+    """cpattn_backward: gradients of sum(o * dout) for the forward o, lse = forward(q, k, v, plan).
+    q/o/dout [B,T,h,d], k/v [B,T,n_kv,d] bf16 and lse [B,h,T] fp32 CUDA tensors (natural order).
+    Returns (dq [B,T,h,d], dk [B,T,n_kv,d], dv [B,T,n_kv,d]) bf16."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    for t, name in ((o, "o"), (dout, "dout")):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if tuple(lse.shape) != (B, plan.h, plan.T) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, h, T]")
+    if ws is None:
+        ws = alloc_workspace(plan.backward_workspace_size(B), q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib().cpattn_backward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
+                                 _dev_ptr(lse, "lse"), _dev_ptr(dout, "dout"), _dev_ptr(pos, "pos"), float(scale or 0.0),
+                                 _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), _dev_ptr(ws, "ws"),
+                                 ws.numel(), _stream_ptr(stream)), "cpattn_backward")
+    return dq, dk, dv
 
 
 def forward_noalloc(q, k, v, plan: Plan, pos=None, scale: float | None = None, out=None, lse=None, stream=None):

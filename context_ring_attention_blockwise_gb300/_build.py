@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcpattn.so")
-SOURCES = ["api.cpp", "plan.cpp", "layout_kernels.cu", "attention.cu", "noalloc.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+SOURCES = ["api.cpp", "plan.cpp", "layout_kernels.cu", "attention.cu", "backward.cu", "noalloc.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "tma_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -164,6 +164,13 @@ cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* by
     return CPATTN_OK;
 }
 
+cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    *bytes = cpattn::ws_layout(*p, B).bwd_end;
+    return CPATTN_OK;
+}
+
 cpattn_status_t cpattn_tile_shape(cpattn_plan_t plan, int* block_q, int* block_k) {
     if (!plan) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     if (block_q) *block_q = cpattn::kBlockQ;
@@ -205,6 +212,48 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
     std::string why;
     int e = launch_attn(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,
+                                void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !dout || !dq || !dk || !dv)
+        return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be non-NULL");
+    if (!aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be 16-byte aligned");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    if (ws_bytes < w.bwd_end)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(w.bwd_end) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st))) return s;
+    cpattn::BwdPrepArgs pa{};
+    pa.B = B; pa.T = p->T; pa.n = p->n; pa.m = p->m; pa.h = p->h; pa.d = p->d; pa.n_cp = p->n_cp;
+    pa.layout = p->layout; pa.n_qt = p->n_qt;
+    pa.o = o; pa.dout = dout; pa.lse = lse;
+    pa.doL = at<char>(ws, w.doL); pa.lse2L = at<float>(ws, w.lse2); pa.DL = at<float>(ws, w.Dl);
+    int e = cpattn::launch_bwd_prep(pa, st);
+    if (e) return cuda_fail(e, "backward prep kernel");
+    cpattn::BwdLaunch a{};
+    a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.n_kv = p->n_kv; a.d = p->d; a.n_cp = p->n_cp;
+    a.layout = p->layout; a.causal = p->causal; a.n_qt = p->n_qt;
+    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)p->d));
+    a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL); a.doL = at<char>(ws, w.doL);
+    a.lse2L = at<float>(ws, w.lse2); a.DL = at<float>(ws, w.Dl);
+    a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.header = at<uint32_t>(ws, w.header);
+    a.timeout_ns = 2000000000ull;
+    std::string why;
+    e = cpattn::launch_backward(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
 

@@ -1,0 +1,817 @@
+// backward.cu -- the backward pass of ring attention on sm_103a: the gradients of the forward
+// with respect to Q, K and V ("Context and expert parallelism", section "What context
+// parallelism communicates": each rank keeps the gradient of its own queries, and the key and
+// value gradients travel back to their owners as a second circulating block of the ring).
+//
+// With P_tu = exp(s_tu - lse_t), dP_tu = <dO_t, v_u>, D_t = <dO_t, O_t> and
+// dS_tu = P_tu (dP_tu - D_t):  dQ_t = scale sum_u dS_tu k_u,  dK_u = scale sum_t dS_tu q_t,
+// dV_u = sum_t P_tu dO_t, the sums over t running over the query heads of the key's group.
+//
+// Three kernels:
+//   bwd_prep_kernel   D_t from O and dO (fp32), and dO, lse (as log2) and D in layout order.
+//   bwd_dkdv_kernel   one CTA per key tile (128 keys of one rank block, one KV head). It walks
+//                     the query tiles in ring order -- the block's gradient visits rank src + s
+//                     at step s -- and for every visible (query tile, query head of the group):
+//                       S^T = K Q^T, dP^T = V dO^T          (tcgen05, SS form)
+//                       P^T, dS^T elementwise (two warpgroups, 64 query columns each)
+//                       dV += P^T dO, dK += dS^T Q          (tcgen05, TS form, P^T / dS^T in TMEM)
+//                     dK and dV accumulate in tensor memory for the whole walk and are written
+//                     once, to natural token order: the block arriving back at its owner.
+//   bwd_dq_kernel     one CTA per query tile (128 queries of one rank, one head). It walks the
+//                     key tiles like the forward and for each: S = Q K^T, dP = dO V^T, dS, then
+//                     dQ += dS K (TS form, dS in TMEM).
+// Both tcgen05 kernels: warp 0 loads tiles by TMA and publishes each step of the walk in a
+// shared-memory ring; warp 1 owns tensor memory and one lane issues the MMAs; warps 4..11 are
+// the elementwise warpgroups. All waits are bounded by the global timer like the forward's.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <string>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace cpattn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;
+constexpr int kRing = 8;            // walk steps published ahead by the producer
+constexpr int kNS = 2;              // stages of the streamed operand pair
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum BwdSite : int { kBSiteStage = 101, kBSiteStageEmpty, kBSiteFixed, kBSiteSt, kBSiteP, kBSiteDone, kBSiteWalk,
+                     kBSiteDrain };
+
+struct BwdParams {
+    int B, h, n_kv, g, n_cp, n_qt, causal, layout;
+    int64_t n, m, T, n_pad;   // n_pad = n_qt * 128: row stride of lse2L and DL
+    float scale, scale_log2;
+    const int32_t* posL;
+    const int4* tile_mm;
+    const float* lse2L;   // [n_cp][B][h][n_pad] lse * log2(e) (tile starts 512-byte aligned)
+    const float* DL;      // [n_cp][B][h][n_pad]
+    uint16_t* dq;         // natural [B,T,h,d]
+    uint16_t* dk;         // natural [B,T,n_kv,d]
+    uint16_t* dv;
+    uint32_t* header;
+    uint64_t timeout_ns;
+};
+
+struct BWaiter {
+    volatile int* abort_flag;
+    uint32_t* header;
+    uint64_t timeout_ns;
+    __device__ bool operator()(uint32_t bar, uint32_t parity, int site, bool honour_abort = true) const {
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(bar, parity)) return true;
+            if ((it & 63u) == 0) {
+                if (honour_abort && (*abort_flag || *(volatile uint32_t*)(header + kErrFlags))) {
+                    *abort_flag = 1;
+                    return false;
+                }
+                if (globaltimer() - t0 > timeout_ns) {
+                    *abort_flag = 1;
+                    atomicOr(header + kErrFlags, kErrTimeoutFlag);
+                    atomicExch(header + kErrWhere, (uint32_t)site);
+                    return false;
+                }
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ int64_t natural_token(int layout, int r, int64_t j, int64_t n, int64_t m, int n_cp) {
+    if (layout == CPATTN_CONTIGUOUS) return (int64_t)r * n + j;
+    if (layout == CPATTN_ZIGZAG) return j < m ? (int64_t)r * m + j : (int64_t)(2 * n_cp - 1 - r) * m + (j - m);
+    return j * n_cp + r;
+}
+
+// Tile classes from the position ranges of a query tile and a key tile (exact for the mask
+// pos[u] <= pos[t]): SKIP if every key follows every query, FULL if every key precedes every
+// query, DIAG otherwise.
+__device__ __forceinline__ int tile_class(int causal, int4 q, int4 k) {
+    if (!causal) return CPATTN_TILE_FULL;
+    if (k.x > q.y) return CPATTN_TILE_SKIP;
+    if (k.y <= q.x) return CPATTN_TILE_FULL;
+    return CPATTN_TILE_DIAG;
+}
+
+// ---- shared-memory layout and barriers (both tcgen05 kernels) --------------------------
+// fixed pair: the CTA's own two tiles (K, V for dK/dV; Q, dO for dQ), loaded once;
+// stream pair: the walked tiles (Q, dO for dK/dV; K, V for dQ), kNS stages;
+// side: per stage 2 x 128 floats (lse2 and D of the query tile, dK/dV only), bulk-copied.
+template <int D>
+struct BCfg {
+    static constexpr int PANELS = D / 64;
+    static constexpr int PANEL_BYTES = 128 * 128;
+    static constexpr int TILE = 128 * D * 2;
+    static constexpr int OFF_F0 = 0, OFF_F1 = TILE;                 // fixed pair
+    static constexpr int OFF_S = 2 * TILE;                          // stream: stage st, member m at + (2 st + m) TILE
+    static constexpr int OFF_SIDE = OFF_S + 2 * kNS * TILE;         // float [kNS][2][128]
+    static constexpr int OFF_BAR = OFF_SIDE + kNS * 2 * 128 * 4;
+    static constexpr int NBAR = 6 + 2 * kNS + kRing;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_RING = (OFF_MISC + 64 + 15) / 16 * 16;   // int4 [kRing]
+    static constexpr int SMEM_BYTES = OFF_RING + 16 * kRing + 1024;
+    static_assert(OFF_S % 1024 == 0 && OFF_SIDE % 16 == 0 && OFF_BAR % 8 == 0 && OFF_RING % 16 == 0,
+                  "shared-memory regions must keep their alignment");
+    // tensor memory: two accumulators (A0, A1) and two score-shaped buffers (X0, X1)
+    static constexpr uint32_t COL_A0 = 0, COL_A1 = D, COL_X0 = 2 * D, COL_X1 = 2 * D + 128;
+};
+
+template <int D>
+struct BBars {
+    uint32_t base;
+    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
+    __device__ uint32_t fixed_full() const { return at(0); }
+    __device__ uint32_t x_full() const { return at(1); }        // both score-shaped MMAs done
+    __device__ uint32_t p_full() const { return at(2); }        // elementwise results in TMEM
+    __device__ uint32_t acc_done() const { return at(3); }      // accumulating MMAs of a step done
+    __device__ uint32_t drain() const { return at(4); }
+    __device__ uint32_t spare() const { return at(5); }
+    __device__ uint32_t st_full(int s) const { return at(6 + s); }
+    __device__ uint32_t st_empty(int s) const { return at(6 + kNS + s); }
+    __device__ uint32_t ring_full(int s) const { return at(6 + 2 * kNS + s); }
+    __device__ void init() const {
+        mbar_init(fixed_full(), 1);
+        mbar_init(x_full(), 1);
+        mbar_init(p_full(), 8);                 // one lane per elementwise warp
+        mbar_init(acc_done(), 1);
+        mbar_init(drain(), 1);
+        mbar_init(spare(), 1);
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(st_full(s), 1);
+            mbar_init(st_empty(s), 1);
+        }
+        for (int s = 0; s < kRing; ++s) mbar_init(ring_full(s), 1);
+    }
+};
+
+// A step of the walk, as published by the producer: x, y = rank and tile of the streamed tile,
+// z = head (dK/dV) or source rank (dQ), w = class | mask << 2 | last << 3 | empty << 4.
+constexpr int kFlagLast = 8, kFlagEmpty = 16;
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// =============================================================================================
+// bwd_prep_kernel: one thread per 8 consecutive d of one (b, t, head) row. D_t is reduced over
+// the row's d/8 threads with shuffles.
+// =============================================================================================
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                       const float* __restrict__ lse, uint4* __restrict__ doL,
+                                                       float* __restrict__ lse2L, float* __restrict__ DL, int B,
+                                                       int64_t T, int64_t n, int64_t m, int64_t n_pad, int h, int d,
+                                                       int n_cp, int layout) {
+    const int cpr = d / 8;                       // 8 or 16 threads per row, aligned within the warp
+    const int64_t total = (int64_t)B * T * h * cpr;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const bool act = i < total;
+        float part = 0.f;
+        int c = 0;
+        int64_t row = 0;
+        if (act) {
+            c = (int)(i % cpr);
+            row = i / cpr;                        // (b, t, head)
+            const uint4 a = __ldg(o + i), g = __ldg(dout + i);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                part += __uint_as_float(aw[e] << 16) * __uint_as_float(gw[e] << 16);
+                part += __uint_as_float(aw[e] & 0xFFFF0000u) * __uint_as_float(gw[e] & 0xFFFF0000u);
+            }
+        }
+        for (int off = cpr / 2; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        if (!act) continue;
+        const int hd = (int)(row % h);
+        const int64_t bt = row / h;
+        const int64_t t = bt % T;
+        const int b = (int)(bt / T);
+        int r;
+        int64_t j;
+        if (layout == CPATTN_CONTIGUOUS) { r = (int)(t / n); j = t - (int64_t)r * n; }
+        else if (layout == CPATTN_ZIGZAG) {
+            const int ch = (int)(t / m);
+            if (ch < n_cp) { r = ch; j = t - (int64_t)ch * m; }
+            else { r = 2 * n_cp - 1 - ch; j = m + (t - (int64_t)ch * m); }
+        } else { r = (int)(t % n_cp); j = t / n_cp; }
+        const int64_t lrow = (((int64_t)r * B + b) * h + hd) * n + j;
+        doL[lrow * cpr + c] = __ldg(dout + i);
+        if (c == 0) {
+            const int64_t prow = (((int64_t)r * B + b) * h + hd) * n_pad + j;
+            const float l = __ldg(lse + ((int64_t)b * h + hd) * T + t);
+            lse2L[prow] = l * kLog2e;             // -inf stays -inf: such a row has P = 0
+            DL[prow] = part;
+        }
+    }
+}
+
+// =============================================================================================
+// bwd_dkdv_kernel
+// =============================================================================================
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const BwdParams P) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    const uint32_t ring = sb + C::OFF_RING;
+    const BBars<D> bars{sb + C::OFF_BAR};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // unit: (b, kvh, src, kt)
+    const int n_units_per_bk = P.n_cp * P.n_qt;
+    const int kt = blockIdx.x % P.n_qt;
+    const int src = (blockIdx.x / P.n_qt) % P.n_cp;
+    const int kvh = (blockIdx.x / n_units_per_bk) % P.n_kv;
+    const int b = blockIdx.x / (n_units_per_bk * P.n_kv);
+
+    if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
+    __syncthreads();
+    if (*skip_flag) return;
+    if (threadIdx.x == 0) {
+        bars.init();
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmDO);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const BWaiter wait{abort_flag, P.header, P.timeout_ns};
+    const int4 kmm = __ldg(P.tile_mm + src * P.n_qt + kt);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: fixed K, V; walk (s, qt, head); stream Q, dO + side data
+            const int krow = (int)((((int64_t)src * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)kt * 128);
+            mbar_arrive_expect_tx(bars.fixed_full(), 2 * C::TILE);
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                tma_load_2d(sb + C::OFF_F0 + pn * C::PANEL_BYTES, &tmK, bars.fixed_full(), pn * 64, krow);
+                tma_load_2d(sb + C::OFF_F1 + pn * C::PANEL_BYTES, &tmV, bars.fixed_full(), pn * 64, krow);
+            }
+            int ns = 0;                 // steps published (each loads one stage, except an empty unit's)
+            int nl = 0;                 // stages loaded
+            bool ok = true;
+            int pending = -1;           // the last visible (r, qt), published one step late so "last" is known
+            int pend_r = 0, pend_qt = 0, pend_head = 0, pend_cls = 0, pend_mask = 0;
+            auto publish = [&](int r, int qt, int head, int flags) -> bool {
+                const int slot = ns % kRing;
+                const int st = ns % kNS;
+                if (!(flags & kFlagEmpty)) {
+                    if (ns >= kNS && !wait(bars.st_empty(st), ((ns / kNS) - 1) & 1, kBSiteStageEmpty)) return false;
+                    const int qrow = (int)((((int64_t)r * P.B + b) * P.h + head) * P.n + (int64_t)qt * 128);
+                    mbar_arrive_expect_tx(bars.st_full(st), 2 * C::TILE + 2 * 512);
+                    const uint32_t s0 = sb + C::OFF_S + (2 * st) * C::TILE, s1 = s0 + C::TILE;
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        tma_load_2d(s0 + pn * C::PANEL_BYTES, &tmQ, bars.st_full(st), pn * 64, qrow);
+                        tma_load_2d(s1 + pn * C::PANEL_BYTES, &tmDO, bars.st_full(st), pn * 64, qrow);
+                    }
+                    const uint32_t side = sb + C::OFF_SIDE + st * 2 * 512;
+                    const int64_t prow = (((int64_t)r * P.B + b) * P.h + head) * P.n_pad + (int64_t)qt * 128;
+                    bulk_copy_g2s(side, P.lse2L + prow, 512, bars.st_full(st));
+                    bulk_copy_g2s(side + 512, P.DL + prow, 512, bars.st_full(st));
+                    ++nl;
+                }
+                st_shared_v4(ring + 16u * (uint32_t)slot, (uint32_t)r, (uint32_t)qt, (uint32_t)head, (uint32_t)flags);
+                mbar_arrive(bars.ring_full(slot));
+                ++ns;
+                return true;
+            };
+            for (int s = 0; s < P.n_cp && ok; ++s) {
+                const int r = (src + s) % P.n_cp;         // the block's gradient is at rank src + s at step s
+                for (int qt = 0; qt < P.n_qt && ok; ++qt) {
+                    const int4 qmm = __ldg(P.tile_mm + r * P.n_qt + qt);
+                    const int cls = tile_class(P.causal, qmm, kmm);
+                    if (cls == CPATTN_TILE_SKIP) continue;
+                    const int qshort = (qt == P.n_qt - 1) && (P.n % 128) != 0;
+                    const int kshort = (kt == P.n_qt - 1) && (P.n % 128) != 0;
+                    const int mask = (cls != CPATTN_TILE_FULL) || qshort || kshort;
+                    for (int hi = 0; hi < P.g && ok; ++hi) {
+                        if (pending >= 0) ok = publish(pend_r, pend_qt, pend_head, pend_cls | (pend_mask << 2));
+                        pending = 1;
+                        pend_r = r; pend_qt = qt; pend_head = kvh * P.g + hi; pend_cls = cls; pend_mask = mask;
+                    }
+                }
+            }
+            if (ok) {
+                if (pending >= 0) ok = publish(pend_r, pend_qt, pend_head, pend_cls | (pend_mask << 2) | kFlagLast);
+                else ok = publish(0, 0, 0, kFlagEmpty | kFlagLast);
+            }
+            // wait (bounded) until every stage we filled has been consumed or, after an abort,
+            // has landed, before the CTA may exit
+            // the CTA exits only after its own copies have landed (bounded waits)
+            const int first = nl > kNS ? nl - kNS : 0;
+            for (int i = first; i < nl; ++i) wait(bars.st_full(i % kNS), (i / kNS) & 1, kBSiteStage, false);
+            wait(bars.fixed_full(), 0, kBSiteFixed, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issue
+            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // S^T: A = K (K-major), B = Q (K-major)
+            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // dV: A = P^T (TMEM), B = dO (MN-major)
+            const uint32_t sK = sb + C::OFF_F0, sV = sb + C::OFF_F1;
+            const uint32_t tS = tmem + C::COL_X0, tDP = tmem + C::COL_X1;
+            const uint32_t tdV = tmem + C::COL_A0, tdK = tmem + C::COL_A1;
+            bool ok = wait(bars.fixed_full(), 0, kBSiteFixed);
+            int step = 0;
+            while (ok) {
+                const int slot = step % kRing, st = step % kNS;
+                if (!wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk)) break;
+                const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
+                if (e.w & kFlagEmpty) break;
+                if (!wait(bars.st_full(st), (step / kNS) & 1, kBSiteStage)) break;
+                tc_fence_after();
+                const uint32_t sQ = sb + C::OFF_S + (2 * st) * C::TILE, sDO = sQ + C::TILE;
+                // S^T = K Q^T and dP^T = V dO^T (the previous step's accumulating MMAs, issued
+                // before these by this thread, have read P^T / dS^T already: MMAs run in order)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(tS, desc_sw128(sK + off, 16, 1024), desc_sw128(sQ + off, 16, 1024), kIdSS, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(tDP, desc_sw128(sV + off, 16, 1024), desc_sw128(sDO + off, 16, 1024), kIdSS, kk > 0);
+                }
+                mma_commit(bars.x_full());
+                if (!wait(bars.p_full(), step & 1, kBSiteP)) break;
+                tc_fence_after();
+                // dV += P^T dO, dK += dS^T Q. P^T / dS^T: query columns 0..63 packed into columns
+                // 0..31 of their buffer, 64..127 into 64..95 (each warpgroup writes inside its own half).
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_bf16_ts(tdV, tS + acol, desc_sw128(sDO + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
+                                (step > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_bf16_ts(tdK, tDP + acol, desc_sw128(sQ + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
+                                (step > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bars.st_empty(st));
+                mma_commit(bars.acc_done());
+                ++step;
+                if (e.w & kFlagLast) break;
+            }
+            mma_commit(bars.drain());
+            wait(bars.drain(), 0, kBSiteDrain, false);
+        }
+    } else if (warp >= 4) {
+        // ---------------- elementwise: warpgroup wg takes query columns 64 wg .. 64 wg + 63
+        const int wg = (warp - 4) >> 2, quarter = warp & 3;
+        const int row = quarter * 32 + lane;                      // key row of the tile (TMEM lane)
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int64_t jk = (int64_t)kt * 128 + row;               // local key index on rank src
+        const bool key_valid = jk < P.n;
+        const int kpos = key_valid ? __ldg(P.posL + (int64_t)src * P.n + jk) : INT_MAX;
+        bool ok = true;
+        int step = 0;
+        int n_steps = 0;
+        for (;;) {
+            const int slot = step % kRing, st = step % kNS;
+            ok = __all_sync(0xffffffffu, wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk));
+            if (!ok) break;
+            const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
+            if (e.w & kFlagEmpty) break;
+            const int qt = e.y, tmask = (e.w >> 2) & 1;
+            int qvalid = 128;
+            if (qt == P.n_qt - 1 && (P.n % 128) != 0) qvalid = (int)(P.n - (int64_t)qt * 128);
+            ok = __all_sync(0xffffffffu, wait(bars.x_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t side = sb + C::OFF_SIDE + st * 2 * 512;   // lse2 [128], D [128]
+            const int32_t* qposg = P.posL + (int64_t)e.x * P.n + (int64_t)qt * 128;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const int c0 = wg * 64 + ch * 32;                    // first query column of the chunk
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
+                tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
+                uint32_t pp[16], pd[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const int4 l4 = ld_shared_v4(side + 4u * (uint32_t)(c0 + 4 * q4));
+                    const int4 d4 = ld_shared_v4(side + 512u + 4u * (uint32_t)(c0 + 4 * q4));
+                    const float lv[4] = {__int_as_float(l4.x), __int_as_float(l4.y), __int_as_float(l4.z), __int_as_float(l4.w)};
+                    const float dv[4] = {__int_as_float(d4.x), __int_as_float(d4.y), __int_as_float(d4.z), __int_as_float(d4.w)};
+                    float pv[4], sv[4];
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const int col = c0 + 4 * q4 + e4;
+                        const float x = __uint_as_float(sr[4 * q4 + e4]);
+                        bool vis = true;
+                        if (tmask) {
+                            const int qp = (col < qvalid) ? __ldg(qposg + col) : INT_MIN;
+                            vis = key_valid && col < qvalid && (!P.causal || kpos <= qp);
+                        }
+                        const float p = vis ? ex2(fmaf(x, P.scale_log2, -lv[e4])) : 0.f;
+                        pv[e4] = p;
+                        sv[e4] = vis ? p * (__uint_as_float(dr[4 * q4 + e4]) - dv[e4]) : 0.f;
+                    }
+                    pp[2 * q4] = pack_bf16(pv[0], pv[1]);
+                    pp[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
+                    pd[2 * q4] = pack_bf16(sv[0], sv[1]);
+                    pd[2 * q4 + 1] = pack_bf16(sv[2], sv[3]);
+                }
+                // packed column of query c: (c % 64) / 2 + 64 * (c / 64), inside this warpgroup's half
+                const uint32_t pcol = (uint32_t)(wg * 64 + ch * 16);
+                tmem_st16(tmem + lane_base + C::COL_X0 + pcol, pp);
+                tmem_st16(tmem + lane_base + C::COL_X1 + pcol, pd);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full());
+            ++step;
+            ++n_steps;
+            if (e.w & kFlagLast) break;
+        }
+        // epilogue: wait for the last accumulating MMAs, then write dK (scaled) and dV
+        if (ok && n_steps > 0) {
+            ok = __all_sync(0xffffffffu, wait(bars.acc_done(), (n_steps - 1) & 1, kBSiteDone));
+            if (ok) tc_fence_after();
+        }
+        // tcgen05.ld is a warp-wide instruction: every lane loads, and only the lanes of valid
+        // keys store (the last key tile of a block may be short)
+        if (ok) {
+            const int64_t tn = key_valid ? natural_token(P.layout, src, jk, P.n, P.m, P.n_cp) : 0;
+            uint4* gk = reinterpret_cast<uint4*>(P.dk + (((int64_t)b * P.T + tn) * P.n_kv + kvh) * D);
+            uint4* gv = reinterpret_cast<uint4*>(P.dv + (((int64_t)b * P.T + tn) * P.n_kv + kvh) * D);
+            // each warpgroup writes half of the columns of both gradients
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col0 = (which ? C::COL_A1 : C::COL_A0) + (uint32_t)(wg * (D / 2));
+                const float mul = which ? P.scale : 1.0f;
+                uint4* g = which ? gk : gv;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t t[32];
+                    if (n_steps > 0) {
+                        tmem_ld32(tmem + lane_base + col0 + c * 32, t);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) t[q] = 0u;
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(t[8 * q4 + 0]) * mul, __uint_as_float(t[8 * q4 + 1]) * mul);
+                        v.y = pack_bf16(__uint_as_float(t[8 * q4 + 2]) * mul, __uint_as_float(t[8 * q4 + 3]) * mul);
+                        v.z = pack_bf16(__uint_as_float(t[8 * q4 + 4]) * mul, __uint_as_float(t[8 * q4 + 5]) * mul);
+                        v.w = pack_bf16(__uint_as_float(t[8 * q4 + 6]) * mul, __uint_as_float(t[8 * q4 + 7]) * mul);
+                        if (key_valid) g[(wg * (D / 2) + c * 32) / 8 + q4] = v;
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// =============================================================================================
+// bwd_dq_kernel
+// =============================================================================================
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const BwdParams P) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* skip_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+    const uint32_t ring = sb + C::OFF_RING;
+    const BBars<D> bars{sb + C::OFF_BAR};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // unit: (b, head, r, qt)
+    const int qt = blockIdx.x % P.n_qt;
+    const int r = (blockIdx.x / P.n_qt) % P.n_cp;
+    const int head = (blockIdx.x / (P.n_qt * P.n_cp)) % P.h;
+    const int b = blockIdx.x / (P.n_qt * P.n_cp * P.h);
+    const int kvh = head / P.g;
+
+    if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
+    __syncthreads();
+    if (*skip_flag) return;
+    if (threadIdx.x == 0) {
+        bars.init();
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmDO);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const BWaiter wait{abort_flag, P.header, P.timeout_ns};
+    const int4 qmm = __ldg(P.tile_mm + r * P.n_qt + qt);
+    const int qrow0 = (int)((((int64_t)r * P.B + b) * P.h + head) * P.n + (int64_t)qt * 128);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: fixed Q, dO; walk the key tiles in ring order
+            mbar_arrive_expect_tx(bars.fixed_full(), 2 * C::TILE);
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+                tma_load_2d(sb + C::OFF_F0 + pn * C::PANEL_BYTES, &tmQ, bars.fixed_full(), pn * 64, qrow0);
+                tma_load_2d(sb + C::OFF_F1 + pn * C::PANEL_BYTES, &tmDO, bars.fixed_full(), pn * 64, qrow0);
+            }
+            int ns = 0, nl = 0;         // steps published, stages loaded
+            bool ok = true;
+            int pending = -1, pend_src = 0, pend_kt = 0, pend_flags = 0;
+            auto publish = [&](int srcr, int ktt, int flags) -> bool {
+                const int slot = ns % kRing, st = ns % kNS;
+                if (!(flags & kFlagEmpty)) {
+                    if (ns >= kNS && !wait(bars.st_empty(st), ((ns / kNS) - 1) & 1, kBSiteStageEmpty)) return false;
+                    const int krow = (int)((((int64_t)srcr * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)ktt * 128);
+                    mbar_arrive_expect_tx(bars.st_full(st), 2 * C::TILE);
+                    const uint32_t s0 = sb + C::OFF_S + (2 * st) * C::TILE, s1 = s0 + C::TILE;
+                    for (int pn = 0; pn < C::PANELS; ++pn) {
+                        tma_load_2d(s0 + pn * C::PANEL_BYTES, &tmK, bars.st_full(st), pn * 64, krow);
+                        tma_load_2d(s1 + pn * C::PANEL_BYTES, &tmV, bars.st_full(st), pn * 64, krow);
+                    }
+                    ++nl;
+                }
+                st_shared_v4(ring + 16u * (uint32_t)slot, (uint32_t)srcr, (uint32_t)ktt, 0u, (uint32_t)flags);
+                mbar_arrive(bars.ring_full(slot));
+                ++ns;
+                return true;
+            };
+            for (int s = 0; s < P.n_cp && ok; ++s) {
+                const int srcr = (r - s + P.n_cp) % P.n_cp;     // the block rank r holds at step s
+                for (int ktt = 0; ktt < P.n_qt && ok; ++ktt) {
+                    const int4 kmm = __ldg(P.tile_mm + srcr * P.n_qt + ktt);
+                    const int cls = tile_class(P.causal, qmm, kmm);
+                    if (cls == CPATTN_TILE_SKIP) continue;
+                    const int qshort = (qt == P.n_qt - 1) && (P.n % 128) != 0;
+                    const int kshort = (ktt == P.n_qt - 1) && (P.n % 128) != 0;
+                    const int mask = (cls != CPATTN_TILE_FULL) || qshort || kshort;
+                    if (pending >= 0) ok = publish(pend_src, pend_kt, pend_flags);
+                    pending = 1;
+                    pend_src = srcr; pend_kt = ktt; pend_flags = cls | (mask << 2);
+                }
+            }
+            if (ok) {
+                if (pending >= 0) ok = publish(pend_src, pend_kt, pend_flags | kFlagLast);
+                else ok = publish(0, 0, kFlagEmpty | kFlagLast);
+            }
+            // the CTA exits only after its own copies have landed (bounded waits)
+            const int first = nl > kNS ? nl - kNS : 0;
+            for (int i = first; i < nl; ++i) wait(bars.st_full(i % kNS), (i / kNS) & 1, kBSiteStage, false);
+            wait(bars.fixed_full(), 0, kBSiteFixed, false);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issue
+            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // S: A = Q, B = K (both K-major)
+            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // dQ: A = dS (TMEM), B = K (MN-major)
+            const uint32_t sQ = sb + C::OFF_F0, sDO = sb + C::OFF_F1;
+            const uint32_t tS = tmem + C::COL_X0, tDP = tmem + C::COL_X1, tdQ = tmem + C::COL_A0;
+            bool ok = wait(bars.fixed_full(), 0, kBSiteFixed);
+            int step = 0;
+            while (ok) {
+                const int slot = step % kRing, st = step % kNS;
+                if (!wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk)) break;
+                const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
+                if (e.w & kFlagEmpty) break;
+                if (!wait(bars.st_full(st), (step / kNS) & 1, kBSiteStage)) break;
+                tc_fence_after();
+                const uint32_t sK = sb + C::OFF_S + (2 * st) * C::TILE, sV = sK + C::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(tS, desc_sw128(sQ + off, 16, 1024), desc_sw128(sK + off, 16, 1024), kIdSS, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(tDP, desc_sw128(sDO + off, 16, 1024), desc_sw128(sV + off, 16, 1024), kIdSS, kk > 0);
+                }
+                mma_commit(bars.x_full());
+                if (!wait(bars.p_full(), step & 1, kBSiteP)) break;
+                tc_fence_after();
+                // dQ += dS K; dS packed like P^T in the dK/dV kernel (keys 64..127 at columns 64..95)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+                    mma_bf16_ts(tdQ, tS + acol, desc_sw128(sK + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
+                                (step > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(bars.st_empty(st));
+                mma_commit(bars.acc_done());
+                ++step;
+                if (e.w & kFlagLast) break;
+            }
+            mma_commit(bars.drain());
+            wait(bars.drain(), 0, kBSiteDrain, false);
+        }
+    } else if (warp >= 4) {
+        // ---------------- elementwise: warpgroup wg takes key columns 64 wg .. 64 wg + 63
+        const int wg = (warp - 4) >> 2, quarter = warp & 3;
+        const int row = quarter * 32 + lane;                      // query row of the tile (TMEM lane)
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int64_t jq = (int64_t)qt * 128 + row;
+        const bool q_valid = jq < P.n;
+        const int64_t lrow = (((int64_t)r * P.B + b) * P.h + head) * P.n_pad + jq;
+        const int qpos = q_valid ? __ldg(P.posL + (int64_t)r * P.n + jq) : INT_MIN;
+        const float lse2 = q_valid ? __ldg(P.lse2L + lrow) : -INFINITY;
+        const float Dv = q_valid ? __ldg(P.DL + lrow) : 0.f;
+        bool ok = true;
+        int step = 0, n_steps = 0;
+        for (;;) {
+            const int slot = step % kRing;
+            ok = __all_sync(0xffffffffu, wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk));
+            if (!ok) break;
+            const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
+            if (e.w & kFlagEmpty) break;
+            const int srcr = e.x, ktt = e.y, tmask = (e.w >> 2) & 1;
+            int kvalid = 128;
+            if (ktt == P.n_qt - 1 && (P.n % 128) != 0) kvalid = (int)(P.n - (int64_t)ktt * 128);
+            const int64_t kbase = (int64_t)srcr * P.n + (int64_t)ktt * 128;
+            ok = __all_sync(0xffffffffu, wait(bars.x_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                const int c0 = wg * 64 + ch * 32;
+                uint32_t sr[32], dr[32];
+                tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
+                tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
+                uint32_t pd[16];
+#pragma unroll
+                for (int q2 = 0; q2 < 16; ++q2) {
+                    float sv[2];
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const int col = c0 + 2 * q2 + e2;
+                        bool vis = q_valid && lse2 != -INFINITY;
+                        if (tmask) {
+                            const int kp = (col < kvalid) ? __ldg(P.posL + kbase + col) : INT_MAX;
+                            vis = vis && col < kvalid && (!P.causal || kp <= qpos);
+                        }
+                        const float p = vis ? ex2(fmaf(__uint_as_float(sr[2 * q2 + e2]), P.scale_log2, -lse2)) : 0.f;
+                        sv[e2] = vis ? p * (__uint_as_float(dr[2 * q2 + e2]) - Dv) : 0.f;
+                    }
+                    pd[q2] = pack_bf16(sv[0], sv[1]);
+                }
+                tmem_st16(tmem + lane_base + C::COL_X0 + (uint32_t)(wg * 64 + ch * 16), pd);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full());
+            ++step;
+            ++n_steps;
+            if (e.w & kFlagLast) break;
+        }
+        if (ok && n_steps > 0) {
+            ok = __all_sync(0xffffffffu, wait(bars.acc_done(), (n_steps - 1) & 1, kBSiteDone));
+            if (ok) tc_fence_after();
+        }
+        // warp-wide TMEM loads; only the lanes of valid query rows store
+        if (ok) {
+            const int64_t tn = q_valid ? natural_token(P.layout, r, jq, P.n, P.m, P.n_cp) : 0;
+            uint4* g = reinterpret_cast<uint4*>(P.dq + (((int64_t)b * P.T + tn) * P.h + head) * D);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t t[32];
+                if (n_steps > 0) {
+                    tmem_ld32(tmem + lane_base + C::COL_A0 + wg * (D / 2) + c * 32, t);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) t[q] = 0u;
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v;
+                    v.x = pack_bf16(__uint_as_float(t[8 * q4 + 0]) * P.scale, __uint_as_float(t[8 * q4 + 1]) * P.scale);
+                    v.y = pack_bf16(__uint_as_float(t[8 * q4 + 2]) * P.scale, __uint_as_float(t[8 * q4 + 3]) * P.scale);
+                    v.z = pack_bf16(__uint_as_float(t[8 * q4 + 4]) * P.scale, __uint_as_float(t[8 * q4 + 5]) * P.scale);
+                    v.w = pack_bf16(__uint_as_float(t[8 * q4 + 6]) * P.scale, __uint_as_float(t[8 * q4 + 7]) * P.scale);
+                    if (q_valid) g[(wg * (D / 2) + c * 32) / 8 + q4] = v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
+    using C = BCfg<D>;
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return (int)e;
+        attr_dev = dev;
+    }
+    CUtensorMap tq, tdo, tk, tv;
+    const uint64_t qrows = (uint64_t)a.n_cp * a.B * a.h * a.n, kvrows = (uint64_t)a.n_cp * a.B * a.n_kv * a.n;
+    if (!make_map(&tq, a.qL, qrows, D) || !make_map(&tdo, a.doL, qrows, D) || !make_map(&tk, a.kL, kvrows, D) ||
+        !make_map(&tv, a.vL, kvrows, D)) {
+        *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor shape)";
+        return (int)cudaErrorInvalidValue;
+    }
+    BwdParams P{};
+    P.B = a.B; P.h = a.h; P.n_kv = a.n_kv; P.g = a.h / a.n_kv; P.n_cp = a.n_cp; P.n_qt = a.n_qt;
+    P.causal = a.causal; P.layout = a.layout; P.n = a.n; P.m = a.m; P.T = a.T; P.n_pad = (int64_t)a.n_qt * 128;
+    P.scale = a.scale; P.scale_log2 = a.scale * kLog2e;
+    P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm);
+    P.lse2L = a.lse2L; P.DL = a.DL;
+    P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
+    P.header = a.header; P.timeout_ns = a.timeout_ns;
+    const int64_t kv_units = (int64_t)a.B * a.n_kv * a.n_cp * a.n_qt, q_units = (int64_t)a.B * a.h * a.n_cp * a.n_qt;
+    if (kv_units > INT_MAX || q_units > INT_MAX) {
+        *why = "too many work units";
+        return (int)cudaErrorInvalidValue;
+    }
+    bwd_dkdv_kernel<D><<<(int)kv_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+    int e = (int)cudaGetLastError();
+    if (e) return e;
+    bwd_dq_kernel<D><<<(int)q_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int launch_bwd_prep(const BwdPrepArgs& a, void* stream) {
+    const int64_t work = (int64_t)a.B * a.T * a.h * (a.d / 8);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (work + 255) / 256, cap = (int64_t)sms * 8;
+    bwd_prep_kernel<<<(int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, static_cast<uint4*>(a.doL), a.lse2L,
+        a.DL, a.B, a.T, a.n, a.m, (int64_t)a.n_qt * 128, a.h, a.d, a.n_cp, a.layout);
+    return (int)cudaGetLastError();
+}
+
+int launch_backward(const BwdLaunch& a, void* stream, std::string* why) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (a.d == 128) return launch_bwd_d<128>(a, st, why);
+    if (a.d == 64) return launch_bwd_d<64>(a, st, why);
+    *why = "unsupported head width";
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace cpattn

@@ -38,6 +38,11 @@ struct WsLayout {
     size_t o_run = 0;       // fp32 [n_cp][B][h][n][d] running output (normalised)
     size_t lse_run = 0;     // fp32 [n_cp][B][h][n] running lse
     size_t ring_end = 0;
+    // backward (after fwd_end; the ring-step regions are not used by the backward)
+    size_t doL = 0;         // bf16 [n_cp][B][h][n][d] output gradient in layout order
+    size_t lse2 = 0;        // fp32 [n_cp][B][h][n_qt * 128] forward lse times log2(e)
+    size_t Dl = 0;          // fp32 [n_cp][B][h][n_qt * 128] D = <dO, O> of every query row
+    size_t bwd_end = 0;
 };
 
 struct Plan {
@@ -97,5 +102,24 @@ int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const 
                  float* lse, void* stream);
 
 int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
+
+struct BwdPrepArgs {
+    int B; int64_t T, n, m; int h, d, n_cp, layout, n_qt;
+    const void* o; const void* dout; const float* lse;   // natural order
+    void* doL; float* lse2L; float* DL;                  // layout order
+};
+int launch_bwd_prep(const BwdPrepArgs& a, void* stream);
+
+struct BwdLaunch {
+    int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt;
+    float scale;
+    const void* qL; const void* kL; const void* vL; const void* doL;
+    const float* lse2L; const float* DL;
+    const int32_t* posL; const int32_t* tile_mm;
+    void* dq; void* dk; void* dv;                         // natural order, bf16
+    uint32_t* header;
+    uint64_t timeout_ns;
+};
+int launch_backward(const BwdLaunch& a, void* stream, std::string* why);
 
 }  // namespace cpattn

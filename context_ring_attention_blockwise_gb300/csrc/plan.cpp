@@ -47,6 +47,13 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.o_run = take(4 * (size_t)B * T * p.h * d);
     w.lse_run = take(4 * (size_t)B * T * p.h);
     w.ring_end = off;
+    // the backward reuses the forward regions and appends its own after them
+    off = w.fwd_end;
+    const size_t padded = (size_t)p.n_cp * B * p.h * (size_t)p.n_qt * 128;
+    w.doL = take(2 * (size_t)B * T * p.h * d);
+    w.lse2 = take(4 * padded);
+    w.Dl = take(4 * padded);
+    w.bwd_end = off;
     return w;
 }
 

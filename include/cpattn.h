@@ -136,6 +136,25 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
 cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, void* ws, size_t ws_bytes,
                                 cpattn_stream_t stream);
 
+/* Backward pass ([CEX] "What context parallelism communicates": each rank keeps the gradient
+ * of its own queries; the key and value gradients travel back to their owners as a second
+ * circulating block of the ring, which on one GPU is a key tile's gradient accumulated over
+ * every rank's queries in ring order). For the loss L = sum <O, dO>:
+ *   P = exp(scale q.k - lse), D_t = <dO_t, O_t>, dS = P (<dO_t, v_u> - D_t),
+ *   dq = scale sum_u dS k_u,  dk = scale sum_t dS q_t,  dv = sum_t P dO_t
+ * (dk, dv summed over the query heads of each KV group).
+ *   q, k, v, pos, scale   as passed to cpattn_forward (natural order, device)
+ *   o [B,T,h,d_k] bf16, lse [B,h,T] fp32   the forward's outputs (device, read)
+ *   dout [B,T,h,d_k] bf16                  gradient of the loss w.r.t. o (device, read)
+ *   dq [B,T,h,d_k], dk, dv [B,T,n_kv,d_k]  bf16 gradients, natural order (device, written)
+ *   ws / ws_bytes  at least cpattn_backward_workspace_size(plan, B) bytes, 1024-byte aligned.
+ * Every pointer non-NULL and 16-byte aligned (pos may be NULL), or CPATTN_ERR_INVALID before any
+ * launch. Asynchronous on `stream`; device-side timeouts are read by cpattn_check. */
+cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,
+                                void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream);
+
 /* S-way log-sum-exp merge of partial attention results ([CEX] online-softmax paragraph: old
  * totals rescaled to a common maximum). For every row and head:
  *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).
