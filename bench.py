@@ -406,6 +406,26 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     ms = a.elapsed_time(b) / 2
     out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12}
     del wsr
+    # the backward pass: dq, dk, dv from the forward's o and lse and a synthetic output gradient
+    wsb = cp.alloc_workspace(plan.backward_workspace_size(w.B), dev)
+    dout = torch.randn(q.shape, dtype=torch.bfloat16, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    cp.backward(q, k, v, o, lse, dout, plan, ws=wsb, dq=dq, dk=dk, dv=dv, stream=stream)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(2):
+        cp.backward(q, k, v, o, lse, dout, plan, ws=wsb, dq=dq, dk=dk, dv=dv, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsb)
+    ms = a.elapsed_time(b) / 2
+    tf = 2.5 * flops_eff(w) / (ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    out["backward"] = {"ms": ms, "tflops_eff": tf, "frac_of_bf16_sustained": tf / peak,
+                       "convention": "2.5 x the forward's effective FLOPs (five GEMMs per visible tile pair); "
+                                     "the kernels compute seven (dQ recomputes S and dP)",
+                       "includes": "placement, D = <dO, O> prep, dK/dV kernel, dQ kernel"}
+    del wsb, dout, dq, dk, dv
     return out
 
 

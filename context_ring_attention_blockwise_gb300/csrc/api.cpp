@@ -241,6 +241,12 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
     pa.doL = at<char>(ws, w.doL); pa.lse2L = at<float>(ws, w.lse2); pa.DL = at<float>(ws, w.Dl);
     int e = cpattn::launch_bwd_prep(pa, st);
     if (e) return cuda_fail(e, "backward prep kernel");
+    const size_t nu = (size_t)p->n_cp * p->n_qt;
+    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), p->order_q.data(), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
+    if (!e)
+        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, p->order_kv.data(), sizeof(int32_t) * nu,
+                            cudaMemcpyHostToDevice, st);
+    if (e) return cuda_fail(e, "cudaMemcpyAsync(backward order)");
     cpattn::BwdLaunch a{};
     a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.n_kv = p->n_kv; a.d = p->d; a.n_cp = p->n_cp;
     a.layout = p->layout; a.causal = p->causal; a.n_qt = p->n_qt;
@@ -248,6 +254,7 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL); a.doL = at<char>(ws, w.doL);
     a.lse2L = at<float>(ws, w.lse2); a.DL = at<float>(ws, w.Dl);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    a.order_q = at<int32_t>(ws, w.bwd_order); a.order_kv = a.order_q + nu;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;

@@ -56,6 +56,8 @@ struct BwdParams {
     const int4* tile_mm;
     const float* lse2L;   // [n_cp][B][h][n_pad] lse * log2(e) (tile starts 512-byte aligned)
     const float* DL;      // [n_cp][B][h][n_pad]
+    const int32_t* order_q;    // (r * n_qt + qt), heaviest first
+    const int32_t* order_kv;   // (src * n_qt + kt), heaviest first
     uint16_t* dq;         // natural [B,T,h,d]
     uint16_t* dk;         // natural [B,T,n_kv,d]
     uint16_t* dv;
@@ -237,12 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BBars<D> bars{sb + C::OFF_BAR};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit: (b, kvh, src, kt)
-    const int n_units_per_bk = P.n_cp * P.n_qt;
-    const int kt = blockIdx.x % P.n_qt;
-    const int src = (blockIdx.x / P.n_qt) % P.n_cp;
-    const int kvh = (blockIdx.x / n_units_per_bk) % P.n_kv;
-    const int b = blockIdx.x / (n_units_per_bk * P.n_kv);
+    // unit: (b, kvh, src, kt); the key tiles in order of work, every (b, kvh) of one tile together
+    const int bk = blockIdx.x % (P.B * P.n_kv);
+    const int ut = __ldg(P.order_kv + blockIdx.x / (P.B * P.n_kv));
+    const int kt = ut % P.n_qt, src = ut / P.n_qt;
+    const int kvh = bk % P.n_kv, b = bk / P.n_kv;
 
     if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
     __syncthreads();
@@ -412,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t side = sb + C::OFF_SIDE + st * 2 * 512;   // lse2 [128], D [128]
-            const int32_t* qposg = P.posL + (int64_t)e.x * P.n + (int64_t)qt * 128;
+            const int64_t qoff = (int64_t)e.x * P.n + (int64_t)qt * 128;   // positions of the query tile
+            const int32_t* qposg = P.posL + qoff;
 #pragma unroll
             for (int ch = 0; ch < 2; ++ch) {
                 const int c0 = wg * 64 + ch * 32;                    // first query column of the chunk
@@ -420,6 +422,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
                 tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
                 uint32_t pp[16], pd[16];
+                // Which keys of the chunk this row sees: all of them on unmasked tiles (no branch in
+                // the element loop), else by position, one bit per query column.
+                uint32_t vis_bits = 0xffffffffu;
+                if (tmask) {
+                    vis_bits = 0u;
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const int col = c0 + 4 * q4;
+                        int4 qp4 = make_int4(INT_MIN, INT_MIN, INT_MIN, INT_MIN);
+                        if (col + 3 < qvalid && ((qoff + col) & 3) == 0) {   // 16-byte aligned: one vector load
+                            qp4 = __ldg(reinterpret_cast<const int4*>(qposg + col));
+                        } else {
+                            if (col < qvalid) qp4.x = __ldg(qposg + col);
+                            if (col + 1 < qvalid) qp4.y = __ldg(qposg + col + 1);
+                            if (col + 2 < qvalid) qp4.z = __ldg(qposg + col + 2);
+                            if (col + 3 < qvalid) qp4.w = __ldg(qposg + col + 3);
+                        }
+                        const int qp[4] = {qp4.x, qp4.y, qp4.z, qp4.w};
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const bool vis = key_valid && col + e4 < qvalid && (!P.causal || kpos <= qp[e4]);
+                            vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
                     const int4 l4 = ld_shared_v4(side + 4u * (uint32_t)(c0 + 4 * q4));
@@ -429,16 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float pv[4], sv[4];
 #pragma unroll
                     for (int e4 = 0; e4 < 4; ++e4) {
-                        const int col = c0 + 4 * q4 + e4;
-                        const float x = __uint_as_float(sr[4 * q4 + e4]);
-                        bool vis = true;
-                        if (tmask) {
-                            const int qp = (col < qvalid) ? __ldg(qposg + col) : INT_MIN;
-                            vis = key_valid && col < qvalid && (!P.causal || kpos <= qp);
-                        }
-                        const float p = vis ? ex2(fmaf(x, P.scale_log2, -lv[e4])) : 0.f;
-                        pv[e4] = p;
-                        sv[e4] = vis ? p * (__uint_as_float(dr[4 * q4 + e4]) - dv[e4]) : 0.f;
+                        const bool vis = (vis_bits >> (4 * q4 + e4)) & 1u;
+                        const float p = ex2(fmaf(__uint_as_float(sr[4 * q4 + e4]), P.scale_log2, -lv[e4]));
+                        const float ds = p * (__uint_as_float(dr[4 * q4 + e4]) - dv[e4]);
+                        pv[e4] = vis ? p : 0.f;
+                        sv[e4] = vis ? ds : 0.f;
                     }
                     pp[2 * q4] = pack_bf16(pv[0], pv[1]);
                     pp[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
@@ -525,11 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BBars<D> bars{sb + C::OFF_BAR};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit: (b, head, r, qt)
-    const int qt = blockIdx.x % P.n_qt;
-    const int r = (blockIdx.x / P.n_qt) % P.n_cp;
-    const int head = (blockIdx.x / (P.n_qt * P.n_cp)) % P.h;
-    const int b = blockIdx.x / (P.n_qt * P.n_cp * P.h);
+    // unit: (b, head, r, qt); the query tiles in order of work, every (b, head) of one tile together
+    const int bh = blockIdx.x % (P.B * P.h);
+    const int uq = __ldg(P.order_q + blockIdx.x / (P.B * P.h));
+    const int qt = uq % P.n_qt, r = uq / P.n_qt;
+    const int head = bh % P.h, b = bh / P.h;
     const int kvh = head / P.g;
 
     if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
@@ -666,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qpos = q_valid ? __ldg(P.posL + (int64_t)r * P.n + jq) : INT_MIN;
         const float lse2 = q_valid ? __ldg(P.lse2L + lrow) : -INFINITY;
         const float Dv = q_valid ? __ldg(P.DL + lrow) : 0.f;
+        const bool row_live = q_valid && lse2 != -INFINITY;   // a row that sees some key
         bool ok = true;
         int step = 0, n_steps = 0;
         for (;;) {
@@ -688,19 +711,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
                 tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
                 uint32_t pd[16];
+                // Which keys of the chunk this row sees: all of them on unmasked tiles, else by
+                // position (keys beyond a short block are never seen), one bit per key column.
+                uint32_t vis_bits = row_live ? 0xffffffffu : 0u;
+                if (tmask && row_live) {
+                    vis_bits = 0u;
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const int col = c0 + 4 * q4;
+                        int4 kp4 = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
+                        if (col + 3 < kvalid && ((kbase + col) & 3) == 0) {   // 16-byte aligned: one vector load
+                            kp4 = __ldg(reinterpret_cast<const int4*>(P.posL + kbase + col));
+                        } else {
+                            if (col < kvalid) kp4.x = __ldg(P.posL + kbase + col);
+                            if (col + 1 < kvalid) kp4.y = __ldg(P.posL + kbase + col + 1);
+                            if (col + 2 < kvalid) kp4.z = __ldg(P.posL + kbase + col + 2);
+                            if (col + 3 < kvalid) kp4.w = __ldg(P.posL + kbase + col + 3);
+                        }
+                        const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const bool vis = col + e4 < kvalid && (!P.causal || kp[e4] <= qpos);
+                            vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
+                        }
+                    }
+                }
 #pragma unroll
                 for (int q2 = 0; q2 < 16; ++q2) {
                     float sv[2];
 #pragma unroll
                     for (int e2 = 0; e2 < 2; ++e2) {
-                        const int col = c0 + 2 * q2 + e2;
-                        bool vis = q_valid && lse2 != -INFINITY;
-                        if (tmask) {
-                            const int kp = (col < kvalid) ? __ldg(P.posL + kbase + col) : INT_MAX;
-                            vis = vis && col < kvalid && (!P.causal || kp <= qpos);
-                        }
-                        const float p = vis ? ex2(fmaf(__uint_as_float(sr[2 * q2 + e2]), P.scale_log2, -lse2)) : 0.f;
-                        sv[e2] = vis ? p * (__uint_as_float(dr[2 * q2 + e2]) - Dv) : 0.f;
+                        const bool vis = (vis_bits >> (2 * q2 + e2)) & 1u;
+                        const float p = ex2(fmaf(__uint_as_float(sr[2 * q2 + e2]), P.scale_log2, -lse2));
+                        const float ds = p * (__uint_as_float(dr[2 * q2 + e2]) - Dv);
+                        sv[e2] = vis ? ds : 0.f;
                     }
                     pd[q2] = pack_bf16(sv[0], sv[1]);
                 }
@@ -777,7 +821,7 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     P.causal = a.causal; P.layout = a.layout; P.n = a.n; P.m = a.m; P.T = a.T; P.n_pad = (int64_t)a.n_qt * 128;
     P.scale = a.scale; P.scale_log2 = a.scale * kLog2e;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm);
-    P.lse2L = a.lse2L; P.DL = a.DL;
+    P.lse2L = a.lse2L; P.DL = a.DL; P.order_q = a.order_q; P.order_kv = a.order_kv;
     P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
     P.header = a.header; P.timeout_ns = a.timeout_ns;
     const int64_t kv_units = (int64_t)a.B * a.n_kv * a.n_cp * a.n_qt, q_units = (int64_t)a.B * a.h * a.n_cp * a.n_qt;

@@ -42,6 +42,7 @@ struct WsLayout {
     size_t doL = 0;         // bf16 [n_cp][B][h][n][d] output gradient in layout order
     size_t lse2 = 0;        // fp32 [n_cp][B][h][n_qt * 128] forward lse times log2(e)
     size_t Dl = 0;          // fp32 [n_cp][B][h][n_qt * 128] D = <dO, O> of every query row
+    size_t bwd_order = 0;   // int32 [2][n_cp * n_qt]: order_q, then order_kv
     size_t bwd_end = 0;
 };
 
@@ -52,6 +53,8 @@ struct Plan {
     int pair_heads = 0;             // a CTA pairs two heads of one KV group (else two adjacent q-tiles)
     int n_grp = 0;                  // row groups per rank: n_qt when pairing heads, ceil(n_qt / 2) otherwise
     std::vector<int32_t> order;     // (r * n_grp + group), longest first
+    std::vector<int32_t> order_q;   // backward: (r * n_qt + q-tile), most visible key tiles first
+    std::vector<int32_t> order_kv;  // backward: (r * n_qt + key tile), most visible query tiles first
     std::vector<int64_t> full, diag, skip;  // [n_cp][n_cp] by (rank, step), per (b, head)
     std::vector<int64_t> pairs;             // [n_cp]
     std::vector<int64_t> half_units;        // [n_cp]
@@ -116,6 +119,7 @@ struct BwdLaunch {
     const void* qL; const void* kL; const void* vL; const void* doL;
     const float* lse2L; const float* DL;
     const int32_t* posL; const int32_t* tile_mm;
+    const int32_t* order_q; const int32_t* order_kv;   // longest-first unit orders
     void* dq; void* dk; void* dv;                         // natural order, bf16
     uint32_t* header;
     uint64_t timeout_ns;

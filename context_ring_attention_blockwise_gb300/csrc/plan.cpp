@@ -53,6 +53,7 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.doL = take(2 * (size_t)B * T * p.h * d);
     w.lse2 = take(4 * padded);
     w.Dl = take(4 * padded);
+    w.bwd_order = take(sizeof(int32_t) * 2 * (size_t)p.n_cp * p.n_qt);
     w.bwd_end = off;
     return w;
 }
@@ -97,6 +98,7 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
     p.pair_heads = ((h / n_kv) % 2 == 0) ? 1 : 0;
     p.n_grp = p.pair_heads ? p.n_qt : (p.n_qt + 1) / 2;
     std::vector<int64_t> work((size_t)n_cp * p.n_grp, 0);  // key tiles a row group computes
+    std::vector<int64_t> work_q((size_t)n_cp * p.n_qt, 0), work_kv((size_t)n_cp * p.n_qt, 0);
     for (int r = 0; r < n_cp; ++r)
         for (int s = 0; s < n_cp; ++s) {
             int src = ((r - s) % n_cp + n_cp) % n_cp;
@@ -109,6 +111,10 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
                     if (c == CPATTN_TILE_FULL) ++p.full[rs];
                     else if (c == CPATTN_TILE_DIAG) ++p.diag[rs];
                     else ++p.skip[rs];
+                    if (c != CPATTN_TILE_SKIP) {
+                        ++work_q[qi];
+                        ++work_kv[ki];
+                    }
                 }
             }
             for (int grp = 0; grp < p.n_grp; ++grp) {
@@ -161,6 +167,13 @@ std::string build_plan(Plan& p, int64_t T, int h, int n_kv, int d, int n_cp, int
     p.order.resize((size_t)n_cp * p.n_grp);
     std::iota(p.order.begin(), p.order.end(), 0);
     std::stable_sort(p.order.begin(), p.order.end(), [&](int32_t a, int32_t b) { return work[a] > work[b]; });
+    // the backward launches one CTA per query tile (dQ) and per key tile (dK, dV), heaviest first
+    p.order_q.resize((size_t)n_cp * p.n_qt);
+    std::iota(p.order_q.begin(), p.order_q.end(), 0);
+    std::stable_sort(p.order_q.begin(), p.order_q.end(), [&](int32_t a, int32_t b) { return work_q[a] > work_q[b]; });
+    p.order_kv.resize((size_t)n_cp * p.n_qt);
+    std::iota(p.order_kv.begin(), p.order_kv.end(), 0);
+    std::stable_sort(p.order_kv.begin(), p.order_kv.end(), [&](int32_t a, int32_t b) { return work_kv[a] > work_kv[b]; });
     return "";
 }
 
