@@ -239,9 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BBars<D> bars{sb + C::OFF_BAR};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit: (b, kvh, src, kt); the key tiles in order of work, every (b, kvh) of one tile together
-    const int bk = blockIdx.x % (P.B * P.n_kv);
-    const int ut = __ldg(P.order_kv + blockIdx.x / (P.B * P.n_kv));
+    // unit: (b, kvh, src, kt), KV-head-major (the CTAs in flight share one head group's Q and dO
+    // in L2), heaviest key tile first within a head
+    const int n_tiles = P.n_cp * P.n_qt;
+    const int bk = blockIdx.x / n_tiles;
+    const int ut = __ldg(P.order_kv + blockIdx.x % n_tiles);
     const int kt = ut % P.n_qt, src = ut / P.n_qt;
     const int kvh = bk % P.n_kv, b = bk / P.n_kv;
 
@@ -547,11 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const BBars<D> bars{sb + C::OFF_BAR};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // unit: (b, head, r, qt); the query tiles in order of work, every (b, head) of one tile together
-    const int bh = blockIdx.x % (P.B * P.h);
-    const int uq = __ldg(P.order_q + blockIdx.x / (P.B * P.h));
+    // unit: (b, head, r, qt), KV-head-major (the CTAs in flight share one head's K and V in L2):
+    // per (b, KV head), the query tiles heaviest first, the group's query heads of a tile together
+    const int n_tiles = P.n_cp * P.n_qt;
+    const int per_bk = n_tiles * P.g;
+    const int bk = blockIdx.x / per_bk, rem = blockIdx.x % per_bk;
+    const int uq = __ldg(P.order_q + rem / P.g);
     const int qt = uq % P.n_qt, r = uq / P.n_qt;
-    const int head = bh % P.h, b = bh / P.h;
+    const int b = bk / P.n_kv, head = (bk % P.n_kv) * P.g + rem % P.g;
     const int kvh = head / P.g;
 
     if (threadIdx.x == 0) *skip_flag = (int)*(volatile uint32_t*)(P.header + kErrFlags);
