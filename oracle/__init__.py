@@ -72,6 +72,8 @@ def bind(path: str):
     lib.oracle_overlap_min_tokens.restype = ctypes.c_double
     lib.oracle_kv_bytes_recv.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.oracle_kv_bytes_recv.restype = _I64
+    lib.oracle_attention_docs.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
+                                          _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _P, _P]
     lib.oracle_attention_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                               _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _I64, _P, _P, _P, _P]
     lib.oracle_ring_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P,
@@ -138,6 +140,30 @@ class Oracle:
                                        int(causal), scale, R, rowsp, K, keysp, o.ctypes.data, lse.ctypes.data)
         if rc:
             raise ValueError("oracle_attention failed")
+        return o, lse
+
+    def attention_docs(self, q, k, v, doc, causal=True, scale=None, pos=None, rows=None):
+        """attention() under a document mask: doc [T] int document id per natural token."""
+        B, T, h, d = q.shape
+        n_kv = k.shape[2]
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        q, k, v = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v))
+        doc = np.ascontiguousarray(doc, dtype=np.int32)
+        posp = None
+        if pos is not None:
+            pos = np.ascontiguousarray(pos, dtype=np.int32)
+            posp = pos.ctypes.data
+        rowsp, R = None, T
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            rowsp, R = rows.ctypes.data, rows.size
+        o = np.empty((B, R, h, d), dtype=np.float64)
+        lse = np.empty((B, h, R), dtype=np.float64)
+        rc = self.lib.oracle_attention_docs(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data, posp,
+                                            doc.ctypes.data, int(causal), scale, R, rowsp, o.ctypes.data,
+                                            lse.ctypes.data)
+        if rc:
+            raise ValueError("oracle_attention_docs failed")
         return o, lse
 
     def ring(self, q, k, v, n_cp, layout, causal=True, scale=None, pos=None, block=16):

@@ -104,14 +104,24 @@ static int visible(const int32_t* pos, int64_t u, int64_t t, int causal) {
     return pu <= pt;
 }
 
+/* Document masks for packed sequences ([CEX] "What context parallelism communicates": the
+ * all-gather variant "makes arbitrary masks, such as document masks for packed sequences, easy
+ * to support"): with a document id per token, a query sees only keys of its own document (and,
+ * causal, only those at or before it). doc NULL: one document. */
+static int visible_doc(const int32_t* pos, const int32_t* doc, int64_t u, int64_t t, int causal) {
+    if (doc && doc[u] != doc[t]) return 0;
+    return visible(pos, u, t, causal);
+}
+
 /* q [B,T,h,d], k/v [B,T,n_kv,d] bf16 bits, natural order. rows: n_rows natural token ids or
  * NULL (all T, n_rows = T). keys: n_keys natural token ids the queries may attend to (one
  * block of the ring, or any key subset), or NULL for all T; a key outside the mask stays
  * hidden. o [B,n_rows,h,d] fp64, lse [B,h,n_rows] fp64 (-inf when a row sees no key, with
  * o = 0). Returns 0 on success. */
-int oracle_attention(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
-                     const uint16_t* v, const int32_t* pos, int causal, double scale, int64_t n_rows,
-                     const int64_t* rows, int64_t n_keys, const int64_t* keys, double* o, double* lse) {
+static int attention_impl(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const int32_t* pos, const int32_t* doc, int causal, double scale,
+                          int64_t n_rows, const int64_t* rows, int64_t n_keys, const int64_t* keys, double* o,
+                          double* lse) {
     if (B <= 0 || T <= 0 || h <= 0 || n_kv <= 0 || d <= 0 || h % n_kv) return 1;
     if (!rows) n_rows = T;
     if (!keys) n_keys = T;
@@ -139,7 +149,7 @@ int oracle_attention(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q
             double mx = -INFINITY;
             for (int64_t ki = 0; ki < n_keys; ++ki) {
                 int64_t u = keys ? keys[ki] : ki;
-                if (!visible(pos, u, t, causal)) continue;
+                if (!visible_doc(pos, doc, u, t, causal)) continue;
                 const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
                 double dot = 0.0;
                 for (int c = 0; c < d; ++c) dot += bf16_value(qrow[c]) * bf16_value(krow[c]);
@@ -158,7 +168,7 @@ int oracle_attention(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q
             for (int c = 0; c < d; ++c) acc[c] = 0.0;
             for (int64_t ki = 0; ki < n_keys; ++ki) {
                 int64_t u = keys ? keys[ki] : ki;
-                if (!visible(pos, u, t, causal)) continue;
+                if (!visible_doc(pos, doc, u, t, causal)) continue;
                 double e = exp(s[ki] - mx);
                 sum += e;
                 const uint16_t* vrow = v + (((int64_t)b * T + u) * n_kv + kv) * d;
@@ -171,6 +181,19 @@ int oracle_attention(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q
         free(acc);
     }
     return err;
+}
+
+int oracle_attention(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                     const uint16_t* v, const int32_t* pos, int causal, double scale, int64_t n_rows,
+                     const int64_t* rows, int64_t n_keys, const int64_t* keys, double* o, double* lse) {
+    return attention_impl(B, T, h, n_kv, d, q, k, v, pos, NULL, causal, scale, n_rows, rows, n_keys, keys, o, lse);
+}
+
+/* The same definition under a document mask: doc [T] int32 document id of each natural token. */
+int oracle_attention_docs(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const int32_t* pos, const int32_t* doc, int causal, double scale,
+                          int64_t n_rows, const int64_t* rows, double* o, double* lse) {
+    return attention_impl(B, T, h, n_kv, d, q, k, v, pos, doc, causal, scale, n_rows, rows, 0, NULL, o, lse);
 }
 
 /* ------------------------------------------------------------------------------------- */

@@ -420,4 +420,30 @@ def pin_backward_bytes(orc):
     assert abs(bwd / fwd - (2 + 1 / 15)) < 1e-12
 
 
+# --------------------------------------------------------------------------------------
+# Document masks (packed sequences)
+# --------------------------------------------------------------------------------------
+
+def pin_document_mask(orc):
+    """A query sees only its own document: against SDPA with the boolean document mask, and
+    against each document's attention computed on its own (the definition on a slice)."""
+    B, T, h, n_kv, d = 1, 40, 4, 2, 8
+    q, k, v = _qkv(41, B, T, h, n_kv, d)
+    lengths = [7, 1, 12, 20]
+    doc = np.repeat(np.arange(len(lengths)), lengths).astype(np.int32)
+    for causal in (True, False):
+        o, lse = orc.attention_docs(q, k, v, doc, causal=causal)
+        same = doc[None, :] == doc[:, None]
+        mask = same & (np.arange(T)[None, :] <= np.arange(T)[:, None]) if causal else same
+        ref = _sdpa(q, k, v, False, mask=torch.from_numpy(mask))
+        assert _maxabs(o, ref) < 1e-12, "document mask differs from SDPA with the same mask"
+        start = 0
+        for ln in lengths:
+            sl = slice(start, start + ln)
+            so, sl_lse = orc.attention(q[:, sl], k[:, sl], v[:, sl], causal=causal)
+            assert _maxabs(o[:, sl], so) < 1e-13 and _maxabs(lse[:, :, sl], sl_lse) < 1e-13, \
+                "a document's rows must equal attention over that document alone"
+            start += ln
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

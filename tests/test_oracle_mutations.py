@@ -61,6 +61,8 @@ MUTANTS = [
      "for (int i = kvh * g; i < kvh * g + 1; ++i)\n            for (int64_t t = 0; t < T; ++t) {", None),
     ("ring_bwd_own_block", "int src = ((r - s) % n_cp + n_cp) % n_cp;     /* block rank r holds at step s */",
      "int src = r;", None),
+    ("doc_mask_ignored", "if (doc && doc[u] != doc[t]) return 0;", "if (0) return 0;", None),
+    ("doc_mask_sees_earlier_docs", "if (doc && doc[u] != doc[t]) return 0;", "if (doc && doc[u] > doc[t]) return 0;", None),
     ("bwd_bytes_grad_hops", "(int64_t)n_cp * 2 * blk * grad_bytes", "(int64_t)(n_cp - 1) * 2 * blk * grad_bytes", None),
 ]
 
