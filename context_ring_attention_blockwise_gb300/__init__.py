@@ -26,7 +26,7 @@ SYMBOLS = [
     "cpattn_attend", "cpattn_forward_noalloc",
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
-    "cpattn_backward_workspace_size", "cpattn_backward",
+    "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked",
 ]
 
 
@@ -67,6 +67,7 @@ def lib():
     L.cpattn_tile_counts.argtypes = [_P, i, _P, _P, _P]
     L.cpattn_check.argtypes = [_P, _P]
     L.cpattn_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, u64, _P]
+    L.cpattn_forward_masked.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_last_error.restype = ctypes.c_char_p
@@ -226,6 +227,27 @@ def backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = 
                                  _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), _dev_ptr(ws, "ws"),
                                  ws.numel(), _stream_ptr(stream)), "cpattn_backward")
     return dq, dk, dv
+
+
+def forward_masked(q, k, v, plan: Plan, lo, pos=None, scale: float | None = None, ws=None, out=None, lse=None,
+                   stream=None):
+    """cpattn_forward_masked: like forward(), with lo [T] int32 CUDA tensor, the lowest key position
+    each query may see (document masks of packed sequences: the first token of its document)."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if tuple(lo.shape) != (plan.T,) or lo.dtype != torch.int32:
+        raise ValueError("lo must be an int32 tensor of T entries")
+    if ws is None:
+        ws = alloc_workspace(plan.workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    _check(lib().cpattn_forward_masked(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                       _dev_ptr(pos, "pos"), _dev_ptr(lo, "lo"), float(scale or 0.0),
+                                       _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"), ws.numel(),
+                                       _stream_ptr(stream)), "cpattn_forward_masked")
+    return out, lse
 
 
 def forward_noalloc(q, k, v, plan: Plan, pos=None, scale: float | None = None, out=None, lse=None, stream=None):

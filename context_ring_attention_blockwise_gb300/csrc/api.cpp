@@ -62,7 +62,7 @@ T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws)
 
 // Reset the header, upload the tile order, place tokens and position ids.
 cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
-                         cudaStream_t st) {
+                         cudaStream_t st, const int32_t* lo = nullptr) {
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
@@ -77,6 +77,7 @@ cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const voi
     a.q = q; a.k = k; a.v = v; a.pos = pos;
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    a.lo = lo; a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo);
     e = cpattn::launch_permute(a, st);
     if (e) return cuda_fail(e, "permute kernel");
     return CPATTN_OK;
@@ -261,6 +262,30 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
     std::string why;
     e = cpattn::launch_backward(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                      const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse, void* ws,
+                                      size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!p->causal) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query needs a causal plan");
+    if (!lo || !aligned16(lo)) return fail(CPATTN_ERR_INVALID, "lo must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, lo))) return s;
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.o = o; a.lse = lse;
+    a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo);
+    std::string why;
+    int e = launch_attn(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
 

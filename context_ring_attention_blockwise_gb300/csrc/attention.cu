@@ -6,7 +6,9 @@
 // adjacent query tiles of one head (otherwise). The unit walks the key/value blocks in ring order
 // ("Context and expert parallelism", "Pass them around a ring": at step s rank r holds the block
 // of rank (r - s) mod n_cp). It skips key tiles no query of the unit can see and masks the partly
-// visible ones ("The causal mask unbalances the sequence"). It keeps the online-softmax state of
+// visible ones ("The causal mask unbalances the sequence"). With document masks for packed
+// sequences ("What context parallelism communicates") every query also has a lowest visible key
+// position; a key is visible iff lo[t] <= pos[u] <= pos[t]. It keeps the online-softmax state of
 // the paragraph after the ring one on chip across every step: running max, running sum of
 // exponentials, running weighted sum of values, rescaled when a larger score arrives.
 //
@@ -62,6 +64,8 @@ struct Params {
     const int32_t* posL;
     const int4* tile_mm;
     const int32_t* order;
+    const int32_t* loL;    // [n_cp][n] lowest visible key position per query, or NULL
+    const int4* tile_lo;   // [n_cp][n_qt] (min, max) of loL over a query tile, or NULL
     int32_t* unit_tiles;   // [n_cp * n_grp]: key tiles of a unit of row group r * n_grp + group
     unsigned long long* counts;
     uint32_t* sched;
@@ -165,12 +169,34 @@ struct Unit {
     int r, b, kvh, rg;   // rank, batch element, KV head, row group r * n_grp + group
     int head[2], qt[2], valid[2];
     int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
+    int2 qlo[2];   // range of the tile's lowest visible key positions; (INT_MIN, INT_MIN) without one
 };
+
+// The query tiles' position ranges and (LB: with a per-query lower bound) lower-bound ranges.
+template <bool LB>
+__device__ __forceinline__ void unit_ranges(const Params& P, Unit& U) {
+    for (int i = 0; i < 2; ++i) {
+        if (U.valid[i]) {
+            const int4 t4 = __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]);
+            U.qmm[i] = make_int2(t4.x, t4.y);
+            if (LB) {
+                const int4 l4 = __ldg(P.tile_lo + U.r * P.n_qt + U.qt[i]);
+                U.qlo[i] = make_int2(l4.x, l4.y);
+            } else {
+                U.qlo[i] = make_int2(INT_MIN, INT_MIN);
+            }
+        } else {
+            U.qmm[i] = make_int2(INT_MAX, INT_MIN);
+            U.qlo[i] = make_int2(INT_MIN, INT_MIN);
+        }
+    }
+}
 
 // Units are numbered KV-head-major: all units of one (batch element, KV head) come before the
 // next, so the CTAs running at any moment read the keys and values of one or two KV heads and
 // those stay in L2. Within a KV head, (rank, row group) follow the plan's longest-first order,
 // then the query heads of the group.
+template <bool LB>
 __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
     Unit U;
     const int per = P.pair_heads ? P.g / 2 : P.g;        // units per (b, kvh, row group)
@@ -197,25 +223,21 @@ __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
         U.valid[0] = 1;
         U.valid[1] = U.qt[1] < P.n_qt;
     }
-    for (int i = 0; i < 2; ++i) {
-        if (U.valid[i]) {
-            const int4 t4 = __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]);
-            U.qmm[i] = make_int2(t4.x, t4.y);
-        } else {
-            U.qmm[i] = make_int2(INT_MAX, INT_MIN);
-        }
-    }
+    unit_ranges<LB>(P, U);
     return U;
 }
 
 // The key tiles a unit visits, in ring order, leaving out tiles that both query tiles skip.
 // cls(i): FULL / DIAG / SKIP for query tile i; mask(i): the tile needs the element mask for
 // query tile i (partly visible, skipped by this tile only, or shorter than 128 keys). A block
-// whose remaining tiles all start after every query of the unit is left in one step.
+// whose remaining tiles all start after every query of the unit is left in one step. LB: the
+// queries also have a lowest visible key position (document masks).
+template <bool LB>
 struct TileWalk {
     const Params* p;
     int r, s, s_end, kt, src;
     int qmin0, qmax0, qmin1, qmax1, qmax, cls0, cls1, mask0, mask1;
+    int lmin0, lmax0, lmin1, lmax1;   // lower-bound ranges of the two query tiles
     __device__ int cls(int i) const { return i ? cls1 : cls0; }
     __device__ int mask(int i) const { return i ? mask1 : mask0; }
     __device__ void init(const Params& P, const Unit& U) {
@@ -223,6 +245,8 @@ struct TileWalk {
         r = U.r;
         qmin0 = U.qmm[0].x; qmax0 = U.qmm[0].y;
         qmin1 = U.qmm[1].x; qmax1 = U.qmm[1].y;
+        lmin0 = U.qlo[0].x; lmax0 = U.qlo[0].y;
+        lmin1 = U.qlo[1].x; lmax1 = U.qlo[1].y;
         qmax = max(qmax0, qmax1);
         s = P.fused ? 0 : P.step;
         s_end = P.fused ? P.n_cp : P.step + 1;
@@ -248,8 +272,17 @@ struct TileWalk {
                 kt = P.n_qt - 1;
                 continue;
             }
-            cls0 = (t4.x > qmax0) ? CPATTN_TILE_SKIP : (t4.y > qmin0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
-            cls1 = (t4.x > qmax1) ? CPATTN_TILE_SKIP : (t4.y > qmin1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            if (LB) {
+                // SKIP: every key after every query, or below every query's lower bound; FULL: every
+                // key at or before every query and at or above every lower bound
+                cls0 = (t4.x > qmax0 || t4.y < lmin0) ? CPATTN_TILE_SKIP
+                       : (t4.y > qmin0 || t4.x < lmax0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+                cls1 = (t4.x > qmax1 || t4.y < lmin1) ? CPATTN_TILE_SKIP
+                       : (t4.y > qmin1 || t4.x < lmax1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            } else {
+                cls0 = (t4.x > qmax0) ? CPATTN_TILE_SKIP : (t4.y > qmin0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+                cls1 = (t4.x > qmax1) ? CPATTN_TILE_SKIP : (t4.y > qmin1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            }
             if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
             mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
             mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
@@ -261,7 +294,7 @@ struct TileWalk {
 // ---------------------------------------------------------------------------------------------
 // warp 0: scheduler and TMA producer
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool LB>
 __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                          uint32_t sQ, uint32_t sK, uint32_t sV, volatile int* unit_slot, const Bars<D>& bars,
                          const Waiter& wait) {
@@ -284,8 +317,8 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
         unit_slot[slot] = (u < P.num_units) ? u : -1;
         mbar_arrive(bars.unit_full(slot));
         if (u >= P.num_units) break;
-        const Unit U = decode_unit(P, u);
-        TileWalk w;
+        const Unit U = decode_unit<LB>(P, u);
+        TileWalk<LB> w;
         w.init(P, U);
         int j = 0, prev_row = 0;
         while (w.next()) {
@@ -362,7 +395,7 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
         const int u = unit_slot[slot];
         mbar_arrive(bars.unit_empty(slot));
         if (u < 0) break;
-        const Unit U = decode_unit(P, u);
+        const Unit U = decode_unit<false>(P, u);
         const int n_tiles = __ldg(P.unit_tiles + U.rg);
         if (n_tiles == 0) continue;                    // nothing visible for this unit
         if (!wait(bars.q_full(), nq & 1, kSiteQ)) { ok = false; break; }
@@ -416,7 +449,7 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
 // ---------------------------------------------------------------------------------------------
 // warps 4..11: softmax and epilogue, warpgroup i for query tile i, one thread per row
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool LB>
 __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* unit_slot, const Bars<D>& bars,
                                  const Waiter& wait) {
     using C = Cfg<D>;
@@ -436,13 +469,14 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.unit_empty(slot));
         if (u < 0) break;
-        const Unit U = decode_unit(P, u);
+        const Unit U = decode_unit<LB>(P, u);
         const int head = wg ? U.head[1] : U.head[0];
         const int qt = wg ? U.qt[1] : U.qt[0];
         const int member_valid = wg ? U.valid[1] : U.valid[0];
         const int64_t jl = (int64_t)qt * 128 + row;             // local index on rank r
         const bool row_valid = member_valid && jl < P.n;
         const int qpos = row_valid ? __ldg(P.posL + (int64_t)U.r * P.n + jl) : 0;
+        const int qlo = (LB && row_valid) ? __ldg(P.loL + (int64_t)U.r * P.n + jl) : INT_MIN;
         // l: sum of the fp32 exponentials (for lse); lr: the same values rounded to bf16 as the PV
         // product sees them (normalises O, so the weights applied to V sum to one exactly).
         float m_used = -INFINITY, l = 0.f, lr = 0.f;
@@ -457,7 +491,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             }
             cnt_full = cnt_diag = 0;
         };
-        TileWalk w;
+        TileWalk<LB> w;
         w.init(P, U);
         int j = 0;
         bool have = w.next();
@@ -491,7 +525,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                         kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.posL + kbase + c0 + c) : INT_MIN;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos;
+                        const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos && (!LB || kp[c] >= qlo);
                         if (!vis) x[c0 + c] = -INFINITY;
                     }
                     asm volatile("" ::: "memory");
@@ -649,7 +683,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
     }
 }
 
-template <int D>
+template <int D, bool LB>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params P) {
@@ -693,11 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsLow>();
-        if (warp == 0 && lane == 0) producer<D>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
+        if (warp == 0 && lane == 0) producer<D, LB>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
         if (warp == 1 && lane == 0) mma_issuer<D>(P, tmem, sQ, sK, sV, unit_slot, bars, wait);
     } else {
         setmaxnreg_inc<kRegsHigh>();
-        softmax_epilogue<D>(P, tmem, unit_slot, bars, wait);
+        softmax_epilogue<D, LB>(P, tmem, unit_slot, bars, wait);
     }
     tc_fence_before();
     __syncthreads();
@@ -724,6 +758,7 @@ __global__ void wait_selftest_kernel(uint32_t* header, uint64_t timeout_ns) {
 // One thread per row group (rank r, group): the number of key tiles a unit of that row group
 // visits in this launch, by the same walk the producer and the softmax warps take. Units of one
 // row group differ only in batch element and heads, which do not change the walk.
+template <bool LB>
 __global__ void unit_tiles_kernel(const Params P) {
     const int rg = blockIdx.x * blockDim.x + threadIdx.x;
     if (rg >= P.n_cp * P.n_grp) return;
@@ -742,16 +777,9 @@ __global__ void unit_tiles_kernel(const Params P) {
         U.valid[0] = 1;
         U.valid[1] = U.qt[1] < P.n_qt;
     }
-    for (int i = 0; i < 2; ++i) {
-        if (U.valid[i]) {
-            const int4 t4 = P.tile_mm[U.r * P.n_qt + U.qt[i]];
-            U.qmm[i] = make_int2(t4.x, t4.y);
-        } else {
-            U.qmm[i] = make_int2(INT_MAX, INT_MIN);
-        }
-        U.head[i] = 0;
-    }
-    TileWalk w;
+    unit_ranges<LB>(P, U);
+    U.head[0] = U.head[1] = 0;
+    TileWalk<LB> w;
     w.init(P, U);
     int c = 0;
     while (w.next()) ++c;
@@ -759,20 +787,20 @@ __global__ void unit_tiles_kernel(const Params P) {
 }
 
 // ---- host side -------------------------------------------------------------------------------
-template <int D>
+template <int D, bool LB>
 int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     using C = Cfg<D>;
     static int attr_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
         // setmaxnreg.inc waits until enough registers are free in the block's allocation: the
         // split must fit in what the block is launched with, or the kernel would never proceed.
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, ring_attention_kernel<D>);
+        e = cudaFuncGetAttributes(&fa, ring_attention_kernel<D, LB>);
         if (e != cudaSuccess) return (int)e;
         if ((long)fa.numRegs * kThreads < 128L * kRegsLow + 256L * kRegsHigh) {
             *why = "attention kernel built with " + std::to_string(fa.numRegs) +
@@ -796,6 +824,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm); P.order = a.order;
     P.unit_tiles = a.unit_tiles;
+    P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
     P.header = a.header; P.timeout_ns = a.timeout_ns;
@@ -807,8 +836,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.num_units = (int)units;
     const int grid = (int)(units < sms ? units : sms);
     const int n_rg = a.n_cp * a.n_grp;
-    unit_tiles_kernel<<<(n_rg + 127) / 128, 128, 0, st>>>(P);
-    ring_attention_kernel<D><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
+    unit_tiles_kernel<LB><<<(n_rg + 127) / 128, 128, 0, st>>>(P);
+    ring_attention_kernel<D, LB><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }
 
@@ -816,8 +845,9 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
 
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a.d == 128) return launch_d<128>(a, st, why);
-    if (a.d == 64) return launch_d<64>(a, st, why);
+    const bool lb = a.loL != nullptr;   // a per-query lower bound (document masks)
+    if (a.d == 128) return lb ? launch_d<128, true>(a, st, why) : launch_d<128, false>(a, st, why);
+    if (a.d == 64) return lb ? launch_d<64, true>(a, st, why) : launch_d<64, false>(a, st, why);
     *why = "unsupported head width";
     return (int)cudaErrorInvalidValue;
 }

@@ -29,6 +29,8 @@ struct WsLayout {
     size_t order = 0;       // int32 [n_cp * n_qt]: (rank, q-tile) pairs, longest first
     size_t counts = 0;      // uint64 [n_cp][n_cp][2]: tiles computed per (rank, step), FULL / DIAG
     size_t sched = 0;       // uint32 [1 + n_cp]: work counters of the persistent kernel (fused, each step)
+    size_t loL = 0;         // int32 [n_cp][n]: lowest visible key position of (rank, local index) (document masks)
+    size_t tile_lo = 0;     // int32x4 [n_cp][n_qt]: min and max of loL over each query tile
     size_t unit_tiles = 0;  // int32 [n_cp * n_qt]: key tiles a unit of row group (r, group) visits in
                             // the current launch (written by the attention launch itself)
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
@@ -74,6 +76,7 @@ struct PermuteArgs {
     int B, T_is_int; int64_t T, n, m; int h, n_kv, d, n_cp, layout, n_qt;
     const void* q; const void* k; const void* v; const int32_t* pos;
     void* qL; void* kL; void* vL; int32_t* posL; int32_t* tile_mm;
+    const int32_t* lo; int32_t* loL; int32_t* tile_lo;   // optional per-query lower bound (NULL: none)
 };
 int launch_permute(const PermuteArgs& a, void* stream);
 
@@ -87,6 +90,7 @@ struct AttnLaunch {
     const void* qL; const void* kv_k; const void* kv_v;   // K/V base: kL/vL or a stage slot
     int kv_by_holder; // K/V rows indexed by the holder rank r instead of the source rank
     const int32_t* posL; const int32_t* tile_mm; const int32_t* order;
+    const int32_t* loL; const int32_t* tile_lo;   // document-mask lower bounds, or NULL
     unsigned long long* counts;     // tiles computed per (rank, step, class)
     void* o; float* lse;            // fused outputs (natural order)
     float* o_run; float* lse_run;   // ring-step running state

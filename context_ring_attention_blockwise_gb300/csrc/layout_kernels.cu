@@ -39,28 +39,45 @@ __device__ __forceinline__ int64_t token_of_dev(int layout, int r, int64_t j, in
 }
 
 // One 128-thread block per (rank, tile): position ids in layout order and their min/max.
+// With a lower-bound array (document masks) the block also writes each token's bound in layout
+// order and the min/max bound of the tile.
 __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restrict__ pos, int32_t* __restrict__ posL,
-                                                        int4* __restrict__ tile_mm, int64_t n, int64_t m, int n_cp,
-                                                        int layout, int n_qt) {
+                                                        int4* __restrict__ tile_mm, const int32_t* __restrict__ lob,
+                                                        int32_t* __restrict__ loL, int4* __restrict__ tile_lo,
+                                                        int64_t n, int64_t m, int n_cp, int layout, int n_qt) {
     const int r = blockIdx.x / n_qt, tile = blockIdx.x % n_qt;
     const int64_t j = (int64_t)tile * kBlockQ + threadIdx.x;
-    int lo = INT_MAX, hi = INT_MIN;
+    int lo = INT_MAX, hi = INT_MIN, blo = INT_MAX, bhi = INT_MIN;
     if (j < n) {
         int64_t t = token_of_dev(layout, r, j, n, m, n_cp);
         int pv = pos ? pos[t] : (int)t;
         posL[(int64_t)r * n + j] = pv;
         lo = hi = pv;
+        if (lob) {
+            const int bv = lob[t];
+            loL[(int64_t)r * n + j] = bv;
+            blo = bhi = bv;
+        }
     }
     for (int o = 16; o > 0; o >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
         hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        blo = min(blo, __shfl_xor_sync(0xffffffffu, blo, o));
+        bhi = max(bhi, __shfl_xor_sync(0xffffffffu, bhi, o));
     }
-    __shared__ int slo[4], shi[4];
-    if ((threadIdx.x & 31) == 0) { slo[threadIdx.x >> 5] = lo; shi[threadIdx.x >> 5] = hi; }
+    __shared__ int slo[4], shi[4], sblo[4], sbhi[4];
+    if ((threadIdx.x & 31) == 0) {
+        slo[threadIdx.x >> 5] = lo; shi[threadIdx.x >> 5] = hi;
+        sblo[threadIdx.x >> 5] = blo; sbhi[threadIdx.x >> 5] = bhi;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int w = 1; w < 4; ++w) { lo = min(lo, slo[w]); hi = max(hi, shi[w]); }
+        for (int w = 1; w < 4; ++w) {
+            lo = min(lo, slo[w]); hi = max(hi, shi[w]);
+            blo = min(blo, sblo[w]); bhi = max(bhi, sbhi[w]);
+        }
         tile_mm[blockIdx.x] = make_int4(lo, hi, lo, 0);
+        if (lob) tile_lo[blockIdx.x] = make_int4(blo, bhi, 0, 0);
     }
 }
 
@@ -245,8 +262,9 @@ int grid_for(int64_t work, int threads) {
 
 int launch_permute(const PermuteArgs& a, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int4*>(a.tile_mm), a.n, a.m,
-                                                      a.n_cp, a.layout, a.n_qt);
+    pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int4*>(a.tile_mm), a.lo, a.loL,
+                                                      reinterpret_cast<int4*>(a.tile_lo), a.n, a.m, a.n_cp, a.layout,
+                                                      a.n_qt);
     int e = (int)cudaGetLastError();
     if (e) return e;
     tile_suffix_kernel<<<(a.n_cp + 127) / 128, 128, 0, st>>>(reinterpret_cast<int4*>(a.tile_mm), a.n_cp, a.n_qt);

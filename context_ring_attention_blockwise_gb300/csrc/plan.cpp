@@ -35,6 +35,8 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.order = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
     w.counts = take(sizeof(uint64_t) * 2 * (size_t)p.n_cp * p.n_cp);
     w.sched = take(sizeof(uint32_t) * (1 + (size_t)p.n_cp));
+    w.loL = take(sizeof(int32_t) * T);
+    w.tile_lo = take(sizeof(int32_t) * 4 * (size_t)p.n_cp * p.n_qt);
     w.unit_tiles = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
     w.qL = take(2 * (size_t)B * T * p.h * d);
     w.kL = take(2 * (size_t)B * T * p.n_kv * d);

@@ -136,6 +136,21 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
 cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, void* ws, size_t ws_bytes,
                                 cpattn_stream_t stream);
 
+/* The forward under a per-query lower bound on the visible key positions: key u is visible to
+ * query t iff lo[t] <= pos[u] <= pos[t]. With positions 0..T-1 (pos NULL) and lo[t] = the first
+ * token of t's document this is the document mask of packed sequences ([CEX] "What context
+ * parallelism communicates": the all-gather variant "makes arbitrary masks, such as document
+ * masks for packed sequences, easy to support"; on one GPU every rank's queries already read the
+ * resident keys and values of all ranks, which is that variant's data flow). Masks on positions
+ * only, so the mask positions must increase through the packed sequence; per-document position
+ * ids (for rotary embeddings) are not what pos means here.
+ *   lo [T] int32 (device, natural order, 16-byte aligned); the plan must be causal, else
+ *   CPATTN_ERR_UNSUPPORTED. Other arguments as cpattn_forward. A row that sees no key gets
+ *   o = 0 and lse = -inf. */
+cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                      const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse, void* ws,
+                                      size_t ws_bytes, cpattn_stream_t stream);
+
 /* Backward pass ([CEX] "What context parallelism communicates": each rank keeps the gradient
  * of its own queries; the key and value gradients travel back to their owners as a second
  * circulating block of the ring, which on one GPU is a key tile's gradient accumulated over
