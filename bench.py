@@ -406,6 +406,30 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     ms = a.elapsed_time(b) / 2
     out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12}
     del wsr
+    # document masks: the same workload packed with seeded documents of 2K..16K tokens
+    rng = np.random.default_rng(w.seed)
+    lengths = []
+    while sum(lengths) < w.T:
+        lengths.append(int(rng.integers(2048, 16385)))
+    lengths[-1] -= sum(lengths) - w.T
+    lengths = [x for x in lengths if x > 0]
+    starts = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+    lo = torch.from_numpy(np.repeat(starts, lengths).astype(np.int32)).to(dev)
+    pairs = sum(x * (x + 1) // 2 for x in lengths)
+    flops_docs = 4.0 * w.B * w.h * w.d * pairs
+    od, lsed = torch.empty_like(o), torch.empty_like(lse)
+    cp.forward_masked(q, k, v, plan, lo, ws=ws, out=od, lse=lsed, stream=stream)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(3):
+        cp.forward_masked(q, k, v, plan, lo, ws=ws, out=od, lse=lsed, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    ms = a.elapsed_time(b) / 3
+    out["documents"] = {"ms": ms, "documents": len(lengths), "tflops_eff": flops_docs / (ms * 1e-3) / 1e12,
+                        "flops": "4 B h d per visible (query, key) pair inside each document"}
+    del od, lsed, lo
     # the backward pass: dq, dk, dv from the forward's o and lse and a synthetic output gradient
     wsb = cp.alloc_workspace(plan.backward_workspace_size(w.B), dev)
     dout = torch.randn(q.shape, dtype=torch.bfloat16, device=dev)
