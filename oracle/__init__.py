@@ -76,6 +76,9 @@ def bind(path: str):
                                           _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _P, _P]
     lib.oracle_attention_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P,
                                               _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _I64, _P, _P, _P, _P]
+    lib.oracle_attention_backward_docs.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P,
+                                                   _P, _P, _P, _P, ctypes.c_int, ctypes.c_double, _I64, _P, _I64, _P,
+                                                   _P, _P, _P]
     lib.oracle_ring_backward.argtypes = [ctypes.c_int, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P,
                                          _P, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          _P, _P, _P]
@@ -184,11 +187,11 @@ class Oracle:
         return o, lse
 
     # -- gradients ----------------------------------------------------------------------
-    def backward(self, q, k, v, dout, causal=True, scale=None, pos=None, rows=None, keys=None):
+    def backward(self, q, k, v, dout, causal=True, scale=None, pos=None, rows=None, keys=None, doc=None):
         """Gradients of L = sum(O * dO) for bf16-bit inputs (dout [B,T,h,d] bf16 bits too).
 
         Returns (dq [B,R,h,d] for the query rows `rows`, dk [B,K,n_kv,d], dv [B,K,n_kv,d] for the
-        keys `keys`), fp64; rows/keys default to all T."""
+        keys `keys`), fp64; rows/keys default to all T. doc: document id per token (document mask)."""
         B, T, h, d = q.shape
         n_kv = k.shape[2]
         scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
@@ -208,9 +211,16 @@ class Oracle:
         dq = np.empty((B, R, h, d), dtype=np.float64)
         dk = np.empty((B, K, n_kv, d), dtype=np.float64)
         dv = np.empty((B, K, n_kv, d), dtype=np.float64)
-        rc = self.lib.oracle_attention_backward(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
-                                                dout.ctypes.data, posp, int(causal), scale, R, rowsp, K, keysp,
-                                                dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+        if doc is not None:
+            doc = np.ascontiguousarray(doc, dtype=np.int32)
+            rc = self.lib.oracle_attention_backward_docs(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                         dout.ctypes.data, posp, doc.ctypes.data, int(causal), scale, R,
+                                                         rowsp, K, keysp, dq.ctypes.data, dk.ctypes.data,
+                                                         dv.ctypes.data)
+        else:
+            rc = self.lib.oracle_attention_backward(B, T, h, n_kv, d, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                    dout.ctypes.data, posp, int(causal), scale, R, rowsp, K, keysp,
+                                                    dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
         if rc:
             raise ValueError("oracle_attention_backward failed")
         return dq, dk, dv

@@ -473,13 +473,13 @@ int64_t oracle_kv_bytes_recv(int B, int64_t n, int n_kv, int d_k, int n_cp) {
 
 /* lse and D = <dO_t, O_t> of one (b, t, head i) row from the definition (two passes). */
 static void row_stats(int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                      const uint16_t* dout, const int32_t* pos, int causal, double scale, int b, int64_t t, int i,
-                      double* acc, double* lse_out, double* d_out) {
+                      const uint16_t* dout, const int32_t* pos, const int32_t* doc, int causal, double scale, int b,
+                      int64_t t, int i, double* acc, double* lse_out, double* d_out) {
     int kv = i / (h / n_kv);
     const uint16_t* qrow = q + (((int64_t)b * T + t) * h + i) * d;
     double mx = -INFINITY;
     for (int64_t u = 0; u < T; ++u) {
-        if (!visible(pos, u, t, causal)) continue;
+        if (!visible_doc(pos, doc, u, t, causal)) continue;
         const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
         double dot = 0.0;
         for (int c = 0; c < d; ++c) dot += bf16_value(qrow[c]) * bf16_value(krow[c]);
@@ -489,7 +489,7 @@ static void row_stats(int64_t T, int h, int n_kv, int d, const uint16_t* q, cons
     double sum = 0.0;
     for (int c = 0; c < d; ++c) acc[c] = 0.0;
     for (int64_t u = 0; u < T; ++u) {
-        if (!visible(pos, u, t, causal)) continue;
+        if (!visible_doc(pos, doc, u, t, causal)) continue;
         const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
         const uint16_t* vrow = v + (((int64_t)b * T + u) * n_kv + kv) * d;
         double dot = 0.0;
@@ -528,10 +528,10 @@ static void pair_terms(int64_t T, int h, int n_kv, int d, const uint16_t* q, con
  * dq [B,n_rows,h,d] for the query rows `rows` (NULL: all T, n_rows = T; dq may be NULL);
  * dk, dv [B,n_keys,n_kv,d] for the keys `keys` (NULL: all T, n_keys = T; dk/dv may be NULL).
  * fp64 outputs. Returns 0 on success. */
-int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
-                              const uint16_t* v, const uint16_t* dout, const int32_t* pos, int causal, double scale,
-                              int64_t n_rows, const int64_t* rows, int64_t n_keys, const int64_t* keys, double* dq,
-                              double* dk, double* dv) {
+static int backward_impl(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, const uint16_t* dout, const int32_t* pos, const int32_t* doc, int causal,
+                         double scale, int64_t n_rows, const int64_t* rows, int64_t n_keys, const int64_t* keys,
+                         double* dq, double* dk, double* dv) {
     if (B <= 0 || T <= 0 || h <= 0 || n_kv <= 0 || d <= 0 || h % n_kv) return 1;
     if (!rows) n_rows = T;
     if (!keys) n_keys = T;
@@ -556,12 +556,12 @@ int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const ui
                 int64_t t = rows ? rows[ri] : ri;
                 int kv = i / g;
                 double lse_t, d_t;
-                row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc, &lse_t, &d_t);
+                row_stats(T, h, n_kv, d, q, k, v, dout, pos, doc, causal, scale, b, t, i, acc, &lse_t, &d_t);
                 double* out = dq + (((int64_t)b * n_rows + ri) * h + i) * d;
                 for (int c = 0; c < d; ++c) out[c] = 0.0;
                 if (lse_t == -INFINITY) continue;
                 for (int64_t u = 0; u < T; ++u) {
-                    if (!visible(pos, u, t, causal)) continue;
+                    if (!visible_doc(pos, doc, u, t, causal)) continue;
                     double p, ds;
                     pair_terms(T, h, n_kv, d, q, k, v, dout, scale, b, t, i, u, lse_t, d_t, &p, &ds);
                     const uint16_t* krow = k + (((int64_t)b * T + u) * n_kv + kv) * d;
@@ -582,7 +582,7 @@ int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const ui
     for (int64_t t = 0; t < T; ++t)
         for (int64_t ki = 0; ki < n_keys; ++ki) {
             int64_t u = keys ? keys[ki] : ki;
-            if (visible(pos, u, t, causal)) { for (int b = 0; b < B; ++b) need[(int64_t)b * T + t] = 1; break; }
+            if (visible_doc(pos, doc, u, t, causal)) { for (int b = 0; b < B; ++b) need[(int64_t)b * T + t] = 1; break; }
         }
     int64_t total = (int64_t)B * T * h;
 #pragma omp parallel
@@ -599,7 +599,7 @@ int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const ui
             int64_t t = (w / h) % T;
             int b = (int)(w / ((int64_t)h * T));
             if (!need[(int64_t)b * T + t]) continue;
-            row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc,
+            row_stats(T, h, n_kv, d, q, k, v, dout, pos, doc, causal, scale, b, t, i, acc,
                       &lse[((int64_t)b * h + i) * T + t], &dd[((int64_t)b * h + i) * T + t]);
         }
         free(acc);
@@ -617,7 +617,7 @@ int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const ui
         for (int c = 0; c < d; ++c) { if (gk) gk[c] = 0.0; if (gv) gv[c] = 0.0; }
         for (int i = kvh * g; i < (kvh + 1) * g; ++i)
             for (int64_t t = 0; t < T; ++t) {
-                if (!visible(pos, u, t, causal)) continue;
+                if (!visible_doc(pos, doc, u, t, causal)) continue;
                 double lse_t = lse[((int64_t)b * h + i) * T + t];
                 if (lse_t == -INFINITY) continue;
                 double p, ds;
@@ -634,6 +634,24 @@ int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const ui
     free(dd);
     free(need);
     return 0;
+}
+
+int oracle_attention_backward(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                              const uint16_t* v, const uint16_t* dout, const int32_t* pos, int causal, double scale,
+                              int64_t n_rows, const int64_t* rows, int64_t n_keys, const int64_t* keys, double* dq,
+                              double* dk, double* dv) {
+    return backward_impl(B, T, h, n_kv, d, q, k, v, dout, pos, NULL, causal, scale, n_rows, rows, n_keys, keys, dq,
+                         dk, dv);
+}
+
+/* The gradients under a document mask (doc [T] document id per natural token): the derivatives
+ * of oracle_attention_docs. */
+int oracle_attention_backward_docs(int B, int64_t T, int h, int n_kv, int d, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const uint16_t* dout, const int32_t* pos, const int32_t* doc,
+                                   int causal, double scale, int64_t n_rows, const int64_t* rows, int64_t n_keys,
+                                   const int64_t* keys, double* dq, double* dk, double* dv) {
+    return backward_impl(B, T, h, n_kv, d, q, k, v, dout, pos, doc, causal, scale, n_rows, rows, n_keys, keys, dq, dk,
+                         dv);
 }
 
 /* The ring backward, simulated literally. [CEX] "What context parallelism communicates":   */
@@ -670,7 +688,7 @@ int oracle_ring_backward(int B, int64_t T, int h, int n_kv, int d, const uint16_
             int i = (int)(w % h);
             int64_t t = (w / h) % T;
             int b = (int)(w / ((int64_t)h * T));
-            row_stats(T, h, n_kv, d, q, k, v, dout, pos, causal, scale, b, t, i, acc,
+            row_stats(T, h, n_kv, d, q, k, v, dout, pos, NULL, causal, scale, b, t, i, acc,
                       &lse[((int64_t)b * h + i) * T + t], &dd[((int64_t)b * h + i) * T + t]);
         }
         free(acc);

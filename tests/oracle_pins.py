@@ -446,4 +446,26 @@ def pin_document_mask(orc):
             start += ln
 
 
+def pin_document_mask_gradients(orc):
+    """Gradients under a document mask: against autograd with the boolean mask, and each document's
+    gradients computed on its own slice."""
+    B, T, h, n_kv, d = 1, 30, 4, 2, 8
+    q, k, v = _qkv(42, B, T, h, n_kv, d)
+    do = _dout(42, B, T, h, d)
+    lengths = [9, 1, 14, 6]
+    doc = np.repeat(np.arange(len(lengths)), lengths).astype(np.int32)
+    dq, dk, dv = orc.backward(q, k, v, do, causal=True, doc=doc)
+    mask = (doc[None, :] == doc[:, None]) & (np.arange(T)[None, :] <= np.arange(T)[:, None])
+    rq, rk, rv = _autograd(q, k, v, do, False, mask=torch.from_numpy(mask))
+    assert _maxabs(dq, rq) < 1e-11 and _maxabs(dk, rk) < 1e-11 and _maxabs(dv, rv) < 1e-11, \
+        "document-mask gradients differ from autograd with the same mask"
+    start = 0
+    for ln in lengths:
+        sl = slice(start, start + ln)
+        gq, gk, gv = orc.backward(q[:, sl], k[:, sl], v[:, sl], do[:, sl], causal=True)
+        assert _maxabs(dq[:, sl], gq) < 1e-12 and _maxabs(dk[:, sl], gk) < 1e-12 and _maxabs(dv[:, sl], gv) < 1e-12, \
+            "a document's gradients must equal the gradients of that document alone"
+        start += ln
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
