@@ -26,7 +26,7 @@ SYMBOLS = [
     "cpattn_attend", "cpattn_forward_noalloc",
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
-    "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked",
+    "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked", "cpattn_backward_masked",
 ]
 
 
@@ -68,6 +68,8 @@ def lib():
     L.cpattn_check.argtypes = [_P, _P]
     L.cpattn_selftest_wait_timeout.argtypes = [_P, ctypes.c_size_t, u64, _P]
     L.cpattn_forward_masked.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_backward_masked.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
+                                         ctypes.c_size_t, _P]
     L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_last_error.restype = ctypes.c_char_p
@@ -206,9 +208,10 @@ def forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, 
 
 
 def backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = None, ws=None, dq=None, dk=None,
-             dv=None, stream=None):
+             dv=None, stream=None, lo=None):
     """cpattn_backward: gradients of sum(o * dout) for the forward o, lse = forward(q, k, v, plan).
     q/o/dout [B,T,h,d], k/v [B,T,n_kv,d] bf16 and lse [B,h,T] fp32 CUDA tensors (natural order).
+    lo: the per-query lower bound of forward_masked (document masks), for cpattn_backward_masked.
     Returns (dq [B,T,h,d], dk [B,T,n_kv,d], dv [B,T,n_kv,d]) bf16."""
     torch = _torch()
     B = _check_inputs(plan, q, k, v)
@@ -222,6 +225,16 @@ def backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = 
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    if lo is not None:
+        if tuple(lo.shape) != (plan.T,) or lo.dtype != torch.int32:
+            raise ValueError("lo must be an int32 tensor of T entries")
+        _check(lib().cpattn_backward_masked(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                            _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), _dev_ptr(dout, "dout"),
+                                            _dev_ptr(pos, "pos"), _dev_ptr(lo, "lo"), float(scale or 0.0),
+                                            _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"),
+                                            _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+               "cpattn_backward_masked")
+        return dq, dk, dv
     _check(lib().cpattn_backward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(o, "o"),
                                  _dev_ptr(lse, "lse"), _dev_ptr(dout, "dout"), _dev_ptr(pos, "pos"), float(scale or 0.0),
                                  _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), _dev_ptr(ws, "ws"),

@@ -216,9 +216,10 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
     return CPATTN_OK;
 }
 
-cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
-                                const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,
-                                void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+namespace {
+cpattn_status_t backward_impl(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, const int32_t* pos, const int32_t* lo, float scale,
+                              void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
@@ -234,7 +235,7 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
         return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(w.bwd_end) + " bytes, got " +
                                               std::to_string(ws_bytes));
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((s = prologue(*p, B, q, k, v, pos, ws, st))) return s;
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, lo))) return s;
     cpattn::BwdPrepArgs pa{};
     pa.B = B; pa.T = p->T; pa.n = p->n; pa.m = p->m; pa.h = p->h; pa.d = p->d; pa.n_cp = p->n_cp;
     pa.layout = p->layout; pa.n_qt = p->n_qt;
@@ -256,6 +257,8 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
     a.lse2L = at<float>(ws, w.lse2); a.DL = at<float>(ws, w.Dl);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
     a.order_q = at<int32_t>(ws, w.bwd_order); a.order_kv = a.order_q + nu;
+    a.loL = lo ? at<int32_t>(ws, w.loL) : nullptr;
+    a.tile_lo = lo ? at<int32_t>(ws, w.tile_lo) : nullptr;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
@@ -263,6 +266,24 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
     e = cpattn::launch_backward(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
+}
+}  // namespace
+
+cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,
+                                void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    return backward_impl(plan, B, q, k, v, o, lse, dout, pos, nullptr, scale, dq, dk, dv, ws, ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const void* o, const float* lse, const void* dout, const int32_t* pos,
+                                       const int32_t* lo, float scale, void* dq, void* dk, void* dv, void* ws,
+                                       size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!p->causal) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query needs a causal plan");
+    if (!lo || !aligned16(lo)) return fail(CPATTN_ERR_INVALID, "lo must be non-NULL and 16-byte aligned");
+    return backward_impl(plan, B, q, k, v, o, lse, dout, pos, lo, scale, dq, dk, dv, ws, ws_bytes, stream);
 }
 
 cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,

@@ -56,6 +56,8 @@ struct BwdParams {
     const int4* tile_mm;
     const float* lse2L;   // [n_cp][B][h][n_pad] lse * log2(e) (tile starts 512-byte aligned)
     const float* DL;      // [n_cp][B][h][n_pad]
+    const int32_t* loL;        // [n_cp][n] lowest visible key position per query (document masks), or NULL
+    const int4* tile_lo;       // [n_cp][n_qt] (min, max) of loL over a query tile, or NULL
     const int32_t* order_q;    // (r * n_qt + qt), heaviest first
     const int32_t* order_kv;   // (src * n_qt + kt), heaviest first
     uint16_t* dq;         // natural [B,T,h,d]
@@ -99,11 +101,21 @@ __device__ __forceinline__ int64_t natural_token(int layout, int r, int64_t j, i
 // Tile classes from the position ranges of a query tile and a key tile (exact for the mask
 // pos[u] <= pos[t]): SKIP if every key follows every query, FULL if every key precedes every
 // query, DIAG otherwise.
-__device__ __forceinline__ int tile_class(int causal, int4 q, int4 k) {
+// With document masks each query also has a lowest visible key position; ql = (min, max) of it
+// over the query tile ((INT_MIN, INT_MIN) without): SKIP also when every key lies below every
+// bound, FULL only when every key lies at or above every bound.
+__device__ __forceinline__ int tile_class(int causal, int4 q, int2 ql, int4 k) {
     if (!causal) return CPATTN_TILE_FULL;
-    if (k.x > q.y) return CPATTN_TILE_SKIP;
-    if (k.y <= q.x) return CPATTN_TILE_FULL;
+    if (k.x > q.y || k.y < ql.x) return CPATTN_TILE_SKIP;
+    if (k.y <= q.x && k.x >= ql.y) return CPATTN_TILE_FULL;
     return CPATTN_TILE_DIAG;
+}
+
+template <bool LB>
+__device__ __forceinline__ int2 tile_bound(const BwdParams& P, int r, int qt) {
+    if (!LB) return make_int2(INT_MIN, INT_MIN);
+    const int4 l4 = __ldg(P.tile_lo + r * P.n_qt + qt);
+    return make_int2(l4.x, l4.y);
 }
 
 // ---- shared-memory layout and barriers (both tcgen05 kernels) --------------------------
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
 // =============================================================================================
 // bwd_dkdv_kernel
 // =============================================================================================
-template <int D>
+template <int D, bool LB>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -313,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int r = (src + s) % P.n_cp;         // the block's gradient is at rank src + s at step s
                 for (int qt = 0; qt < P.n_qt && ok; ++qt) {
                     const int4 qmm = __ldg(P.tile_mm + r * P.n_qt + qt);
-                    const int cls = tile_class(P.causal, qmm, kmm);
+                    const int cls = tile_class(P.causal, qmm, tile_bound<LB>(P, r, qt), kmm);
                     if (cls == CPATTN_TILE_SKIP) continue;
                     const int qshort = (qt == P.n_qt - 1) && (P.n % 128) != 0;
                     const int kshort = (kt == P.n_qt - 1) && (P.n % 128) != 0;
@@ -442,9 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (col + 3 < qvalid) qp4.w = __ldg(qposg + col + 3);
                         }
                         const int qp[4] = {qp4.x, qp4.y, qp4.z, qp4.w};
+                        int ql[4] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN};
+                        if (LB) {
+                            const int32_t* qlog = P.loL + qoff;
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4)
+                                if (col + e4 < qvalid) ql[e4] = __ldg(qlog + col + e4);
+                        }
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) {
-                            const bool vis = key_valid && col + e4 < qvalid && (!P.causal || kpos <= qp[e4]);
+                            const bool vis = key_valid && col + e4 < qvalid && (!P.causal || kpos <= qp[e4]) &&
+                                             (!LB || kpos >= ql[e4]);
                             vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
                         }
                     }
@@ -533,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =============================================================================================
 // bwd_dq_kernel
 // =============================================================================================
-template <int D>
+template <int D, bool LB>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -583,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const BWaiter wait{abort_flag, P.header, P.timeout_ns};
     const int4 qmm = __ldg(P.tile_mm + r * P.n_qt + qt);
+    const int2 qlb = tile_bound<LB>(P, r, qt);
     const int qrow0 = (int)((((int64_t)r * P.B + b) * P.h + head) * P.n + (int64_t)qt * 128);
 
     if (warp == 0) {
@@ -618,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int srcr = (r - s + P.n_cp) % P.n_cp;     // the block rank r holds at step s
                 for (int ktt = 0; ktt < P.n_qt && ok; ++ktt) {
                     const int4 kmm = __ldg(P.tile_mm + srcr * P.n_qt + ktt);
-                    const int cls = tile_class(P.causal, qmm, kmm);
+                    const int cls = tile_class(P.causal, qmm, qlb, kmm);
                     if (cls == CPATTN_TILE_SKIP) continue;
                     const int qshort = (qt == P.n_qt - 1) && (P.n % 128) != 0;
                     const int kshort = (ktt == P.n_qt - 1) && (P.n % 128) != 0;
@@ -694,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse2 = q_valid ? __ldg(P.lse2L + lrow) : -INFINITY;
         const float Dv = q_valid ? __ldg(P.DL + lrow) : 0.f;
         const bool row_live = q_valid && lse2 != -INFINITY;   // a row that sees some key
+        const int qlo = (LB && q_valid) ? __ldg(P.loL + (int64_t)r * P.n + jq) : INT_MIN;
         bool ok = true;
         int step = 0, n_steps = 0;
         for (;;) {
@@ -736,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) {
-                            const bool vis = col + e4 < kvalid && (!P.causal || kp[e4] <= qpos);
+                            const bool vis = col + e4 < kvalid && (!P.causal || kp[e4] <= qpos) && (!LB || kp[e4] >= qlo);
                             vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
                         }
                     }
@@ -801,16 +823,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool LB>
 int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     using C = BCfg<D>;
     static int attr_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+            e = cudaFuncSetAttribute(bwd_dq_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
         attr_dev = dev;
     }
@@ -827,6 +850,7 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     P.scale = a.scale; P.scale_log2 = a.scale * kLog2e;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm);
     P.lse2L = a.lse2L; P.DL = a.DL; P.order_q = a.order_q; P.order_kv = a.order_kv;
+    P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
     P.header = a.header; P.timeout_ns = a.timeout_ns;
     const int64_t kv_units = (int64_t)a.B * a.n_kv * a.n_cp * a.n_qt, q_units = (int64_t)a.B * a.h * a.n_cp * a.n_qt;
@@ -834,10 +858,10 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
         *why = "too many work units";
         return (int)cudaErrorInvalidValue;
     }
-    bwd_dkdv_kernel<D><<<(int)kv_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+    bwd_dkdv_kernel<D, LB><<<(int)kv_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
     int e = (int)cudaGetLastError();
     if (e) return e;
-    bwd_dq_kernel<D><<<(int)q_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+    bwd_dq_kernel<D, LB><<<(int)q_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
     return (int)cudaGetLastError();
 }
 
@@ -857,8 +881,9 @@ int launch_bwd_prep(const BwdPrepArgs& a, void* stream) {
 
 int launch_backward(const BwdLaunch& a, void* stream, std::string* why) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a.d == 128) return launch_bwd_d<128>(a, st, why);
-    if (a.d == 64) return launch_bwd_d<64>(a, st, why);
+    const bool lb = a.loL != nullptr;   // document masks
+    if (a.d == 128) return lb ? launch_bwd_d<128, true>(a, st, why) : launch_bwd_d<128, false>(a, st, why);
+    if (a.d == 64) return lb ? launch_bwd_d<64, true>(a, st, why) : launch_bwd_d<64, false>(a, st, why);
     *why = "unsupported head width";
     return (int)cudaErrorInvalidValue;
 }

@@ -124,6 +124,7 @@ struct BwdLaunch {
     const float* lse2L; const float* DL;
     const int32_t* posL; const int32_t* tile_mm;
     const int32_t* order_q; const int32_t* order_kv;   // longest-first unit orders
+    const int32_t* loL; const int32_t* tile_lo;         // document-mask lower bounds, or NULL
     void* dq; void* dk; void* dv;                         // natural order, bf16
     uint32_t* header;
     uint64_t timeout_ns;

@@ -170,6 +170,15 @@ cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const 
                                 const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,
                                 void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream);
 
+/* The backward pass under the per-query lower bound of cpattn_forward_masked (document masks of
+ * packed sequences: "the backward pass is the mirror image", [CEX] "What context parallelism
+ * communicates"). lo [T] int32 as for cpattn_forward_masked; the plan must be causal, else
+ * CPATTN_ERR_UNSUPPORTED. Other arguments as cpattn_backward. */
+cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const void* o, const float* lse, const void* dout, const int32_t* pos,
+                                       const int32_t* lo, float scale, void* dq, void* dk, void* dv, void* ws,
+                                       size_t ws_bytes, cpattn_stream_t stream);
+
 /* S-way log-sum-exp merge of partial attention results ([CEX] online-softmax paragraph: old
  * totals rescaled to a common maximum). For every row and head:
  *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).

@@ -97,3 +97,52 @@ def test_documents_gqa_16k_sampled():
     rows = synth.sample_rows(w.T, w.n_cp, 256, seed=w.seed)
     ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=True, rows=rows)
     compare(o[:, rows], lse[:, :, rows], ref_o, ref_lse, what="16K documents")
+
+
+# ---- the backward under document masks -------------------------------------------------------
+
+def _masked_backward(q, k, v, do, lo, n_cp, layout):
+    B, T, h, d = q.shape
+    plan = cp.Plan(T, h, k.shape[2], d, n_cp, layout, True)
+    qd, kd, vd, dod = (to_device_bf16(x) for x in (q, k, v, do))
+    lod = torch.from_numpy(lo).cuda()
+    o, lse = cp.forward_masked(qd, kd, vd, plan, lod)
+    ws = cp.alloc_workspace(plan.backward_workspace_size(B))
+    dq, dk, dv = cp.backward(qd, kd, vd, o, lse, dod, plan, ws=ws, lo=lod)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    return tuple(x.float().cpu().numpy() for x in (dq, dk, dv))
+
+
+BWD_CASES = [
+    (1024, 4, 2, 128, 4, ZIGZAG, 300),
+    (1040, 2, 1, 64, 4, CONTIGUOUS, 40),
+    (1536, 4, 1, 128, 4, STRIPED, 700),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=[f"T{c[0]}_h{c[1]}_kv{c[2]}_d{c[3]}_cp{c[4]}_"
+                                                 f"{synth.LAYOUT_NAMES[c[5]]}_max{c[6]}" for c in BWD_CASES])
+def test_document_mask_backward_matches_oracle(case):
+    from tests.test_gpu_backward import _compare
+    T, h, n_kv, d, n_cp, layout, max_len = case
+    q, k, v = inputs(70 + T + h, 1, T, h, n_kv, d)
+    do = synth.normal_bf16(70 + T, 4, (1, T, h, d))
+    doc, lo = packed_documents(T, seed=T + 3 * max_len, max_len=max_len)
+    dq, dk, dv = _masked_backward(q, k, v, do, lo, n_cp, layout)
+    rq, rk, rv = oracle.get().backward(q, k, v, do, causal=True, doc=doc)
+    _compare(dq, rq, "dq")
+    _compare(dk, rk, "dk")
+    _compare(dv, rv, "dv")
+
+
+def test_document_mask_backward_lower_bound_zero_is_plain():
+    q, k, v = inputs(71, 1, 1024, 4, 2, 128)
+    do = synth.normal_bf16(71, 4, (1, 1024, 4, 128))
+    a = _masked_backward(q, k, v, do, np.zeros(1024, dtype=np.int32), 4, ZIGZAG)
+    plan = cp.Plan(1024, 4, 2, 128, 4, ZIGZAG, True)
+    qd, kd, vd, dod = (to_device_bf16(x) for x in (q, k, v, do))
+    o, lse = cp.forward(qd, kd, vd, plan)
+    b = cp.backward(qd, kd, vd, o, lse, dod, plan)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y.float().cpu().numpy())
