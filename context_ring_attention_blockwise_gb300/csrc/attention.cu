@@ -261,6 +261,24 @@ struct TileWalk {
             }
             src = r - s;
             if (src < 0) src += P.n_cp;
+            if (LB && kt == 0 && P.causal) {
+                // Entering a block: its tiles below every query's lower bound come first in the
+                // non-decreasing running maximum (.w); skip the block, or start at its first tile
+                // whose running maximum reaches the smallest bound.
+                const int lmin = min(lmin0, lmin1);
+                const int* mm = reinterpret_cast<const int*>(P.tile_mm + src * P.n_qt);
+                if (__ldg(mm + 4 * (P.n_qt - 1) + 3) < lmin) {
+                    kt = P.n_qt - 1;
+                    continue;
+                }
+                int lo = 0, hi = P.n_qt - 1;              // first kt with running max >= lmin
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldg(mm + 4 * mid + 3) < lmin) lo = mid + 1;
+                    else hi = mid;
+                }
+                kt = lo;
+            }
             const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
             if (!P.causal) {
                 cls0 = cls1 = CPATTN_TILE_FULL;

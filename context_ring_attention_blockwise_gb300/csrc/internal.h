@@ -25,7 +25,8 @@ struct WsLayout {
     size_t header = 0;      // uint32[kHeaderWords]
     size_t posL = 0;        // int32 [n_cp][n]: position id of (rank, local index)
     size_t tile_mm = 0;     // int32x4 [n_cp][n_qt]: min, max position of each tile, min over the
-                            // tiles from this one to the end of its block, unused
+                            // tiles from this one to the end of its block, max over the tiles
+                            // from the start of its block to this one
     size_t order = 0;       // int32 [n_cp * n_qt]: (rank, q-tile) pairs, longest first
     size_t counts = 0;      // uint64 [n_cp][n_cp][2]: tiles computed per (rank, step), FULL / DIAG
     size_t sched = 0;       // uint32 [1 + n_cp]: work counters of the persistent kernel (fused, each step)

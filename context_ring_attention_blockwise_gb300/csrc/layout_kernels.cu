@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restric
 }
 
 // Per rank block, the minimum position over tiles kt..n_qt-1 (a backward scan): a key walk that
-// finds it above every query position skips the rest of the block in one step.
+// finds it above every query position skips the rest of the block in one step. And the maximum
+// over tiles 0..kt (a forward scan, non-decreasing in kt): under per-query lower bounds a walk
+// skips a block whose maximum lies below every bound, or searches for its first tile that does not.
 __global__ void tile_suffix_kernel(int4* __restrict__ tile_mm, int n_cp, int n_qt) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= n_cp) return;
@@ -91,6 +93,13 @@ __global__ void tile_suffix_kernel(int4* __restrict__ tile_mm, int n_cp, int n_q
         int4 t = tile_mm[(int64_t)r * n_qt + kt];
         run = min(run, t.x);
         t.z = run;
+        tile_mm[(int64_t)r * n_qt + kt] = t;
+    }
+    int pre = INT_MIN;
+    for (int kt = 0; kt < n_qt; ++kt) {
+        int4 t = tile_mm[(int64_t)r * n_qt + kt];
+        pre = max(pre, t.y);
+        t.w = pre;
         tile_mm[(int64_t)r * n_qt + kt] = t;
     }
 }
