@@ -322,7 +322,10 @@ def run_gpu(args, w):
     if rank == 0:
         kernel_ms = attn_ms if attn_ms is not None else ms_per_step
         achieved = flops_eff(w) / (kernel_ms * 1e-3) / 1e12
-        launches_per_step = (3 if not ring else 1 + 1 + w.n_cp + 1)
+        # the library's kernels per step: placement (pos_tiles, tile_suffix, permute), then per
+        # attention launch the per-row-group tile counts and the attention kernel; the ring-step
+        # path launches attention once per step and finalizes once
+        launches_per_step = (3 + 2) if not ring else (3 + 2 * w.n_cp + 1)
         result = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
