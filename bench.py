@@ -282,39 +282,68 @@ def run_gpu(args, w):
         perm_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
         attn_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
 
-    # e2e through the public API with host buffers: H2D of the inputs from pinned memory and D2H
-    # of O and lse into pinned memory, every step, inside the timed region.
+    # e2e through the public API with host buffers: every step copies its inputs from pinned host
+    # memory and reads O and lse back into pinned host memory, inside the timed region. Two device
+    # buffer sets and two copy streams double-buffer the steps, as a caller streaming batches
+    # would: the upload of step i+1 and the readback of step i-1 overlap the forward of step i.
     qp = torch.from_numpy(q_h.view(np.int16)).view(torch.bfloat16).pin_memory()
     kp = torch.from_numpy(k_h.view(np.int16)).view(torch.bfloat16).pin_memory()
     vp = torch.from_numpy(v_h.view(np.int16)).view(torch.bfloat16).pin_memory()
-    op = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    lp = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(args.steps, 5))
+    bufs = [(q, k, v, o, lse),
+            (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o), torch.empty_like(lse))]
+    outs = [(torch.empty(o.shape, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(lse.shape, dtype=torch.float32).pin_memory()) for _ in range(2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e_steps = max(3, min(args.steps, 8))
 
-    def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        if ring:
-            cp.ring_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream, copy_stream=copy)
-        else:
-            cp.forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream)
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+    def e2e_run(n):
+        computed = [None, None]   # forward of the last step that used each buffer set
+        read = [None, None]       # readback of that step
+        for i in range(n):
+            s = i % 2
+            qb, kb, vb, ob, lb = bufs[s]
+            with torch.cuda.stream(up):
+                if computed[s] is not None:
+                    up.wait_event(computed[s])
+                qb.copy_(qp, non_blocking=True)
+                kb.copy_(kp, non_blocking=True)
+                vb.copy_(vp, non_blocking=True)
+                uploaded = torch.cuda.Event()
+                uploaded.record(up)
+            stream.wait_event(uploaded)
+            if read[s] is not None:
+                stream.wait_event(read[s])
+            if ring:
+                cp.ring_forward(qb, kb, vb, plan, ws=ws, out=ob, lse=lb, stream=stream, copy_stream=copy)
+            else:
+                cp.forward(qb, kb, vb, plan, ws=ws, out=ob, lse=lb, stream=stream)
+            computed[s] = torch.cuda.Event()
+            computed[s].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[s])
+                outs[s][0].copy_(ob, non_blocking=True)
+                outs[s][1].copy_(lb, non_blocking=True)
+                read[s] = torch.cuda.Event()
+                read[s].record(down)
+        for r in read:
+            if r is not None:
+                stream.wait_event(r)
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    up.wait_stream(stream)
+    e2e_run(e2e_steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dist, dev)
+    for s in range(2):
+        assert torch.equal(outs[s][0].view(torch.int16), o.cpu().view(torch.int16)), "e2e readback differs from the device-resident forward"
     h2d = q_h.nbytes + k_h.nbytes + v_h.nbytes
-    d2h = op.numel() * 2 + lp.numel() * 4
+    d2h = o.numel() * 2 + lse.numel() * 4
 
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -343,7 +372,7 @@ def run_gpu(args, w):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
-    del qp, kp, vp, op, lp
+    del qp, kp, vp, outs, bufs
     if rank == 0 and args.extras and not ring:
         result["extras"] = extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks)
     if rank == 0 and args.cpu_baseline:

@@ -3,9 +3,11 @@
 // and kernel launches. Every compute step runs in the CUDA kernels.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -60,6 +62,29 @@ cpattn_status_t check_ws(const Plan& p, int B, const void* ws, size_t ws_bytes, 
 template <class T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
+// The plan's unit orders as the source of an asynchronous upload: a page-locked copy made on
+// first use (order, then order_q, then order_kv), or the plan's own vectors when page-locked
+// memory cannot be had (the upload is then still correct, only possibly host-synchronous).
+const int32_t* order_src(Plan& p, int which) {
+    static std::mutex mu;   // calls on one plan from several threads create the copy once
+    std::lock_guard<std::mutex> lock(mu);
+    const size_t n0 = p.order.size(), n1 = p.order_q.size(), n2 = p.order_kv.size();
+    if (!p.pinned_orders) {
+        void* h = nullptr;
+        if (cudaHostAlloc(&h, sizeof(int32_t) * (n0 + n1 + n2), cudaHostAllocDefault) == cudaSuccess) {
+            int32_t* d = static_cast<int32_t*>(h);
+            std::copy(p.order.begin(), p.order.end(), d);
+            std::copy(p.order_q.begin(), p.order_q.end(), d + n0);
+            std::copy(p.order_kv.begin(), p.order_kv.end(), d + n0 + n1);
+            p.pinned_orders = d;
+        } else {
+            cudaGetLastError();   // not sticky; clear it so later checks do not see it
+        }
+    }
+    if (p.pinned_orders) return p.pinned_orders + (which == 0 ? 0 : which == 1 ? n0 : n0 + n1);
+    return which == 0 ? p.order.data() : which == 1 ? p.order_q.data() : p.order_kv.data();
+}
+
 // Reset the header, upload the tile order, place tokens and position ids.
 cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
                          cudaStream_t st, const int32_t* lo = nullptr) {
@@ -68,7 +93,7 @@ cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const voi
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
     e = cudaMemsetAsync(at<char>(ws, w.counts), 0, w.sched + sizeof(uint32_t) * (1 + (size_t)p.n_cp) - w.counts, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(counts)");
-    e = cudaMemcpyAsync(at<char>(ws, w.order), p.order.data(), sizeof(int32_t) * p.order.size(),
+    e = cudaMemcpyAsync(at<char>(ws, w.order), order_src(p, 0), sizeof(int32_t) * p.order.size(),
                         cudaMemcpyHostToDevice, st);
     if (e) return cuda_fail(e, "cudaMemcpyAsync(order)");
     cpattn::PermuteArgs a{};
@@ -147,6 +172,7 @@ cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan) {
         if (p->ev_copy[i]) cudaEventDestroy(p->ev_copy[i]);
     }
     if (p->ev_start) cudaEventDestroy(p->ev_start);
+    if (p->pinned_orders) cudaFreeHost(p->pinned_orders);
     delete p;
     return CPATTN_OK;
 }
@@ -240,13 +266,21 @@ cpattn_status_t backward_impl(cpattn_plan_t plan, int B, const void* q, const vo
     pa.B = B; pa.T = p->T; pa.n = p->n; pa.m = p->m; pa.h = p->h; pa.d = p->d; pa.n_cp = p->n_cp;
     pa.layout = p->layout; pa.n_qt = p->n_qt;
     pa.o = o; pa.dout = dout; pa.lse = lse;
-    pa.doL = at<char>(ws, w.doL); pa.lse2L = at<float>(ws, w.lse2); pa.DL = at<float>(ws, w.Dl);
-    int e = cpattn::launch_bwd_prep(pa, st);
+    pa.doL = at<char>(ws, w.doL); pa.nlse2L = at<float>(ws, w.lse2); pa.nDL = at<float>(ws, w.Dl);
+    int e = 0;
+    if (p->n % 128 != 0) {
+        // the padding after a short last tile must hold finite values: zero both side tables
+        const size_t padded = sizeof(float) * (size_t)p->n_cp * B * p->h * (size_t)p->n_qt * 128;
+        e = cudaMemsetAsync(at<char>(ws, w.lse2), 0, padded, st);
+        if (!e) e = cudaMemsetAsync(at<char>(ws, w.Dl), 0, padded, st);
+        if (e) return cuda_fail(e, "cudaMemsetAsync(backward side tables)");
+    }
+    e = cpattn::launch_bwd_prep(pa, st);
     if (e) return cuda_fail(e, "backward prep kernel");
     const size_t nu = (size_t)p->n_cp * p->n_qt;
-    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), p->order_q.data(), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), order_src(*p, 1), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
     if (!e)
-        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, p->order_kv.data(), sizeof(int32_t) * nu,
+        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, order_src(*p, 2), sizeof(int32_t) * nu,
                             cudaMemcpyHostToDevice, st);
     if (e) return cuda_fail(e, "cudaMemcpyAsync(backward order)");
     cpattn::BwdLaunch a{};
@@ -254,7 +288,7 @@ cpattn_status_t backward_impl(cpattn_plan_t plan, int B, const void* q, const vo
     a.layout = p->layout; a.causal = p->causal; a.n_qt = p->n_qt;
     a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)p->d));
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL); a.doL = at<char>(ws, w.doL);
-    a.lse2L = at<float>(ws, w.lse2); a.DL = at<float>(ws, w.Dl);
+    a.nlse2L = at<float>(ws, w.lse2); a.nDL = at<float>(ws, w.Dl);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
     a.order_q = at<int32_t>(ws, w.bwd_order); a.order_kv = a.order_q + nu;
     a.loL = lo ? at<int32_t>(ws, w.loL) : nullptr;

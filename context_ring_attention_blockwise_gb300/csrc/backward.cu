@@ -8,7 +8,7 @@
 // dV_u = sum_t P_tu dO_t, the sums over t running over the query heads of the key's group.
 //
 // Three kernels:
-//   bwd_prep_kernel   D_t from O and dO (fp32), and dO, lse (as log2) and D in layout order.
+//   bwd_prep_kernel   D_t from O and dO (fp32), and dO, -lse (as log2) and -D in layout order.
 //   bwd_dkdv_kernel   one CTA per key tile (128 keys of one rank block, one KV head). It walks
 //                     the query tiles in ring order -- the block's gradient visits rank src + s
 //                     at step s -- and for every visible (query tile, query head of the group):
@@ -50,12 +50,12 @@ enum BwdSite : int { kBSiteStage = 101, kBSiteStageEmpty, kBSiteFixed, kBSiteSt,
 
 struct BwdParams {
     int B, h, n_kv, g, n_cp, n_qt, causal, layout;
-    int64_t n, m, T, n_pad;   // n_pad = n_qt * 128: row stride of lse2L and DL
+    int64_t n, m, T, n_pad;   // n_pad = n_qt * 128: row stride of nlse2L and nDL
     float scale, scale_log2;
     const int32_t* posL;
     const int4* tile_mm;
-    const float* lse2L;   // [n_cp][B][h][n_pad] lse * log2(e) (tile starts 512-byte aligned)
-    const float* DL;      // [n_cp][B][h][n_pad]
+    const float* nlse2L;  // [n_cp][B][h][n_pad] -lse * log2(e) (tile starts 512-byte aligned; padding 0)
+    const float* nDL;     // [n_cp][B][h][n_pad] -D (padding 0)
     const int32_t* loL;        // [n_cp][n] lowest visible key position per query (document masks), or NULL
     const int4* tile_lo;       // [n_cp][n_qt] (min, max) of loL over a query tile, or NULL
     const int32_t* order_q;    // (r * n_qt + qt), heaviest first
@@ -121,7 +121,7 @@ __device__ __forceinline__ int2 tile_bound(const BwdParams& P, int r, int qt) {
 // ---- shared-memory layout and barriers (both tcgen05 kernels) --------------------------
 // fixed pair: the CTA's own two tiles (K, V for dK/dV; Q, dO for dQ), loaded once;
 // stream pair: the walked tiles (Q, dO for dK/dV; K, V for dQ), kNS stages;
-// side: per stage 2 x 128 floats (lse2 and D of the query tile, dK/dV only), bulk-copied.
+// side: per stage 2 x 128 floats (-lse2 and -D of the query tile, dK/dV only), bulk-copied.
 template <int D>
 struct BCfg {
     static constexpr int PANELS = D / 64;
@@ -131,36 +131,50 @@ struct BCfg {
     static constexpr int OFF_S = 2 * TILE;                          // stream: stage st, member m at + (2 st + m) TILE
     static constexpr int OFF_SIDE = OFF_S + 2 * kNS * TILE;         // float [kNS][2][128]
     static constexpr int OFF_BAR = OFF_SIDE + kNS * 2 * 128 * 4;
-    static constexpr int NBAR = 6 + 2 * kNS + kRing;
+    static constexpr int NBAR = 7 + 2 * kNS + kRing;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_RING = (OFF_MISC + 64 + 15) / 16 * 16;   // int4 [kRing]
     static constexpr int SMEM_BYTES = OFF_RING + 16 * kRing + 1024;
     static_assert(OFF_S % 1024 == 0 && OFF_SIDE % 16 == 0 && OFF_BAR % 8 == 0 && OFF_RING % 16 == 0,
                   "shared-memory regions must keep their alignment");
-    // tensor memory: two accumulators (A0, A1) and two score-shaped buffers (X0, X1)
-    static constexpr uint32_t COL_A0 = 0, COL_A1 = D, COL_X0 = 2 * D, COL_X1 = 2 * D + 128;
+    // tensor memory: two accumulators (A0, A1: dV and dK, or dQ), the score tile S and the dP
+    // tile (128 columns each). The elementwise warps overwrite the first half of each warpgroup's
+    // 64 columns of S with packed bf16 P and of dP with packed bf16 dS, the A operands of the
+    // accumulating MMAs.
+    static constexpr uint32_t COL_A0 = 0, COL_A1 = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+    static_assert(2 * D + 2 * 128 <= 512, "tensor-memory columns");
 };
 
+// A walk step runs in two phases on the elementwise warps: P from S, then dS from dP (P stays in
+// registers in between). The barriers follow them:
+//   s_full   the score MMA of the step has completed          (MMA commit)
+//   p_done   P has been read out of S (and, for dK/dV, packed back into it)  (8 warps)
+//   dp_full  the dP MMA of the step has completed             (MMA commit)
+//   ds_done  dS has been packed into the dP columns           (8 warps)
+// The MMA issuer orders each step as  [p_done] dV or S(next) ... [ds_done] dK or dQ, dP(next),
+// so the score MMA of the next step and the dP MMA overlap the elementwise phases.
 template <int D>
 struct BBars {
     uint32_t base;
     __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
     __device__ uint32_t fixed_full() const { return at(0); }
-    __device__ uint32_t x_full() const { return at(1); }        // both score-shaped MMAs done
-    __device__ uint32_t p_full() const { return at(2); }        // elementwise results in TMEM
-    __device__ uint32_t acc_done() const { return at(3); }      // accumulating MMAs of a step done
-    __device__ uint32_t drain() const { return at(4); }
-    __device__ uint32_t spare() const { return at(5); }
-    __device__ uint32_t st_full(int s) const { return at(6 + s); }
-    __device__ uint32_t st_empty(int s) const { return at(6 + kNS + s); }
-    __device__ uint32_t ring_full(int s) const { return at(6 + 2 * kNS + s); }
+    __device__ uint32_t s_full() const { return at(1); }
+    __device__ uint32_t p_done() const { return at(2); }
+    __device__ uint32_t dp_full() const { return at(3); }
+    __device__ uint32_t ds_done() const { return at(4); }
+    __device__ uint32_t acc_done() const { return at(5); }          // accumulating MMAs of a step done
+    __device__ uint32_t drain() const { return at(6); }
+    __device__ uint32_t st_full(int s) const { return at(7 + s); }
+    __device__ uint32_t st_empty(int s) const { return at(7 + kNS + s); }
+    __device__ uint32_t ring_full(int s) const { return at(7 + 2 * kNS + s); }
     __device__ void init() const {
         mbar_init(fixed_full(), 1);
-        mbar_init(x_full(), 1);
-        mbar_init(p_full(), 8);                 // one lane per elementwise warp
+        mbar_init(s_full(), 1);
+        mbar_init(p_done(), 8);                 // one lane per elementwise warp
+        mbar_init(dp_full(), 1);
+        mbar_init(ds_done(), 8);
         mbar_init(acc_done(), 1);
         mbar_init(drain(), 1);
-        mbar_init(spare(), 1);
         for (int s = 0; s < kNS; ++s) {
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
@@ -185,7 +199,7 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
 // =============================================================================================
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                        const float* __restrict__ lse, uint4* __restrict__ doL,
-                                                       float* __restrict__ lse2L, float* __restrict__ DL, int B,
+                                                       float* __restrict__ nlse2L, float* __restrict__ nDL, int B,
                                                        int64_t T, int64_t n, int64_t m, int64_t n_pad, int h, int d,
                                                        int n_cp, int layout) {
     const int cpr = d / 8;                       // 8 or 16 threads per row, aligned within the warp
@@ -226,9 +240,57 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint4* __restrict__
         if (c == 0) {
             const int64_t prow = (((int64_t)r * B + b) * h + hd) * n_pad + j;
             const float l = __ldg(lse + ((int64_t)b * h + hd) * T + t);
-            lse2L[prow] = l * kLog2e;             // -inf stays -inf: such a row has P = 0
-            DL[prow] = part;
+            nlse2L[prow] = -l * kLog2e;           // negated: the kernels add them in fused multiply-adds
+            nDL[prow] = -part;
         }
+    }
+}
+
+// ---- elementwise bodies -----------------------------------------------------------------
+// 32 columns of one TMEM lane at a time, in packed fp32 pairs: x = s scale log2(e) - lse2,
+// P = 2^x; later dS = P (dP - D). Masked chunks force x = -inf where the bit of the column is
+// clear, which makes P = 0 and dS = 0 (dP and the side tables are finite, their padding zero).
+
+// P of 32 columns; nl = -lse2 per column (dK/dV: the columns are queries, nl4 from shared
+// memory) or per row (dQ: nl4 == nullptr, nl2 the row's pair).
+template <bool MASKED>
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[32], const float4* nl4, uint64_t nl2, uint64_t c2,
+                                        uint32_t vis_bits, float* pf) {
+#pragma unroll
+    for (int q2 = 0; q2 < 16; ++q2) {
+        uint64_t nl = nl2;
+        if (nl4) {
+            const float4 l = nl4[q2 >> 1];
+            nl = (q2 & 1) ? f2_pack(l.z, l.w) : f2_pack(l.x, l.y);
+        }
+        float x[2];
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q2]), __uint_as_float(sr[2 * q2 + 1])), c2, nl), x[0], x[1]);
+        if (MASKED) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) x[e] = ((vis_bits >> (2 * q2 + e)) & 1u) ? x[e] : -INFINITY;
+        }
+        pf[2 * q2] = ex2(x[0]);
+        pf[2 * q2 + 1] = ex2(x[1]);
+    }
+}
+__device__ __forceinline__ void pack_chunk(const float* v, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int q2 = 0; q2 < 16; ++q2) pk[q2] = pack_bf16(v[2 * q2], v[2 * q2 + 1]);
+}
+// dS = P (dP - D) of 32 columns, packed; nd = -D per column (nd4) or per row (nd2).
+__device__ __forceinline__ void ds_chunk(const uint32_t (&dr)[32], const float* pf, const float4* nd4, uint64_t nd2,
+                                         uint32_t (&pd)[16]) {
+#pragma unroll
+    for (int q2 = 0; q2 < 16; ++q2) {
+        uint64_t nd = nd2;
+        if (nd4) {
+            const float4 d4 = nd4[q2 >> 1];
+            nd = (q2 & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+        }
+        const uint64_t t = f2_add(f2_pack(__uint_as_float(dr[2 * q2]), __uint_as_float(dr[2 * q2 + 1])), nd);
+        float ds[2];
+        f2_unpack(f2_mul(f2_pack(pf[2 * q2], pf[2 * q2 + 1]), t), ds[0], ds[1]);
+        pd[q2] = pack_bf16(ds[0], ds[1]);
     }
 }
 
@@ -312,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t side = sb + C::OFF_SIDE + st * 2 * 512;
                     const int64_t prow = (((int64_t)r * P.B + b) * P.h + head) * P.n_pad + (int64_t)qt * 128;
-                    bulk_copy_g2s(side, P.lse2L + prow, 512, bars.st_full(st));
-                    bulk_copy_g2s(side + 512, P.DL + prow, 512, bars.st_full(st));
+                    bulk_copy_g2s(side, P.nlse2L + prow, 512, bars.st_full(st));
+                    bulk_copy_g2s(side + 512, P.nDL + prow, 512, bars.st_full(st));
                     ++nl;
                 }
                 st_shared_v4(ring + 16u * (uint32_t)slot, (uint32_t)r, (uint32_t)qt, (uint32_t)head, (uint32_t)flags);
@@ -350,67 +412,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issue
-            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // S^T: A = K (K-major), B = Q (K-major)
-            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // dV: A = P^T (TMEM), B = dO (MN-major)
+            // ---------------- MMA issue. Per walked query tile (stage st):
+            //   S^T = K Q^T into S and dP^T = V dO^T into dP           (SS form)
+            //   dV += P^T dO once P^T is packed into S                 (TS form)
+            //   dK += dS^T Q once dS^T is packed into dP                (TS form)
+            // issued as  [p_done] dV(i), S(i+1), [ds_done] dK(i), dP(i+1): the score MMAs of the next
+            // tile run while the elementwise warps work on this one. MMAs run in issue order, so
+            // S(i+1) cannot overwrite P^T before dV(i) has read it, nor dP(i+1) dS^T before dK(i).
+            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // A = K or V, B = Q or dO (K-major)
+            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // A = P^T / dS^T (TMEM), B = dO / Q (MN-major)
             const uint32_t sK = sb + C::OFF_F0, sV = sb + C::OFF_F1;
-            const uint32_t tS = tmem + C::COL_X0, tDP = tmem + C::COL_X1;
-            const uint32_t tdV = tmem + C::COL_A0, tdK = tmem + C::COL_A1;
+            const uint32_t tdV = tmem + C::COL_A0, tdK = tmem + C::COL_A1, tS = tmem + C::COL_S, tDP = tmem + C::COL_DP;
+            auto score = [&](uint32_t d, uint32_t a, uint32_t b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(d, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), kIdSS, kk > 0);
+                }
+            };
+            // packed P^T / dS^T: the 64 queries of warpgroup w in columns 64 w .. 64 w + 31 of their
+            // buffer, so query 16 kk .. 16 kk + 15 sits at 64 (kk / 4) + 8 (kk % 4)
+            auto accumulate = [&](uint32_t d, uint32_t a_t, uint32_t b, bool first) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(d, a_t + 64 * (kk >> 2) + 8 * (kk & 3), desc_sw128(b + kk * 2048, C::PANEL_BYTES, 1024),
+                                kIdTS, (first && kk == 0) ? 0u : 1u);
+            };
+            auto sQ_of = [&](int st) { return sb + C::OFF_S + (2 * st) * C::TILE; };
             bool ok = wait(bars.fixed_full(), 0, kBSiteFixed);
+            int4 e = make_int4(0, 0, 0, kFlagEmpty);
+            if (ok) ok = wait(bars.ring_full(0), 0, kBSiteWalk);
+            if (ok) e = ld_shared_v4(ring);
+            if (ok && !(e.w & kFlagEmpty)) {
+                ok = wait(bars.st_full(0), 0, kBSiteStage);
+                if (ok) {
+                    tc_fence_after();
+                    score(tS, sK, sQ_of(0));
+                    mma_commit(bars.s_full());
+                    score(tDP, sV, sQ_of(0) + C::TILE);
+                    mma_commit(bars.dp_full());
+                }
+            }
             int step = 0;
-            while (ok) {
-                const int slot = step % kRing, st = step % kNS;
-                if (!wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk)) break;
-                const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
-                if (e.w & kFlagEmpty) break;
-                if (!wait(bars.st_full(st), (step / kNS) & 1, kBSiteStage)) break;
+            while (ok && !(e.w & kFlagEmpty)) {
+                const int st = step % kNS, st1 = (step + 1) % kNS;
+                const bool last = (e.w & kFlagLast) != 0;
+                if (!wait(bars.p_done(), step & 1, kBSiteP)) break;
                 tc_fence_after();
-                const uint32_t sQ = sb + C::OFF_S + (2 * st) * C::TILE, sDO = sQ + C::TILE;
-                // S^T = K Q^T and dP^T = V dO^T (the previous step's accumulating MMAs, issued
-                // before these by this thread, have read P^T / dS^T already: MMAs run in order)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                    mma_bf16_ss(tS, desc_sw128(sK + off, 16, 1024), desc_sw128(sQ + off, 16, 1024), kIdSS, kk > 0);
+                accumulate(tdV, tS, sQ_of(st) + C::TILE, step == 0);
+                int4 nx = e;
+                if (!last) {
+                    const int n1 = step + 1;
+                    if (!wait(bars.ring_full(n1 % kRing), (n1 / kRing) & 1, kBSiteWalk)) break;
+                    nx = ld_shared_v4(ring + 16u * (uint32_t)(n1 % kRing));
+                    if (!wait(bars.st_full(st1), (n1 / kNS) & 1, kBSiteStage)) break;
+                    tc_fence_after();
+                    score(tS, sK, sQ_of(st1));
+                    mma_commit(bars.s_full());
                 }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                    mma_bf16_ss(tDP, desc_sw128(sV + off, 16, 1024), desc_sw128(sDO + off, 16, 1024), kIdSS, kk > 0);
-                }
-                mma_commit(bars.x_full());
-                if (!wait(bars.p_full(), step & 1, kBSiteP)) break;
+                if (!wait(bars.ds_done(), step & 1, kBSiteP)) break;
                 tc_fence_after();
-                // dV += P^T dO, dK += dS^T Q. P^T / dS^T: query columns 0..63 packed into columns
-                // 0..31 of their buffer, 64..127 into 64..95 (each warpgroup writes inside its own half).
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_bf16_ts(tdV, tS + acol, desc_sw128(sDO + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
-                                (step > 0 || kk > 0) ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_bf16_ts(tdK, tDP + acol, desc_sw128(sQ + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
-                                (step > 0 || kk > 0) ? 1u : 0u);
-                }
+                accumulate(tdK, tDP, sQ_of(st), step == 0);
                 mma_commit(bars.st_empty(st));
                 mma_commit(bars.acc_done());
+                if (!last) {
+                    score(tDP, sV, sQ_of(st1) + C::TILE);
+                    mma_commit(bars.dp_full());
+                }
                 ++step;
-                if (e.w & kFlagLast) break;
+                if (last) break;
+                e = nx;
             }
             mma_commit(bars.drain());
             wait(bars.drain(), 0, kBSiteDrain, false);
         }
     } else if (warp >= 4) {
-        // ---------------- elementwise: warpgroup wg takes query columns 64 wg .. 64 wg + 63
+        // ---------------- elementwise: warpgroup wg takes query columns 64 wg .. 64 wg + 63,
+        // in two chunks of 32
         const int wg = (warp - 4) >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;                      // key row of the tile (TMEM lane)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const int64_t jk = (int64_t)kt * 128 + row;               // local key index on rank src
         const bool key_valid = jk < P.n;
         const int kpos = key_valid ? __ldg(P.posL + (int64_t)src * P.n + jk) : INT_MAX;
+        const uint64_t c2 = f2_pack(P.scale_log2, P.scale_log2);
+        const uint32_t xs = tmem + lane_base + C::COL_S + 64 * wg, xd = tmem + lane_base + C::COL_DP + 64 * wg;
         bool ok = true;
         int step = 0;
         int n_steps = 0;
@@ -423,24 +509,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qt = e.y, tmask = (e.w >> 2) & 1;
             int qvalid = 128;
             if (qt == P.n_qt - 1 && (P.n % 128) != 0) qvalid = (int)(P.n - (int64_t)qt * 128);
-            ok = __all_sync(0xffffffffu, wait(bars.x_full(), step & 1, kBSiteSt));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t side = sb + C::OFF_SIDE + st * 2 * 512;   // lse2 [128], D [128]
             const int64_t qoff = (int64_t)e.x * P.n + (int64_t)qt * 128;   // positions of the query tile
             const int32_t* qposg = P.posL + qoff;
+            // Which queries of each chunk this row is seen by: all on unmasked tiles (no branch in
+            // the element loop), else by position, one bit per query column. Computed before the
+            // scores are ready.
+            uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+            if (tmask) {
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int c0 = wg * 64 + ch * 32;                    // first query column of the chunk
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
-                tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
-                uint32_t pp[16], pd[16];
-                // Which keys of the chunk this row sees: all of them on unmasked tiles (no branch in
-                // the element loop), else by position, one bit per query column.
-                uint32_t vis_bits = 0xffffffffu;
-                if (tmask) {
-                    vis_bits = 0u;
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int c0 = 64 * wg + 32 * ch;
+                    uint32_t bits = 0u;
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
                         const int col = c0 + 4 * q4;
@@ -463,41 +542,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) {
-                            const bool vis = key_valid && col + e4 < qvalid && (!P.causal || kpos <= qp[e4]) &&
-                                             (!LB || kpos >= ql[e4]);
-                            vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
+                            const bool vis_q = key_valid && col + e4 < qvalid && (!P.causal || kpos <= qp[e4]) &&
+                                               (!LB || kpos >= ql[e4]);
+                            bits |= (vis_q ? 1u : 0u) << (4 * q4 + e4);
                         }
                     }
+                    vis[ch] = bits;
                 }
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const int4 l4 = ld_shared_v4(side + 4u * (uint32_t)(c0 + 4 * q4));
-                    const int4 d4 = ld_shared_v4(side + 512u + 4u * (uint32_t)(c0 + 4 * q4));
-                    const float lv[4] = {__int_as_float(l4.x), __int_as_float(l4.y), __int_as_float(l4.z), __int_as_float(l4.w)};
-                    const float dv[4] = {__int_as_float(d4.x), __int_as_float(d4.y), __int_as_float(d4.z), __int_as_float(d4.w)};
-                    float pv[4], sv[4];
-#pragma unroll
-                    for (int e4 = 0; e4 < 4; ++e4) {
-                        const bool vis = (vis_bits >> (4 * q4 + e4)) & 1u;
-                        const float p = ex2(fmaf(__uint_as_float(sr[4 * q4 + e4]), P.scale_log2, -lv[e4]));
-                        const float ds = p * (__uint_as_float(dr[4 * q4 + e4]) - dv[e4]);
-                        pv[e4] = vis ? p : 0.f;
-                        sv[e4] = vis ? ds : 0.f;
-                    }
-                    pp[2 * q4] = pack_bf16(pv[0], pv[1]);
-                    pp[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
-                    pd[2 * q4] = pack_bf16(sv[0], sv[1]);
-                    pd[2 * q4 + 1] = pack_bf16(sv[2], sv[3]);
+            }
+            const float4* nl4 = reinterpret_cast<const float4*>(smem + C::OFF_SIDE + st * 2 * 512) + 16 * wg;   // -lse2
+            const float4* nd4 = nl4 + 32;                                                                       // -D
+            // phase 1: P^T from S^T, kept in registers, packed back into S for dV += P^T dO
+            ok = __all_sync(0xffffffffu, wait(bars.s_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+            float pf[64];
+            {
+                uint32_t sa[32], sb2[32];
+                tmem_ld32_nw(xs, sa);
+                tmem_ld32_nw(xs + 32, sb2);
+                tmem_ld_wait2(sa, sb2);
+                if (tmask) {
+                    p_chunk<true>(sa, nl4, 0, c2, vis[0], pf);
+                    p_chunk<true>(sb2, nl4 + 8, 0, c2, vis[1], pf + 32);
+                } else {
+                    p_chunk<false>(sa, nl4, 0, c2, 0u, pf);
+                    p_chunk<false>(sb2, nl4 + 8, 0, c2, 0u, pf + 32);
                 }
-                // packed column of query c: (c % 64) / 2 + 64 * (c / 64), inside this warpgroup's half
-                const uint32_t pcol = (uint32_t)(wg * 64 + ch * 16);
-                tmem_st16(tmem + lane_base + C::COL_X0 + pcol, pp);
-                tmem_st16(tmem + lane_base + C::COL_X1 + pcol, pd);
+                uint32_t pk[16];
+                pack_chunk(pf, pk);
+                tmem_st16(xs, pk);
+                pack_chunk(pf + 32, pk);
+                tmem_st16(xs + 16, pk);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full());
+            if (lane == 0) mbar_arrive(bars.p_done());
+            // phase 2: dS^T = P^T (dP^T - D), packed into dP for dK += dS^T Q
+            ok = __all_sync(0xffffffffu, wait(bars.dp_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t dr[32], pd[16];
+                tmem_ld32(xd + 32 * ch, dr);
+                ds_chunk(dr, pf + 32 * ch, nd4 + 8 * ch, 0, pd);
+                tmem_st16(xd + 16 * ch, pd);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.ds_done());
             ++step;
             ++n_steps;
             if (e.w & kFlagLast) break;
@@ -660,51 +756,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issue
-            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // S: A = Q, B = K (both K-major)
-            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // dQ: A = dS (TMEM), B = K (MN-major)
+            // ---------------- MMA issue. Per walked key tile (stage st):
+            //   S = Q K^T into S and dP = dO V^T into dP               (SS form)
+            //   dQ += dS K once dS is packed into dP                   (TS form)
+            // issued as  [p_done] S(i+1), [ds_done] dQ(i), dP(i+1): the next score MMA starts as soon
+            // as the elementwise warps hold P(i) in registers.
+            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // A = Q or dO, B = K or V (K-major)
+            constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // A = dS (TMEM), B = K (MN-major)
             const uint32_t sQ = sb + C::OFF_F0, sDO = sb + C::OFF_F1;
-            const uint32_t tS = tmem + C::COL_X0, tDP = tmem + C::COL_X1, tdQ = tmem + C::COL_A0;
+            const uint32_t tdQ = tmem + C::COL_A0, tS = tmem + C::COL_S, tDP = tmem + C::COL_DP;
+            auto score = [&](uint32_t d, uint32_t a, uint32_t b) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
+                    mma_bf16_ss(d, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), kIdSS, kk > 0);
+                }
+            };
+            auto sK_of = [&](int st) { return sb + C::OFF_S + (2 * st) * C::TILE; };
             bool ok = wait(bars.fixed_full(), 0, kBSiteFixed);
+            int4 e = make_int4(0, 0, 0, kFlagEmpty);
+            if (ok) ok = wait(bars.ring_full(0), 0, kBSiteWalk);
+            if (ok) e = ld_shared_v4(ring);
+            if (ok && !(e.w & kFlagEmpty)) {
+                ok = wait(bars.st_full(0), 0, kBSiteStage);
+                if (ok) {
+                    tc_fence_after();
+                    score(tS, sQ, sK_of(0));
+                    mma_commit(bars.s_full());
+                    score(tDP, sDO, sK_of(0) + C::TILE);
+                    mma_commit(bars.dp_full());
+                }
+            }
             int step = 0;
-            while (ok) {
-                const int slot = step % kRing, st = step % kNS;
-                if (!wait(bars.ring_full(slot), (step / kRing) & 1, kBSiteWalk)) break;
-                const int4 e = ld_shared_v4(ring + 16u * (uint32_t)slot);
-                if (e.w & kFlagEmpty) break;
-                if (!wait(bars.st_full(st), (step / kNS) & 1, kBSiteStage)) break;
-                tc_fence_after();
-                const uint32_t sK = sb + C::OFF_S + (2 * st) * C::TILE, sV = sK + C::TILE;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                    mma_bf16_ss(tS, desc_sw128(sQ + off, 16, 1024), desc_sw128(sK + off, 16, 1024), kIdSS, kk > 0);
+            while (ok && !(e.w & kFlagEmpty)) {
+                const int st = step % kNS, st1 = (step + 1) % kNS;
+                const bool last = (e.w & kFlagLast) != 0;
+                if (!wait(bars.p_done(), step & 1, kBSiteP)) break;
+                int4 nx = e;
+                if (!last) {
+                    const int n1 = step + 1;
+                    if (!wait(bars.ring_full(n1 % kRing), (n1 / kRing) & 1, kBSiteWalk)) break;
+                    nx = ld_shared_v4(ring + 16u * (uint32_t)(n1 % kRing));
+                    if (!wait(bars.st_full(st1), (n1 / kNS) & 1, kBSiteStage)) break;
+                    tc_fence_after();
+                    score(tS, sQ, sK_of(st1));
+                    mma_commit(bars.s_full());
                 }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                    mma_bf16_ss(tDP, desc_sw128(sDO + off, 16, 1024), desc_sw128(sV + off, 16, 1024), kIdSS, kk > 0);
-                }
-                mma_commit(bars.x_full());
-                if (!wait(bars.p_full(), step & 1, kBSiteP)) break;
+                if (!wait(bars.ds_done(), step & 1, kBSiteP)) break;
                 tc_fence_after();
-                // dQ += dS K; dS packed like P^T in the dK/dV kernel (keys 64..127 at columns 64..95)
+                // dS packed like P^T in the dK/dV kernel: keys 16 kk .. 16 kk + 15 at 64 (kk / 4) + 8 (kk % 4)
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t acol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
-                    mma_bf16_ts(tdQ, tS + acol, desc_sw128(sK + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16_ts(tdQ, tDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                                desc_sw128(sK_of(st) + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
                                 (step > 0 || kk > 0) ? 1u : 0u);
-                }
                 mma_commit(bars.st_empty(st));
                 mma_commit(bars.acc_done());
+                if (!last) {
+                    score(tDP, sDO, sK_of(st1) + C::TILE);
+                    mma_commit(bars.dp_full());
+                }
                 ++step;
-                if (e.w & kFlagLast) break;
+                if (last) break;
+                e = nx;
             }
             mma_commit(bars.drain());
             wait(bars.drain(), 0, kBSiteDrain, false);
         }
     } else if (warp >= 4) {
-        // ---------------- elementwise: warpgroup wg takes key columns 64 wg .. 64 wg + 63
+        // ---------------- elementwise: warpgroup wg takes key columns 64 wg .. 64 wg + 63, in two
+        // chunks of 32
         const int wg = (warp - 4) >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;                      // query row of the tile (TMEM lane)
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -712,10 +833,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool q_valid = jq < P.n;
         const int64_t lrow = (((int64_t)r * P.B + b) * P.h + head) * P.n_pad + jq;
         const int qpos = q_valid ? __ldg(P.posL + (int64_t)r * P.n + jq) : INT_MIN;
-        const float lse2 = q_valid ? __ldg(P.lse2L + lrow) : -INFINITY;
-        const float Dv = q_valid ? __ldg(P.DL + lrow) : 0.f;
-        const bool row_live = q_valid && lse2 != -INFINITY;   // a row that sees some key
+        const float nl = q_valid ? __ldg(P.nlse2L + lrow) : INFINITY;
+        const bool row_live = q_valid && nl != INFINITY;      // a row that sees some key
+        // a row that sees no key gets x = -inf everywhere: P = 0 and dS = 0
+        const uint64_t nl2 = row_live ? f2_pack(nl, nl) : f2_pack(-INFINITY, -INFINITY);
+        const float nd = row_live ? __ldg(P.nDL + lrow) : 0.f;
+        const uint64_t nd2 = f2_pack(nd, nd);
+        const uint64_t c2 = f2_pack(P.scale_log2, P.scale_log2);
         const int qlo = (LB && q_valid) ? __ldg(P.loL + (int64_t)r * P.n + jq) : INT_MIN;
+        const uint32_t xs = tmem + lane_base + C::COL_S + 64 * wg, xd = tmem + lane_base + C::COL_DP + 64 * wg;
         bool ok = true;
         int step = 0, n_steps = 0;
         for (;;) {
@@ -728,21 +854,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int kvalid = 128;
             if (ktt == P.n_qt - 1 && (P.n % 128) != 0) kvalid = (int)(P.n - (int64_t)ktt * 128);
             const int64_t kbase = (int64_t)srcr * P.n + (int64_t)ktt * 128;
-            ok = __all_sync(0xffffffffu, wait(bars.x_full(), step & 1, kBSiteSt));
-            if (!ok) break;
-            tc_fence_after();
+            // Which keys of each chunk this row sees: all of them on unmasked tiles, else by
+            // position (keys beyond a short block are never seen), one bit per key column.
+            // Computed before the scores are ready.
+            uint32_t vis[2] = {0u, 0u};
+            if (tmask && row_live) {
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int c0 = wg * 64 + ch * 32;
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_base + C::COL_X0 + c0, sr);
-                tmem_ld32(tmem + lane_base + C::COL_X1 + c0, dr);
-                uint32_t pd[16];
-                // Which keys of the chunk this row sees: all of them on unmasked tiles, else by
-                // position (keys beyond a short block are never seen), one bit per key column.
-                uint32_t vis_bits = row_live ? 0xffffffffu : 0u;
-                if (tmask && row_live) {
-                    vis_bits = 0u;
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int c0 = 64 * wg + 32 * ch;
+                    uint32_t bits = 0u;
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4) {
                         const int col = c0 + 4 * q4;
@@ -758,29 +878,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
 #pragma unroll
                         for (int e4 = 0; e4 < 4; ++e4) {
-                            const bool vis = col + e4 < kvalid && (!P.causal || kp[e4] <= qpos) && (!LB || kp[e4] >= qlo);
-                            vis_bits |= (vis ? 1u : 0u) << (4 * q4 + e4);
+                            const bool vis_k = col + e4 < kvalid && (!P.causal || kp[e4] <= qpos) && (!LB || kp[e4] >= qlo);
+                            bits |= (vis_k ? 1u : 0u) << (4 * q4 + e4);
                         }
                     }
+                    vis[ch] = bits;
                 }
-#pragma unroll
-                for (int q2 = 0; q2 < 16; ++q2) {
-                    float sv[2];
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const bool vis = (vis_bits >> (2 * q2 + e2)) & 1u;
-                        const float p = ex2(fmaf(__uint_as_float(sr[2 * q2 + e2]), P.scale_log2, -lse2));
-                        const float ds = p * (__uint_as_float(dr[2 * q2 + e2]) - Dv);
-                        sv[e2] = vis ? ds : 0.f;
-                    }
-                    pd[q2] = pack_bf16(sv[0], sv[1]);
+            }
+            // phase 1: P from S, kept in registers; S is free for the next key tile's scores
+            ok = __all_sync(0xffffffffu, wait(bars.s_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+            float pf[64];
+            {
+                uint32_t sa[32], sb2[32];
+                tmem_ld32_nw(xs, sa);
+                tmem_ld32_nw(xs + 32, sb2);
+                tmem_ld_wait2(sa, sb2);
+                if (tmask) {
+                    p_chunk<true>(sa, nullptr, nl2, c2, vis[0], pf);
+                    p_chunk<true>(sb2, nullptr, nl2, c2, vis[1], pf + 32);
+                } else {
+                    p_chunk<false>(sa, nullptr, nl2, c2, 0u, pf);
+                    p_chunk<false>(sb2, nullptr, nl2, c2, 0u, pf + 32);
                 }
-                tmem_st16(tmem + lane_base + C::COL_X0 + (uint32_t)(wg * 64 + ch * 16), pd);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_done());
+            // phase 2: dS = P (dP - D), packed into dP for dQ += dS K
+            ok = __all_sync(0xffffffffu, wait(bars.dp_full(), step & 1, kBSiteSt));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t dr[32], pd[16];
+                tmem_ld32(xd + 32 * ch, dr);
+                ds_chunk(dr, pf + 32 * ch, nullptr, nd2, pd);
+                tmem_st16(xd + 16 * ch, pd);
             }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full());
+            if (lane == 0) mbar_arrive(bars.ds_done());
             ++step;
             ++n_steps;
             if (e.w & kFlagLast) break;
@@ -849,7 +989,7 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     P.causal = a.causal; P.layout = a.layout; P.n = a.n; P.m = a.m; P.T = a.T; P.n_pad = (int64_t)a.n_qt * 128;
     P.scale = a.scale; P.scale_log2 = a.scale * kLog2e;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm);
-    P.lse2L = a.lse2L; P.DL = a.DL; P.order_q = a.order_q; P.order_kv = a.order_kv;
+    P.nlse2L = a.nlse2L; P.nDL = a.nDL; P.order_q = a.order_q; P.order_kv = a.order_kv;
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
     P.header = a.header; P.timeout_ns = a.timeout_ns;
@@ -874,8 +1014,8 @@ int launch_bwd_prep(const BwdPrepArgs& a, void* stream) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int64_t blocks = (work + 255) / 256, cap = (int64_t)sms * 8;
     bwd_prep_kernel<<<(int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, static_cast<uint4*>(a.doL), a.lse2L,
-        a.DL, a.B, a.T, a.n, a.m, (int64_t)a.n_qt * 128, a.h, a.d, a.n_cp, a.layout);
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, static_cast<uint4*>(a.doL), a.nlse2L,
+        a.nDL, a.B, a.T, a.n, a.m, (int64_t)a.n_qt * 128, a.h, a.d, a.n_cp, a.layout);
     return (int)cudaGetLastError();
 }
 

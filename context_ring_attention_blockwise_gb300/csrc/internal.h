@@ -43,8 +43,8 @@ struct WsLayout {
     size_t ring_end = 0;
     // backward (after fwd_end; the ring-step regions are not used by the backward)
     size_t doL = 0;         // bf16 [n_cp][B][h][n][d] output gradient in layout order
-    size_t lse2 = 0;        // fp32 [n_cp][B][h][n_qt * 128] forward lse times log2(e)
-    size_t Dl = 0;          // fp32 [n_cp][B][h][n_qt * 128] D = <dO, O> of every query row
+    size_t lse2 = 0;        // fp32 [n_cp][B][h][n_qt * 128] -lse * log2(e) of the forward (padding 0)
+    size_t Dl = 0;          // fp32 [n_cp][B][h][n_qt * 128] -D = -<dO, O> of every query row (padding 0)
     size_t bwd_order = 0;   // int32 [2][n_cp * n_qt]: order_q, then order_kv
     size_t bwd_end = 0;
 };
@@ -66,6 +66,9 @@ struct Plan {
     CUevent_st* ev_copy[2] = {nullptr, nullptr};
     CUevent_st* ev_start = nullptr;
     int next_step = -1;             // step expected next on the ring path (-1: permute first)
+    // page-locked copy of order, order_q, order_kv (created on first use): an upload from
+    // pageable memory may block the calling thread until the stream drains
+    int32_t* pinned_orders = nullptr;
 };
 
 WsLayout ws_layout(const Plan& p, int B);
@@ -114,7 +117,7 @@ int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
 struct BwdPrepArgs {
     int B; int64_t T, n, m; int h, d, n_cp, layout, n_qt;
     const void* o; const void* dout; const float* lse;   // natural order
-    void* doL; float* lse2L; float* DL;                  // layout order
+    void* doL; float* nlse2L; float* nDL;                  // layout order
 };
 int launch_bwd_prep(const BwdPrepArgs& a, void* stream);
 
@@ -122,7 +125,7 @@ struct BwdLaunch {
     int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt;
     float scale;
     const void* qL; const void* kL; const void* vL; const void* doL;
-    const float* lse2L; const float* DL;
+    const float* nlse2L; const float* nDL;
     const int32_t* posL; const int32_t* tile_mm;
     const int32_t* order_q; const int32_t* order_kv;   // longest-first unit orders
     const int32_t* loL; const int32_t* tile_lo;         // document-mask lower bounds, or NULL
