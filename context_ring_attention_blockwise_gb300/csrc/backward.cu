@@ -131,7 +131,7 @@ struct BCfg {
     static constexpr int OFF_S = 2 * TILE;                          // stream: stage st, member m at + (2 st + m) TILE
     static constexpr int OFF_SIDE = OFF_S + 2 * kNS * TILE;         // float [kNS][2][128]
     static constexpr int OFF_BAR = OFF_SIDE + kNS * 2 * 128 * 4;
-    static constexpr int NBAR = 7 + 2 * kNS + kRing;
+    static constexpr int NBAR = 8 + 2 * kNS + kRing;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_RING = (OFF_MISC + 64 + 15) / 16 * 16;   // int4 [kRing]
     static constexpr int SMEM_BYTES = OFF_RING + 16 * kRing + 1024;
@@ -142,6 +142,9 @@ struct BCfg {
     // 64 columns of S with packed bf16 P and of dP with packed bf16 dS, the A operands of the
     // accumulating MMAs.
     static constexpr uint32_t COL_A0 = 0, COL_A1 = D, COL_S = 2 * D, COL_DP = 2 * D + 128;
+    // dQ only: the CTA's fixed Q and dO tiles as packed bf16 rows (D / 2 columns each), where the
+    // dK accumulator sits in the other kernel: the A operands of its score MMAs (TS form)
+    static constexpr uint32_t COL_Q = D, COL_DO = D + D / 2;
     static_assert(2 * D + 2 * 128 <= 512, "tensor-memory columns");
 };
 
@@ -162,19 +165,23 @@ struct BBars {
     __device__ uint32_t p_done() const { return at(2); }
     __device__ uint32_t dp_full() const { return at(3); }
     __device__ uint32_t ds_done() const { return at(4); }
-    __device__ uint32_t acc_done() const { return at(5); }          // accumulating MMAs of a step done
+    __device__ uint32_t spare() const { return at(5); }
+    // every MMA of the CTA has completed: committed once, after the last one (a single phase, so
+    // no waiter can mistake an older phase for it)
     __device__ uint32_t drain() const { return at(6); }
-    __device__ uint32_t st_full(int s) const { return at(7 + s); }
-    __device__ uint32_t st_empty(int s) const { return at(7 + kNS + s); }
-    __device__ uint32_t ring_full(int s) const { return at(7 + 2 * kNS + s); }
+    __device__ uint32_t fixed_tmem() const { return at(7); }        // dQ: Q and dO copied into TMEM (8 warps)
+    __device__ uint32_t st_full(int s) const { return at(8 + s); }
+    __device__ uint32_t st_empty(int s) const { return at(8 + kNS + s); }
+    __device__ uint32_t ring_full(int s) const { return at(8 + 2 * kNS + s); }
     __device__ void init() const {
         mbar_init(fixed_full(), 1);
         mbar_init(s_full(), 1);
         mbar_init(p_done(), 8);                 // one lane per elementwise warp
         mbar_init(dp_full(), 1);
         mbar_init(ds_done(), 8);
-        mbar_init(acc_done(), 1);
+        mbar_init(spare(), 1);
         mbar_init(drain(), 1);
+        mbar_init(fixed_tmem(), 8);
         for (int s = 0; s < kNS; ++s) {
             mbar_init(st_full(s), 1);
             mbar_init(st_empty(s), 1);
@@ -474,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 accumulate(tdK, tDP, sQ_of(st), step == 0);
                 mma_commit(bars.st_empty(st));
-                mma_commit(bars.acc_done());
                 if (!last) {
                     score(tDP, sV, sQ_of(st1) + C::TILE);
                     mma_commit(bars.dp_full());
@@ -600,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // epilogue: wait for the last accumulating MMAs, then write dK (scaled) and dV
         if (ok && n_steps > 0) {
-            ok = __all_sync(0xffffffffu, wait(bars.acc_done(), (n_steps - 1) & 1, kBSiteDone));
+            ok = __all_sync(0xffffffffu, wait(bars.drain(), 0, kBSiteDone));
             if (ok) tc_fence_after();
         }
         // tcgen05.ld is a warp-wide instruction: every lane loads, and only the lanes of valid
@@ -757,23 +763,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issue. Per walked key tile (stage st):
-            //   S = Q K^T into S and dP = dO V^T into dP               (SS form)
+            //   S = Q K^T into S and dP = dO V^T into dP               (TS form, Q and dO in TMEM)
             //   dQ += dS K once dS is packed into dP                   (TS form)
             // issued as  [p_done] S(i+1), [ds_done] dQ(i), dP(i+1): the next score MMA starts as soon
             // as the elementwise warps hold P(i) in registers.
-            constexpr uint32_t kIdSS = idesc_bf16(128, 128, 0, 0);   // A = Q or dO, B = K or V (K-major)
+            // The score MMAs take Q and dO from tensor memory (TS form), so only K and V are read
+            // from shared memory, which the stage loads also write.
+            constexpr uint32_t kIdX = idesc_bf16(128, 128, 0, 0);    // A = Q or dO (TMEM), B = K or V (K-major)
             constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);     // A = dS (TMEM), B = K (MN-major)
-            const uint32_t sQ = sb + C::OFF_F0, sDO = sb + C::OFF_F1;
+            const uint32_t tQ = tmem + C::COL_Q, tDO = tmem + C::COL_DO;
             const uint32_t tdQ = tmem + C::COL_A0, tS = tmem + C::COL_S, tDP = tmem + C::COL_DP;
-            auto score = [&](uint32_t d, uint32_t a, uint32_t b) {
+            auto score = [&](uint32_t d, uint32_t a_t, uint32_t b) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::PANEL_BYTES + (kk & 3) * 32;
-                    mma_bf16_ss(d, desc_sw128(a + off, 16, 1024), desc_sw128(b + off, 16, 1024), kIdSS, kk > 0);
+                    mma_bf16_ts(d, a_t + 8 * kk, desc_sw128(b + off, 16, 1024), kIdX, kk > 0);
                 }
             };
             auto sK_of = [&](int st) { return sb + C::OFF_S + (2 * st) * C::TILE; };
-            bool ok = wait(bars.fixed_full(), 0, kBSiteFixed);
+            bool ok = wait(bars.fixed_tmem(), 0, kBSiteFixed);
             int4 e = make_int4(0, 0, 0, kFlagEmpty);
             if (ok) ok = wait(bars.ring_full(0), 0, kBSiteWalk);
             if (ok) e = ld_shared_v4(ring);
@@ -781,9 +789,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait(bars.st_full(0), 0, kBSiteStage);
                 if (ok) {
                     tc_fence_after();
-                    score(tS, sQ, sK_of(0));
+                    score(tS, tQ, sK_of(0));
                     mma_commit(bars.s_full());
-                    score(tDP, sDO, sK_of(0) + C::TILE);
+                    score(tDP, tDO, sK_of(0) + C::TILE);
                     mma_commit(bars.dp_full());
                 }
             }
@@ -799,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     nx = ld_shared_v4(ring + 16u * (uint32_t)(n1 % kRing));
                     if (!wait(bars.st_full(st1), (n1 / kNS) & 1, kBSiteStage)) break;
                     tc_fence_after();
-                    score(tS, sQ, sK_of(st1));
+                    score(tS, tQ, sK_of(st1));
                     mma_commit(bars.s_full());
                 }
                 if (!wait(bars.ds_done(), step & 1, kBSiteP)) break;
@@ -811,9 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 desc_sw128(sK_of(st) + kk * 2048, C::PANEL_BYTES, 1024), kIdTS,
                                 (step > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bars.st_empty(st));
-                mma_commit(bars.acc_done());
                 if (!last) {
-                    score(tDP, sDO, sK_of(st1) + C::TILE);
+                    score(tDP, tDO, sK_of(st1) + C::TILE);
                     mma_commit(bars.dp_full());
                 }
                 ++step;
@@ -842,7 +849,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t c2 = f2_pack(P.scale_log2, P.scale_log2);
         const int qlo = (LB && q_valid) ? __ldg(P.loL + (int64_t)r * P.n + jq) : INT_MIN;
         const uint32_t xs = tmem + lane_base + C::COL_S + 64 * wg, xd = tmem + lane_base + C::COL_DP + 64 * wg;
-        bool ok = true;
+        // The fixed tiles into tensor memory: warpgroup 0 copies Q, warpgroup 1 dO, each thread its
+        // row. Row r of a 128-byte-swizzled panel holds its 16-byte chunk j at chunk j ^ (r % 8).
+        bool ok = __all_sync(0xffffffffu, wait(bars.fixed_full(), 0, kBSiteFixed));
+        if (ok) {
+            const uint8_t* tile = smem + (wg == 0 ? C::OFF_F0 : C::OFF_F1);
+            uint32_t rw[D / 2];
+#pragma unroll
+            for (int pn = 0; pn < C::PANELS; ++pn)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(tile + pn * C::PANEL_BYTES + row * 128 + ((j ^ (row & 7)) << 4));
+                    rw[32 * pn + 4 * j] = v.x;
+                    rw[32 * pn + 4 * j + 1] = v.y;
+                    rw[32 * pn + 4 * j + 2] = v.z;
+                    rw[32 * pn + 4 * j + 3] = v.w;
+                }
+            const uint32_t dst = tmem + lane_base + (wg == 0 ? C::COL_Q : C::COL_DO);
+            if constexpr (D == 128) tmem_st64(dst, rw);
+            else tmem_st32(dst, rw);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.fixed_tmem());
         int step = 0, n_steps = 0;
         for (;;) {
             const int slot = step % kRing;
@@ -926,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (e.w & kFlagLast) break;
         }
         if (ok && n_steps > 0) {
-            ok = __all_sync(0xffffffffu, wait(bars.acc_done(), (n_steps - 1) & 1, kBSiteDone));
+            ok = __all_sync(0xffffffffu, wait(bars.drain(), 0, kBSiteDone));
             if (ok) tc_fence_after();
         }
         // warp-wide TMEM loads; only the lanes of valid query rows store
