@@ -482,6 +482,26 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
                                      "the kernels compute seven (dQ recomputes S and dP)",
                        "includes": "placement, D = <dO, O> prep, dK/dV kernel, dQ kernel"}
     del wsb, dout, dq, dk, dv
+    # the head split (Ulysses) as the comparison workload: all-to-all, per-rank attention over
+    # every token of h / n_cp heads, all-to-all back; bytes per rank against the ring's
+    up = cp.UlyssesPlan(w.T, w.h, w.n_kv, w.d, w.n_cp, w.causal)
+    wsu = cp.alloc_workspace(up.workspace_size(w.B), dev)
+    ou, lseu = torch.empty_like(o), torch.empty_like(lse)
+    cp.ulysses_forward(q, k, v, up, ws=wsu, out=ou, lse=lseu, stream=stream)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(3):
+        cp.ulysses_forward(q, k, v, up, ws=wsu, out=ou, lse=lseu, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(up, wsu)
+    ms = a.elapsed_time(b) / 3
+    out["ulysses"] = {"ms": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12, "n_cp": w.n_cp,
+                      "heads_per_rank": w.h // w.n_cp, "kv_heads_per_rank": max(w.n_kv // w.n_cp, 1),
+                      "a2a_bytes_recv_per_rank": int(up.counts(w.B)["bytes_recv"][0]),
+                      "ring_kv_bytes_recv_per_rank": int(plan.counts(w.B)["kv_bytes_recv"][0]),
+                      "includes": "both all-to-alls (as on-GPU layout switches) and the per-rank attention"}
+    del wsu, ou, lseu, up
     return out
 
 

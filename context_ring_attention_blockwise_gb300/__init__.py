@@ -27,6 +27,7 @@ SYMBOLS = [
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
     "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked", "cpattn_backward_masked",
+    "cpattn_ulysses_plan", "cpattn_ulysses_workspace_size", "cpattn_ulysses_counts", "cpattn_ulysses_forward",
 ]
 
 
@@ -72,6 +73,10 @@ def lib():
                                          ctypes.c_size_t, _P]
     L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_ulysses_plan.argtypes = [_I64, i, i, i, i, i, ctypes.POINTER(_P)]
+    L.cpattn_ulysses_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_ulysses_counts.argtypes = [_P, i, _P]
+    L.cpattn_ulysses_forward.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_last_error.restype = ctypes.c_char_p
     L.cpattn_last_error.argtypes = []
     L.cpattn_version.restype = ctypes.c_char_p
@@ -148,6 +153,29 @@ class Plan:
         return {"full": full, "diag": diag, "skip": skip, "pairs": pairs, "kv_bytes_recv": kvb, "half_units": half}
 
 
+class UlyssesPlan(Plan):
+    """Host-side plan for the head split (cpattn_ulysses_plan): n_cp virtual ranks, each with all
+    T tokens of h / n_cp query heads after an all-to-all."""
+
+    def __init__(self, T: int, h: int, n_kv: int, d_k: int, n_cp: int, causal: bool = True):
+        self.T, self.h, self.n_kv, self.d, self.n_cp = int(T), int(h), int(n_kv), int(d_k), int(n_cp)
+        self.layout, self.causal = CONTIGUOUS, bool(causal)
+        self._h = _P()
+        _check(lib().cpattn_ulysses_plan(self.T, self.h, self.n_kv, self.d, self.n_cp, int(self.causal),
+                                         ctypes.byref(self._h)), "cpattn_ulysses_plan")
+
+    def workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_ulysses_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_ulysses_workspace_size")
+        return out.value
+
+    def counts(self, B: int = 1):
+        import numpy as np
+        recv = np.zeros(self.n_cp, dtype=np.int64)
+        _check(lib().cpattn_ulysses_counts(self._h, B, recv.ctypes.data), "cpattn_ulysses_counts")
+        return {"bytes_recv": recv}
+
+
 # ---- device calls (torch tensors for memory and streams) ------------------------------------
 
 def _torch():
@@ -204,6 +232,27 @@ def forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, 
     _check(lib().cpattn_forward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
                                 _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
                                 _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_forward")
+    return out, lse
+
+
+def ulysses_forward(q, k, v, plan: UlyssesPlan, pos=None, scale: float | None = None, ws=None, out=None, lse=None,
+                    stream=None):
+    """cpattn_ulysses_forward: the head split's all-to-all, per-rank attention and all-to-all
+    back. Arguments and results as forward()."""
+    torch = _torch()
+    if not isinstance(plan, UlyssesPlan):
+        raise ValueError("ulysses_forward needs a UlyssesPlan")
+    B = _check_inputs(plan, q, k, v)
+    if ws is None:
+        ws = alloc_workspace(plan.workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    _check(lib().cpattn_ulysses_forward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                        _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"),
+                                        _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+           "cpattn_ulysses_forward")
     return out, lse
 
 

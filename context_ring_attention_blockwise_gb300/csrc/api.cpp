@@ -43,12 +43,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 Plan* as_plan(cpattn_plan_t p) { return reinterpret_cast<Plan*>(p); }
 
+// A plan made by cpattn_ulysses_plan describes the per-rank problem of the head split and works
+// only with the cpattn_ulysses_* calls; a ring plan does not work with those.
+cpattn_status_t reject_ulysses(const Plan& p) {
+    return p.u_ncp ? fail(CPATTN_ERR_INVALID, "a plan made by cpattn_ulysses_plan works only with the cpattn_ulysses_* calls")
+                   : CPATTN_OK;
+}
+
 float resolve_scale(const Plan& p, float scale) {
     double s = scale > 0.f ? (double)scale : 1.0 / std::sqrt((double)p.d);
     return (float)(s * 1.4426950408889634);   // scores are exponentiated with exp2
 }
 
 cpattn_status_t check_ws(const Plan& p, int B, const void* ws, size_t ws_bytes, bool ring) {
+    if (cpattn_status_t s = reject_ulysses(p)) return s;
     if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
     if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
@@ -109,6 +117,7 @@ cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const voi
 }
 
 cpattn_status_t check_inputs(const Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos) {
+    if (cpattn_status_t s = reject_ulysses(p)) return s;
     if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
     if (!q || !k || !v) return fail(CPATTN_ERR_INVALID, "q, k and v must be non-NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (pos && !aligned16(pos)))
@@ -180,6 +189,7 @@ cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan) {
 cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
     Plan* p = as_plan(plan);
     if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
     *bytes = cpattn::ws_layout(*p, B).fwd_end;
     return CPATTN_OK;
 }
@@ -187,6 +197,7 @@ cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) 
 cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
     Plan* p = as_plan(plan);
     if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
     *bytes = cpattn::ws_layout(*p, B).ring_end;
     return CPATTN_OK;
 }
@@ -194,6 +205,7 @@ cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* by
 cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
     Plan* p = as_plan(plan);
     if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
     *bytes = cpattn::ws_layout(*p, B).bwd_end;
     return CPATTN_OK;
 }
@@ -210,6 +222,7 @@ cpattn_status_t cpattn_plan_counts(cpattn_plan_t plan, int B, int64_t* tiles_ful
                                    int64_t* half_units) {
     Plan* p = as_plan(plan);
     if (!p || B <= 0) return fail(CPATTN_ERR_INVALID, "plan and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
     size_t nn = (size_t)p->n_cp * p->n_cp;
     if (tiles_full) std::memcpy(tiles_full, p->full.data(), nn * sizeof(int64_t));
     if (tiles_diag) std::memcpy(tiles_diag, p->diag.data(), nn * sizeof(int64_t));
@@ -446,6 +459,115 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
     int e = cpattn::launch_finalize(a, stream);
     if (e) return cuda_fail(e, "finalize kernel");
     p->next_step = -1;
+    return CPATTN_OK;
+}
+
+// ---- Ulysses ("Ulysses, splitting by heads instead") ---------------------------------------
+
+cpattn_status_t cpattn_ulysses_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, int causal, cpattn_plan_t* out) {
+    if (!out) return fail(CPATTN_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (d_k != 64 && d_k != 128) return fail(CPATTN_ERR_UNSUPPORTED, "d_k must be 64 or 128");
+    if (n_cp < 1 || h < 1 || n_kv < 1 || T < 1) return fail(CPATTN_ERR_INVALID, "T, h, n_kv and n_cp must be positive");
+    if (h % n_kv) return fail(CPATTN_ERR_INVALID, "h must be a multiple of n_kv");
+    if (h % n_cp) return fail(CPATTN_ERR_INVALID, "Ulysses gives every rank whole heads: h must be a multiple of n_cp");
+    if (n_kv % n_cp && n_cp % n_kv)
+        return fail(CPATTN_ERR_INVALID, "the KV heads split evenly (n_cp divides n_kv) or are replicated evenly (n_kv divides n_cp)");
+    if (T % n_cp) return fail(CPATTN_ERR_INVALID, "T must be a multiple of n_cp (equal token shards)");
+    Plan* p = new Plan();
+    const int hp = h / n_cp, nkvp = n_kv >= n_cp ? n_kv / n_cp : 1;
+    std::string why = cpattn::build_plan(*p, T, hp, nkvp, d_k, 1, CPATTN_CONTIGUOUS, causal);
+    if (!why.empty()) {
+        delete p;
+        return fail(CPATTN_ERR_INVALID, why);
+    }
+    p->u_ncp = n_cp; p->u_h = h; p->u_nkv = n_kv;
+    *out = reinterpret_cast<cpattn_plan_t>(p);
+    return CPATTN_OK;
+}
+
+namespace {
+struct UlyssesWs {
+    size_t inner, qs, ks, vs, os, end;
+};
+UlyssesWs ulysses_ws(const Plan& p, int B) {
+    const size_t bp = (size_t)B * p.u_ncp;
+    auto up = [](size_t x) { return (x + 1023) / 1024 * 1024; };
+    UlyssesWs w{};
+    w.inner = 0;
+    w.qs = up(cpattn::ws_layout(p, (int)bp).fwd_end);
+    const size_t qbytes = bp * (size_t)p.T * p.h * p.d * 2, kvbytes = bp * (size_t)p.T * p.n_kv * p.d * 2;
+    w.ks = up(w.qs + qbytes);
+    w.vs = up(w.ks + kvbytes);
+    w.os = up(w.vs + kvbytes);
+    w.end = up(w.os + qbytes);
+    return w;
+}
+cpattn_status_t need_ulysses(const Plan* p) {
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!p->u_ncp) return fail(CPATTN_ERR_INVALID, "the cpattn_ulysses_* calls need a plan made by cpattn_ulysses_plan");
+    return CPATTN_OK;
+}
+}  // namespace
+
+cpattn_status_t cpattn_ulysses_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (cpattn_status_t s = need_ulysses(p)) return s;
+    if (!bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "bytes and B > 0 required");
+    *bytes = ulysses_ws(*p, B).end;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_ulysses_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv) {
+    Plan* p = as_plan(plan);
+    if (cpattn_status_t s = need_ulysses(p)) return s;
+    if (!bytes_recv || B <= 0) return fail(CPATTN_ERR_INVALID, "bytes_recv and B > 0 required");
+    // Per rank: the other ranks' n tokens of its hp query heads and of its nkvp KV heads (K and V)
+    // in the first all-to-all, and its own n tokens of the other ranks' heads of the output in the
+    // second; 2 bytes a number.
+    const int64_t n = p->T / p->u_ncp, others = p->u_ncp - 1;
+    const int64_t per = (int64_t)B * n * p->d * 2 * others * (2 * (int64_t)p->h + 2 * (int64_t)p->n_kv);
+    for (int r = 0; r < p->u_ncp; ++r) bytes_recv[r] = per;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_ulysses_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                                       cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (cpattn_status_t s = need_ulysses(p)) return s;
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_INVALID, "q, k, v, o and lse must be non-NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || (pos && !aligned16(pos)))
+        return fail(CPATTN_ERR_INVALID, "q, k, v, pos, o and lse must be 16-byte aligned");
+    if ((double)B * (double)p->T * p->u_h > 2.0e9) return fail(CPATTN_ERR_UNSUPPORTED, "B*T*h beyond 2e9 rows");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    const UlyssesWs uw = ulysses_ws(*p, B);
+    if (ws_bytes < uw.end)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(uw.end) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int Bp = B * p->u_ncp;
+    cpattn::UlyssesArgs u{};
+    u.B = B; u.T = p->T; u.h = p->u_h; u.n_kv = p->u_nkv; u.d = p->d; u.n_cp = p->u_ncp; u.hp = p->h; u.nkvp = p->n_kv;
+    u.q = q; u.k = k; u.v = v;
+    u.qs = at<char>(ws, uw.qs); u.ks = at<char>(ws, uw.ks); u.vs = at<char>(ws, uw.vs);
+    u.os = at<char>(ws, uw.os); u.o = o;
+    int e = cpattn::launch_ulysses_split(u, st);                       // first all-to-all
+    if (e) return cuda_fail(e, "Ulysses all-to-all (split)");
+    // every rank's exact attention over all T tokens of its heads: one problem of B n_cp batches;
+    // its lse [B n_cp][hp][T] is the natural lse [B][h][T] already
+    cpattn_status_t s = prologue(*p, Bp, u.qs, u.ks, u.vs, pos, ws, st);
+    if (s) return s;
+    cpattn::AttnLaunch a = attn_args(*p, Bp, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.o = at<char>(ws, uw.os); a.lse = lse;
+    std::string why;
+    e = launch_attn(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    e = cpattn::launch_ulysses_merge(u, st);                           // second all-to-all
+    if (e) return cuda_fail(e, "Ulysses all-to-all (merge)");
     return CPATTN_OK;
 }
 

@@ -69,6 +69,9 @@ struct Plan {
     // page-locked copy of order, order_q, order_kv (created on first use): an upload from
     // pageable memory may block the calling thread until the stream drains
     int32_t* pinned_orders = nullptr;
+    // Ulysses plans (cpattn_ulysses_plan): the attention above is the per-rank problem (T tokens,
+    // h / u_ncp query heads, its KV heads, one rank); these are the outer shape. 0 otherwise.
+    int u_ncp = 0, u_h = 0, u_nkv = 0;
 };
 
 WsLayout ws_layout(const Plan& p, int B);
@@ -113,6 +116,17 @@ int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const 
                  float* lse, void* stream);
 
 int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
+
+// Ulysses all-to-alls: natural q [B][T][h][d], k/v [B][T][n_kv][d] to per-rank head shards
+// qs [B n_cp][T][hp][d], ks/vs [B n_cp][T][nkvp][d] (batch b n_cp + r'), and the output os
+// [B n_cp][T][hp][d] back to natural o [B][T][h][d].
+struct UlyssesArgs {
+    int B; int64_t T; int h, n_kv, d, n_cp, hp, nkvp;
+    const void* q; const void* k; const void* v; void* qs; void* ks; void* vs;
+    const void* os; void* o;
+};
+int launch_ulysses_split(const UlyssesArgs& a, void* stream);
+int launch_ulysses_merge(const UlyssesArgs& a, void* stream);
 
 struct BwdPrepArgs {
     int B; int64_t T, n, m; int h, d, n_cp, layout, n_qt;

@@ -269,6 +269,104 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
+// ---- Ulysses all-to-alls ("Ulysses, splitting by heads instead") --------------------------
+// Virtual rank r' of n_cp holds, after the first all-to-all, every token of its hp = h / n_cp query
+// heads r' hp .. r' hp + hp - 1 and of the nkvp KV heads they use: (r' hp) / g + j' for j' < nkvp,
+// with g = h / n_kv (one KV head shared by n_cp / n_kv ranks when n_cp > n_kv). Its buffers are
+// the batches b' = b n_cp + r' of a natural-order [B n_cp][T][hp or nkvp][d] problem. One
+// natural token row (b, t) per block iteration: the block writes the row's head slices to every
+// rank that holds them.
+__global__ void __launch_bounds__(256, 4) ulysses_split_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k,
+                                                             const uint4* __restrict__ v, uint4* __restrict__ qs,
+                                                             uint4* __restrict__ ks, uint4* __restrict__ vs, int B,
+                                                             int64_t T, int h, int n_kv, int d, int n_cp, int hp,
+                                                             int nkvp) {
+    const int lg = (d == 128) ? 4 : 3;                      // log2 of the 16-byte pieces per head row
+    const int cpr = 1 << lg;
+    const int g = h / n_kv;
+    const int slots_kv = n_cp * nkvp;                       // (rank, KV head of the rank) pairs
+    const int per_row = (h + 2 * slots_kv) * cpr;
+    const int64_t rows = (int64_t)B * T;
+    for (int64_t rw = blockIdx.x; rw < rows; rw += gridDim.x) {
+        const int64_t t = rw % T;
+        const int b = (int)(rw / T);
+        for (int e0 = threadIdx.x; e0 < per_row; e0 += kPermuteUnroll * blockDim.x) {
+            uint4 x[kPermuteUnroll];
+            uint4* dp[kPermuteUnroll];
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u) {
+                const int e = e0 + u * blockDim.x;
+                dp[u] = nullptr;
+                if (e < per_row) {
+                    const int sl = e >> lg, c = e & (cpr - 1);
+                    if (sl < h) {                           // query head sl -> rank sl / hp
+                        const int rr = sl / hp, i = sl - rr * hp;
+                        x[u] = __ldg(q + (rw * h + sl) * cpr + c);
+                        dp[u] = qs + ((((int64_t)b * n_cp + rr) * T + t) * hp + i) * cpr + c;
+                    } else {
+                        const bool is_k = sl < h + slots_kv;
+                        const int s2 = sl - h - (is_k ? 0 : slots_kv);
+                        const int rr = s2 / nkvp, j = s2 - rr * nkvp;
+                        const int kvh = (rr * hp) / g + j;
+                        x[u] = __ldg((is_k ? k : v) + (rw * n_kv + kvh) * cpr + c);
+                        dp[u] = (is_k ? ks : vs) + ((((int64_t)b * n_cp + rr) * T + t) * nkvp + j) * cpr + c;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u)
+                if (dp[u]) *dp[u] = x[u];
+        }
+    }
+}
+
+// The second all-to-all: every rank's output rows back to natural order [B][T][h][d].
+__global__ void __launch_bounds__(256, 4) ulysses_merge_kernel(const uint4* __restrict__ os, uint4* __restrict__ o,
+                                                             int B, int64_t T, int h, int d, int n_cp, int hp) {
+    const int lg = (d == 128) ? 4 : 3;
+    const int cpr = 1 << lg;
+    const int per_row = h * cpr;
+    const int64_t rows = (int64_t)B * T;
+    for (int64_t rw = blockIdx.x; rw < rows; rw += gridDim.x) {
+        const int64_t t = rw % T;
+        const int b = (int)(rw / T);
+        for (int e0 = threadIdx.x; e0 < per_row; e0 += kPermuteUnroll * blockDim.x) {
+            uint4 x[kPermuteUnroll];
+            uint4* dp[kPermuteUnroll];
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u) {
+                const int e = e0 + u * blockDim.x;
+                dp[u] = nullptr;
+                if (e < per_row) {
+                    const int hh = e >> lg, c = e & (cpr - 1);
+                    const int rr = hh / hp, i = hh - rr * hp;
+                    x[u] = __ldg(os + ((((int64_t)b * n_cp + rr) * T + t) * hp + i) * cpr + c);
+                    dp[u] = o + (rw * h + hh) * cpr + c;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPermuteUnroll; ++u)
+                if (dp[u]) *dp[u] = x[u];
+        }
+    }
+}
+
+int launch_ulysses_split(const UlyssesArgs& a, void* stream) {
+    const int64_t rows = (int64_t)a.B * a.T, cap = (int64_t)sm_count() * 4;
+    ulysses_split_kernel<<<(int)(rows < cap ? rows : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(a.q), static_cast<const uint4*>(a.k), static_cast<const uint4*>(a.v),
+        static_cast<uint4*>(a.qs), static_cast<uint4*>(a.ks), static_cast<uint4*>(a.vs), a.B, a.T, a.h, a.n_kv, a.d,
+        a.n_cp, a.hp, a.nkvp);
+    return (int)cudaGetLastError();
+}
+
+int launch_ulysses_merge(const UlyssesArgs& a, void* stream) {
+    const int64_t rows = (int64_t)a.B * a.T, cap = (int64_t)sm_count() * 4;
+    ulysses_merge_kernel<<<(int)(rows < cap ? rows : cap), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(a.os), static_cast<uint4*>(a.o), a.B, a.T, a.h, a.d, a.n_cp, a.hp);
+    return (int)cudaGetLastError();
+}
+
 int launch_permute(const PermuteArgs& a, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int4*>(a.tile_mm), a.lo, a.loL,

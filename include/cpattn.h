@@ -179,6 +179,33 @@ cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q,
                                        const int32_t* lo, float scale, void* dq, void* dk, void* dv, void* ws,
                                        size_t ws_bytes, cpattn_stream_t stream);
 
+/* Ulysses, the head split ([CEX] "Ulysses, splitting by heads instead"), as a comparison
+ * workload on one GPU with n_cp virtual ranks. Rank r starts with the tokens r n .. r n + n - 1
+ * (n = T / n_cp) of every head; a first all-to-all gives every rank all T tokens of its
+ * hp = h / n_cp query heads r hp .. r hp + hp - 1 and of the KV heads they use; each rank runs
+ * exact attention on them; a second all-to-all returns the outputs to the token split. The KV
+ * heads of a rank are (r hp) / g + j for j < n_kv / n_cp (g = h / n_kv). When n_cp > n_kv each
+ * rank holds the one KV head its query heads use, replicated on n_cp / n_kv ranks.
+ *   cpattn_ulysses_plan: h a multiple of n_cp (whole heads per rank); n_cp a divisor or a
+ *   multiple of n_kv; T a multiple of n_cp; d_k 64 or 128; else CPATTN_ERR_INVALID /
+ *   CPATTN_ERR_UNSUPPORTED. The plan works only with the cpattn_ulysses_* calls (the other
+ *   calls return CPATTN_ERR_INVALID for it) and is destroyed by cpattn_plan_destroy.
+ *   cpattn_ulysses_counts: bytes_recv [n_cp] (host, written), the bytes rank r receives in the
+ *   two all-to-alls of one forward pass for B sequences: the other ranks' n tokens of its query
+ *   heads, its KV heads (K and V) and, back, of the other ranks' output heads for its own tokens,
+ *   2 bytes a number: 2 B n d_k (n_cp - 1) (2 hp + 2 nkv_r) with nkv_r its KV heads.
+ *   cpattn_ulysses_forward: arguments, layouts and results as cpattn_forward (natural order,
+ *   device pointers, 16-byte aligned; pos NULL or T int32 positions), the workspace at least
+ *   cpattn_ulysses_workspace_size(plan, B) bytes, 1024-byte aligned. The result equals plain
+ *   attention (head split changes no arithmetic of a head). Asynchronous on `stream`;
+ *   device-side timeouts are read by cpattn_check(plan, ws). */
+cpattn_status_t cpattn_ulysses_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, int causal, cpattn_plan_t* out);
+cpattn_status_t cpattn_ulysses_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+cpattn_status_t cpattn_ulysses_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv);
+cpattn_status_t cpattn_ulysses_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                                       cpattn_stream_t stream);
+
 /* S-way log-sum-exp merge of partial attention results ([CEX] online-softmax paragraph: old
  * totals rescaled to a common maximum). For every row and head:
  *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).

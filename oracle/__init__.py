@@ -296,6 +296,62 @@ class Oracle:
         return int(self.lib.oracle_kv_bytes_recv(B, n, n_kv, d_k, n_cp))
 
 
+    # -- Ulysses, the head split ([CEX] "Ulysses, splitting by heads instead") ------------------
+    @staticmethod
+    def ulysses_heads(h, n_kv, n_cp, r):
+        """Query heads and KV heads rank r holds after the first all-to-all: h / n_cp whole query
+        heads, and the KV heads those use under the GQA map i -> i // (h / n_kv)."""
+        hp = h // n_cp
+        heads = list(range(r * hp, (r + 1) * hp))
+        g = h // n_kv
+        return heads, sorted({i // g for i in heads})
+
+    def ulysses(self, q, k, v, n_cp, causal=True, scale=None, pos=None):
+        """The head split run literally: rank r holds tokens r n .. r n + n - 1 (n = T / n_cp) of
+        every head; the first all-to-all gives each rank all T tokens of its heads; each rank runs
+        the attention definition on them; the second all-to-all returns every rank's outputs to
+        the token split. Data movement only around attention(); returns (o [B,T,h,d], lse [B,h,T])."""
+        B, T, h, d = q.shape
+        n_kv = k.shape[2]
+        if h % n_cp or T % n_cp:
+            raise ValueError("Ulysses needs whole heads and equal token shards per rank")
+        n = T // n_cp
+        q, k, v = (np.ascontiguousarray(x, dtype=np.uint16) for x in (q, k, v))
+        shard = [(q[:, r * n:(r + 1) * n], k[:, r * n:(r + 1) * n], v[:, r * n:(r + 1) * n]) for r in range(n_cp)]
+        o_shard = [np.empty((B, n, h, d)) for _ in range(n_cp)]
+        lse_shard = [np.empty((B, h, n)) for _ in range(n_cp)]
+        for rr in range(n_cp):
+            heads, kvh = self.ulysses_heads(h, n_kv, n_cp, rr)
+            # the rank's local GQA map must be the global one: local head i uses local KV head
+            # i // (len(heads) / len(kvh)) in attention()
+            g_loc = len(heads) // len(kvh)
+            assert all(heads[i] // (h // n_kv) == kvh[i // g_loc] for i in range(len(heads)))
+            qh = np.concatenate([shard[r][0][:, :, heads] for r in range(n_cp)], axis=1)
+            kh = np.concatenate([shard[r][1][:, :, kvh] for r in range(n_cp)], axis=1)
+            vh = np.concatenate([shard[r][2][:, :, kvh] for r in range(n_cp)], axis=1)
+            o_r, lse_r = self.attention(qh, kh, vh, causal=causal, scale=scale, pos=pos)
+            for r in range(n_cp):                        # second all-to-all
+                o_shard[r][:, :, heads] = o_r[:, r * n:(r + 1) * n]
+                lse_shard[r][:, heads] = lse_r[:, :, r * n:(r + 1) * n]
+        return np.concatenate(o_shard, axis=1), np.concatenate(lse_shard, axis=2)
+
+    def ulysses_bytes_recv(self, B, T, h, n_kv, d_k, n_cp) -> np.ndarray:
+        """Bytes each rank receives in the two all-to-alls of one forward pass, counted rank pair
+        by rank pair: from every other rank, its n tokens of the receiver's query heads and KV
+        heads (K and V), and back, the receiver's own n tokens of the sender's output heads;
+        2 bytes a number."""
+        n = T // n_cp
+        out = np.zeros(n_cp, dtype=np.int64)
+        for r in range(n_cp):
+            heads, kvh = self.ulysses_heads(h, n_kv, n_cp, r)
+            for src in range(n_cp):
+                if src == r:
+                    continue
+                src_heads, _ = self.ulysses_heads(h, n_kv, n_cp, src)
+                numbers = n * d_k * (len(heads) + 2 * len(kvh)) + n * d_k * len(src_heads)
+                out[r] += 2 * B * numbers
+        return out
+
 _default = None
 
 

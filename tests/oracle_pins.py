@@ -292,6 +292,41 @@ def pin_ulysses(orc):
     assert orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 2) < orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, 16, 0)
 
 
+def pin_ulysses_split_equals_definition(orc):
+    """The head split run literally (token shards, all-to-all, per-rank attention, all-to-all
+    back) gives plain attention: against the library routine, every head count, KV split or
+    replication, mask and position case."""
+    rng = np.random.default_rng(11)
+    for (h, n_kv) in ((8, 8), (8, 2), (8, 1)):
+        q, k, v = _qkv(40 + h + n_kv, 1, 32, h, n_kv, 16)
+        for n_cp in (1, 2, 4, 8):
+            for causal in (True, False):
+                o, lse = orc.ulysses(q, k, v, n_cp, causal=causal)
+                assert _maxabs(o, _sdpa(q, k, v, causal)) < 1e-12
+                o2, lse2 = orc.attention(q, k, v, causal=causal)
+                assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+        pos = np.sort(rng.integers(0, 64, size=32)).astype(np.int32)
+        o, _ = orc.ulysses(q, k, v, 4, causal=True, pos=pos)
+        mask = torch.from_numpy(pos[None, :] <= pos[:, None])
+        assert _maxabs(o, _sdpa(q, k, v, False, mask=mask)) < 1e-12
+
+
+def pin_ulysses_bytes(orc):
+    """Per-rank all-to-all bytes counted rank pair by rank pair: the pages' closed form when the
+    KV heads split evenly, a hand count when they are replicated, and more bytes than the closed
+    form once replication sets in."""
+    for (B, T, h, n_kv, d_k, n_cp) in ((1, 131072, 64, 8, 128, 8), (2, 4096, 16, 16, 64, 4), (1, 16384, 32, 8, 128, 2)):
+        got = orc.ulysses_bytes_recv(B, T, h, n_kv, d_k, n_cp)
+        closed = B * orc.cp_comm_bytes(T, h * d_k, n_kv * d_k, n_cp, 2)
+        assert np.all(got == got[0]) and got[0] == closed
+    # T = 4, h = 2, n_kv = 1, n_cp = 2, d_k = 1: each rank receives the other rank's 2 tokens of its
+    # query head, of the shared KV head (K and V), and 2 tokens of the other rank's output head:
+    # 8 numbers of 2 bytes
+    assert list(orc.ulysses_bytes_recv(1, 4, 2, 1, 1, 2)) == [16, 16]
+    rep = orc.ulysses_bytes_recv(1, 131072, 64, 8, 128, 16)[0]
+    assert rep > orc.cp_comm_bytes(131072, 64 * 128, 8 * 128, 16, 2)
+
+
 # --------------------------------------------------------------------------------------
 # Gradients: a library's automatic differentiation, finite differences of the forward
 # definition, closed forms, an invariant, and the ring simulation
