@@ -134,3 +134,18 @@ def test_backward_workload_sampled():
     _compare(dq[:, rows], rq, "dq (sampled rows)")
     _compare(dk[:, keys], rk, "dk (last keys)")
     _compare(dv[:, keys], rv, "dv (last keys)")
+
+
+def test_backward_70b_128k_sampled():
+    """The 70B-shaped zigzag T=131072 workload the bench's backward extra times (GQA 8:1, 16
+    ranks): dq of sampled rows, dk/dv of the last 64 keys."""
+    w = synth.workload("llama70b_zigzag_T128k")
+    q, k, v = synth.make_qkv(w)
+    do = synth.normal_bf16(w.seed, 4, (w.B, w.T, w.h, w.d))
+    dq, dk, dv = _run(q, k, v, do, w.n_cp, w.layouts[0], w.causal)
+    rows = synth.sample_rows(w.T, w.n_cp, 24, seed=w.seed)
+    keys = np.arange(w.T - 64, w.T)
+    rq, rk, rv = oracle.get().backward(q, k, v, do, causal=w.causal, rows=rows, keys=keys)
+    _compare(dq[:, rows], rq, "dq (sampled rows)")
+    _compare(dk[:, keys], rk, "dk (last keys)")
+    _compare(dv[:, keys], rv, "dv (last keys)")
