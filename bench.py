@@ -480,7 +480,9 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     out["backward"] = {"ms": ms, "tflops_eff": tf, "frac_of_bf16_sustained": tf / peak,
                        "convention": "2.5 x the forward's effective FLOPs (five GEMMs per visible tile pair); "
                                      "the kernels compute seven (dQ recomputes S and dP)",
-                       "includes": "placement, D = <dO, O> prep, dK/dV kernel, dQ kernel"}
+                       "includes": "placement, D = <dO, O> prep, dK/dV kernel, dQ kernel",
+                       "ring_bytes_recv_per_rank": int(plan.backward_counts(w.B)["bytes_recv"][0]),
+                       "ring_bytes_note": "K and V blocks (bf16) plus the circulating dK and dV blocks (fp32 partial sums)"}
     del wsb, dout, dq, dk, dv
     # the head split (Ulysses) as the comparison workload: all-to-all, per-rank attention over
     # every token of h / n_cp heads, all-to-all back; bytes per rank against the ring's

@@ -28,6 +28,7 @@ SYMBOLS = [
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
     "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked", "cpattn_backward_masked",
     "cpattn_ulysses_plan", "cpattn_ulysses_workspace_size", "cpattn_ulysses_counts", "cpattn_ulysses_forward",
+    "cpattn_backward_counts",
 ]
 
 
@@ -73,6 +74,7 @@ def lib():
                                          ctypes.c_size_t, _P]
     L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_backward_counts.argtypes = [_P, i, _P]
     L.cpattn_ulysses_plan.argtypes = [_I64, i, i, i, i, i, ctypes.POINTER(_P)]
     L.cpattn_ulysses_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_ulysses_counts.argtypes = [_P, i, _P]
@@ -151,6 +153,12 @@ class Plan:
         _check(lib().cpattn_plan_counts(self._h, B, full.ctypes.data, diag.ctypes.data, skip.ctypes.data,
                                         pairs.ctypes.data, kvb.ctypes.data, half.ctypes.data), "cpattn_plan_counts")
         return {"full": full, "diag": diag, "skip": skip, "pairs": pairs, "kv_bytes_recv": kvb, "half_units": half}
+
+    def backward_counts(self, B: int = 1):
+        import numpy as np
+        recv = np.zeros(self.n_cp, dtype=np.int64)
+        _check(lib().cpattn_backward_counts(self._h, B, recv.ctypes.data), "cpattn_backward_counts")
+        return {"bytes_recv": recv}
 
 
 class UlyssesPlan(Plan):

@@ -235,6 +235,18 @@ cpattn_status_t cpattn_plan_counts(cpattn_plan_t plan, int B, int64_t* tiles_ful
     return CPATTN_OK;
 }
 
+cpattn_status_t cpattn_backward_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv) {
+    Plan* p = as_plan(plan);
+    if (!p || B <= 0 || !bytes_recv) return fail(CPATTN_ERR_INVALID, "plan, B > 0 and bytes_recv required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
+    // the other ranks' K and V blocks (bf16), and the circulating dK and dV blocks (fp32 partial
+    // sums), which arrive n_cp times: the last hop returns a rank's own block
+    const int64_t blk = (int64_t)B * p->n * p->n_kv * p->d;
+    for (int r = 0; r < p->n_cp; ++r)
+        bytes_recv[r] = (int64_t)(p->n_cp - 1) * 2 * blk * 2 + (int64_t)p->n_cp * 2 * blk * 4;
+    return CPATTN_OK;
+}
+
 cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                                cpattn_stream_t stream) {

@@ -165,6 +165,13 @@ cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, 
  *   ws / ws_bytes  at least cpattn_backward_workspace_size(plan, B) bytes, 1024-byte aligned.
  * Every pointer non-NULL and 16-byte aligned (pos may be NULL), or CPATTN_ERR_INVALID before any
  * launch. Asynchronous on `stream`; device-side timeouts are read by cpattn_check. */
+/* Bytes each rank receives in one backward pass of the ring ([CEX] "What context parallelism
+ * communicates": the key/value gradients travel back to their owners as a second circulating
+ * block, roughly doubling the traffic): the other n_cp - 1 ranks' K and V blocks in bf16, and the
+ * n_cp arrivals of the circulating dK and dV blocks as fp32 partial sums (the last hop returns a
+ * rank's own block): 4 B n d_kv (n_cp - 1) + 8 B n d_kv n_cp. bytes_recv [n_cp] (host, written).
+ * Host only; the one-GPU backward keeps each block's partial sums in tensor memory. */
+cpattn_status_t cpattn_backward_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv);
 cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
                                 const float* lse, const void* dout, const int32_t* pos, float scale, void* dq, void* dk,

@@ -141,3 +141,15 @@ def test_plan_counts_128k_closed_forms():
     assert np.all(z["full"][:, 1:] == 2 * 32 * 32) and np.all(z["diag"][:, 1:] == 0)
     # striped: only the 64 diagonal tiles of each block are partly visible
     assert np.all(s["diag"] == 64)
+
+
+@pytest.mark.parametrize("shape", [(1, 131072, 64, 8, 128, 16), (2, 32768, 16, 16, 128, 4), (1, 1040, 8, 2, 64, 4)])
+def test_backward_counts_match_oracle(shape):
+    """Bytes each rank receives in the backward ring: the oracle's count with fp32 gradient blocks."""
+    B, T, h, n_kv, d, n_cp = shape
+    plan = cp.Plan(T, h, n_kv, d, n_cp, cp.ZIGZAG if T % (2 * n_cp) == 0 else cp.CONTIGUOUS, True)
+    got = plan.backward_counts(B)["bytes_recv"]
+    want = oracle.get().bwd_bytes_recv(B, T // n_cp, n_kv, d, n_cp, 4)
+    assert np.all(got == want)
+    fwd = plan.counts(B)["kv_bytes_recv"]
+    assert np.all(got > 2 * fwd)
