@@ -9,6 +9,9 @@ read bf16 operands, take D = <dO, O> from the bf16 forward output, and round the
 up to four relative errors of 2^-9 meet in one term, so a term is off by at most ~2^-7 of its
 size. The terms carry both signs and cancel, so the reference scale is the largest gradient
 magnitude of the tensor (b, head slice): |got - exact| <= 2^-6 * max|exact| + 2^-8 * |exact|.
+When the cancellation is total the exact gradient is 0 (one visible key: dS = P (dP - D) with
+D = dP) and what remains is the fp32 rounding difference between the tensor core's dP and the
+prep kernel's D (~1e-7 here): the bound has an absolute floor of 2^-16 for that case.
 """
 import numpy as np
 import pytest
@@ -24,6 +27,7 @@ pytestmark = pytest.mark.gpu
 
 ATOL_FRAC = 2.0 ** -6
 RTOL = 2.0 ** -8
+FLOOR = 2.0 ** -16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -56,7 +60,7 @@ def _run(q, k, v, do, n_cp, layout, causal, pos=None, scale=None):
 
 
 def _compare(got, exact, what):
-    """Per (b, head) slice: |got - exact| <= ATOL_FRAC * max|exact| + RTOL * |exact|."""
+    """Per (b, head) slice: |got - exact| <= ATOL_FRAC * max|exact| + RTOL * |exact| + FLOOR."""
     assert got.shape == exact.shape
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     B, T, H, d = exact.shape
@@ -67,7 +71,7 @@ def _compare(got, exact, what):
             g = got[b, :, hh]
             scale = float(np.max(np.abs(e))) if e.size else 0.0
             err = np.abs(g - e)
-            bound = ATOL_FRAC * scale + RTOL * np.abs(e)
+            bound = ATOL_FRAC * scale + RTOL * np.abs(e) + FLOOR
             ratio = float(np.max(err / np.maximum(bound, 1e-30))) if e.size else 0.0
             worst = max(worst, ratio)
             if ratio > 1.0:
