@@ -146,3 +146,20 @@ def test_document_mask_backward_lower_bound_zero_is_plain():
     b = cp.backward(qd, kd, vd, o, lse, dod, plan)
     for x, y in zip(a, b):
         assert np.array_equal(x, y.float().cpu().numpy())
+
+
+def test_document_mask_backward_gqa_16k_sampled():
+    """The GQA 4:1 zigzag T=16384 shape with packed documents of 256..4096 tokens: dq of sampled
+    rows, dk/dv of sampled keys (each sees only the queries of its own document)."""
+    from tests.test_gpu_backward import _compare
+    w = synth.workload("gqa_zigzag_T16k")
+    q, k, v = synth.make_qkv(w)
+    do = synth.normal_bf16(w.seed, 4, (w.B, w.T, w.h, w.d))
+    doc, lo = packed_documents(w.T, seed=9, min_len=256, max_len=4096)
+    dq, dk, dv = _masked_backward(q, k, v, do, lo, w.n_cp, w.layouts[0])
+    rows = synth.sample_rows(w.T, w.n_cp, 32, seed=w.seed)
+    keys = np.sort(np.random.default_rng(11).choice(w.T, size=64, replace=False))
+    rq, rk, rv = oracle.get().backward(q, k, v, do, causal=True, doc=doc, rows=rows, keys=keys)
+    _compare(dq[:, rows], rq, "dq (sampled rows)")
+    _compare(dk[:, keys], rk, "dk (sampled keys)")
+    _compare(dv[:, keys], rv, "dv (sampled keys)")
