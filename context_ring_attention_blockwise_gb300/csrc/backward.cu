@@ -392,7 +392,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             for (int s = 0; s < P.n_cp && ok; ++s) {
                 const int r = (src + s) % P.n_cp;         // the block's gradient is at rank src + s at step s
-                for (int qt = 0; qt < P.n_qt && ok; ++qt) {
+                // Causal: the query tiles whose positions all precede the key tile's first one see
+                // none of it, and they are the tiles before the first whose running maximum (.w,
+                // non-decreasing) reaches it: start there (binary search, exact for any positions).
+                int qt0 = 0;
+                if (P.causal) {
+                    int lo = 0, hi = P.n_qt;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (__ldg(P.tile_mm + r * P.n_qt + mid).w < kmm.x) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    qt0 = lo;
+                }
+                for (int qt = qt0; qt < P.n_qt && ok; ++qt) {
                     const int4 qmm = __ldg(P.tile_mm + r * P.n_qt + qt);
                     const int cls = tile_class(P.causal, qmm, tile_bound<LB>(P, r, qt), kmm);
                     if (cls == CPATTN_TILE_SKIP) continue;
@@ -741,6 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int srcr = (r - s + P.n_cp) % P.n_cp;     // the block rank r holds at step s
                 for (int ktt = 0; ktt < P.n_qt && ok; ++ktt) {
                     const int4 kmm = __ldg(P.tile_mm + srcr * P.n_qt + ktt);
+                    // causal: this key tile and every later one of the block start after every
+                    // query (suffix minimum .z): none of the rest is visible
+                    if (P.causal && kmm.z > qmm.y) break;
                     const int cls = tile_class(P.causal, qmm, qlb, kmm);
                     if (cls == CPATTN_TILE_SKIP) continue;
                     const int qshort = (qt == P.n_qt - 1) && (P.n % 128) != 0;
