@@ -133,6 +133,8 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt; a.pair_heads = p.pair_heads; a.n_grp = p.n_grp;
     a.sched = at<uint32_t>(ws, w.sched);
     a.unit_tiles = at<int32_t>(ws, w.unit_tiles);
+    a.walk_tab = at<int32_t>(ws, w.walk_tab);
+    a.walk_nz = at<unsigned long long>(ws, w.walk_nz);
     a.scale_log2 = resolve_scale(p, scale);
     a.qL = at<char>(ws, w.qL);
     a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);
@@ -351,6 +353,7 @@ cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, 
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     if (!p->causal) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query needs a causal plan");
+    if (p->n_qt > 65535) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query supports up to 65535 tiles per rank");
     if (!lo || !aligned16(lo)) return fail(CPATTN_ERR_INVALID, "lo must be non-NULL and 16-byte aligned");
     cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
     if (s) return s;

@@ -67,6 +67,10 @@ struct Params {
     const int32_t* loL;    // [n_cp][n] lowest visible key position per query, or NULL
     const int4* tile_lo;   // [n_cp][n_qt] (min, max) of loL over a query tile, or NULL
     int32_t* unit_tiles;   // [n_cp * n_grp]: key tiles of a unit of row group r * n_grp + group
+    // document masks only, written by unit_tiles_kernel: per row group and ring step, the key
+    // tiles its walk visits lie in [begin, end) (begin | end << 16), and a bit per non-empty step
+    int32_t* walk_tab;               // [n_cp * n_grp][n_cp]
+    unsigned long long* walk_nz;     // [n_cp * n_grp], for n_cp <= 64
     unsigned long long* counts;
     uint32_t* sched;
     uint16_t* o;
@@ -251,8 +255,55 @@ struct TileWalk {
         s = P.fused ? 0 : P.step;
         s_end = P.fused ? P.n_cp : P.step + 1;
         kt = -1;
+        rg = U.rg;
+        if (LB && P.causal) {
+            // the table walk starts before its first step: kt >= kend moves to the next one
+            s -= 1;
+            kt = kend = 0;
+            nz = P.n_cp <= 64 ? __ldg(P.walk_nz + rg) : 0ull;
+            if (!P.fused && P.n_cp <= 64) nz &= 1ull << P.step;   // one step: only its own bit
+        }
     }
+    // Document masks: the walk of a row group is the same for all its units, and the kernel
+    // before this one recorded it per step as a key-tile range (next_scan below): jump from one
+    // non-empty step to the next with one table load, instead of a chain of dependent loads
+    // (a running-maximum test and a binary search) per step.
+    int rg, kend;
+    unsigned long long nz;
     __device__ bool next() {
+        if (!LB || !p->causal) return next_scan();
+        const Params& P = *p;
+        for (;;) {
+            if (++kt >= kend) {
+                int sn = s + 1;
+                if (P.n_cp <= 64) {
+                    const unsigned long long rest = sn < 64 ? (nz >> sn) : 0ull;
+                    if (rest == 0ull) return false;
+                    sn += __ffsll((long long)rest) - 1;
+                }
+                if (sn >= s_end) return false;
+                s = sn;
+                const int e = __ldg(P.walk_tab + (int64_t)rg * P.n_cp + s);
+                kt = e & 0xFFFF;
+                kend = e >> 16;
+                if (kt >= kend) { kt = kend; continue; }   // (n_cp > 64: empty steps are visited)
+                src = r - s;
+                if (src < 0) src += P.n_cp;
+            }
+            const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
+            const int4 t4 = __ldg(P.tile_mm + src * P.n_qt + kt);
+            cls0 = (t4.x > qmax0 || t4.y < lmin0) ? CPATTN_TILE_SKIP
+                   : (t4.y > qmin0 || t4.x < lmax0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            cls1 = (t4.x > qmax1 || t4.y < lmin1) ? CPATTN_TILE_SKIP
+                   : (t4.y > qmin1 || t4.x < lmax1) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+            if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
+            mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
+            mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
+            return true;
+        }
+    }
+    // The walk from the position tables alone (every step, every layout and mask).
+    __device__ bool next_scan() {
         const Params& P = *p;
         for (;;) {
             if (++kt >= P.n_qt) {
@@ -799,8 +850,33 @@ __global__ void unit_tiles_kernel(const Params P) {
     U.head[0] = U.head[1] = 0;
     TileWalk<LB> w;
     w.init(P, U);
+    if (LB && P.causal) {                 // the scan, as the table walk will replay it
+        w.s = P.fused ? 0 : P.step;
+        w.kt = -1;
+    }
     int c = 0;
-    while (w.next()) ++c;
+    int cur = -1, first = 0, last = 0;
+    unsigned long long nz = 0ull;
+    while (w.next_scan()) {
+        ++c;
+        if (LB && P.causal) {
+            if (w.s != cur) {
+                if (cur >= 0) P.walk_tab[(int64_t)rg * P.n_cp + cur] = first | ((last + 1) << 16);
+                for (int t = cur + 1; t < w.s; ++t) P.walk_tab[(int64_t)rg * P.n_cp + t] = 0;
+                cur = w.s;
+                first = w.kt;
+                if (cur < 64) nz |= 1ull << cur;
+            }
+            last = w.kt;
+        }
+    }
+    if (LB && P.causal) {
+        if (cur >= 0) P.walk_tab[(int64_t)rg * P.n_cp + cur] = first | ((last + 1) << 16);
+        for (int t = cur + 1; t < P.n_cp; ++t) P.walk_tab[(int64_t)rg * P.n_cp + t] = 0;
+        if (cur < 0)
+            for (int t = 0; t < P.n_cp; ++t) P.walk_tab[(int64_t)rg * P.n_cp + t] = 0;
+        P.walk_nz[rg] = nz;
+    }
     P.unit_tiles[rg] = c;
 }
 
@@ -842,6 +918,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm); P.order = a.order;
     P.unit_tiles = a.unit_tiles;
+    P.walk_tab = a.walk_tab;
+    P.walk_nz = a.walk_nz;
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;

@@ -34,6 +34,8 @@ struct WsLayout {
     size_t tile_lo = 0;     // int32x4 [n_cp][n_qt]: min and max of loL over each query tile
     size_t unit_tiles = 0;  // int32 [n_cp * n_qt]: key tiles a unit of row group (r, group) visits in
                             // the current launch (written by the attention launch itself)
+    size_t walk_tab = 0;    // int32 [n_cp * n_qt][n_cp]: document masks: visited key-tile range per row group and step
+    size_t walk_nz = 0;     // uint64 [n_cp * n_qt]: document masks: the steps with visited tiles
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
@@ -91,6 +93,8 @@ struct AttnLaunch {
     int B; int64_t T, n, m; int h, n_kv, d, n_cp, layout, causal, n_qt, pair_heads, n_grp;
     uint32_t* sched;  // work counter of this launch (zeroed before the launch)
     int32_t* unit_tiles;  // [n_cp * n_grp] scratch: key tiles per row group for this launch
+    int32_t* walk_tab;    // [n_cp * n_grp][n_cp] scratch (document masks)
+    unsigned long long* walk_nz;  // [n_cp * n_grp] scratch (document masks)
     float scale_log2;
     int fused;        // 1: all ring steps, natural-order bf16 output; 0: one step, merge into running state
     int step;         // ring step (fused == 0)

@@ -38,6 +38,8 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.loL = take(sizeof(int32_t) * T);
     w.tile_lo = take(sizeof(int32_t) * 4 * (size_t)p.n_cp * p.n_qt);
     w.unit_tiles = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
+    w.walk_tab = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt * p.n_cp);
+    w.walk_nz = take(sizeof(uint64_t) * (size_t)p.n_cp * p.n_qt);
     w.qL = take(2 * (size_t)B * T * p.h * d);
     w.kL = take(2 * (size_t)B * T * p.n_kv * d);
     w.vL = take(2 * (size_t)B * T * p.n_kv * d);
