@@ -166,6 +166,34 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name (x86: "model name"; Arm: implementer and part numbers)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = (x.strip() for x in line.split(":", 1))
+                    fields.setdefault(key, val)
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU implementer" in fields:
+        return f"{platform.machine()} implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    return platform.machine()
+
+
+def cpu_baseline_entry(w, rate: float, seconds: float, sample: str) -> dict:
+    """The oracle's rate with its per-core figure and the full workload's time extrapolated
+    linearly in visible pairs (the oracle's cost per pair does not depend on the row)."""
+    cores = host_cores()
+    return {"value": rate, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "seconds": seconds, "per_core_gflops": rate * 1e3 / cores, "cpu": host_cpu_model(),
+            "full_workload_s_extrapolated": flops_eff(w) / (rate * 1e12) if rate > 0 else None}
+
+
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -187,8 +215,8 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-                         "sample": f"per step: {rows_per_step} query rows x {w.h} heads of the workload"},
+        "cpu_baseline": cpu_baseline_entry(w, value, float(np.sum(times)),
+                                           f"per step: {rows_per_step} query rows x {w.h} heads of the workload"),
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -377,8 +405,7 @@ def run_gpu(args, w):
         result["extras"] = extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks)
     if rank == 0 and args.cpu_baseline:
         rate, dt, desc = oracle_sample_rate(w, q_h, k_h, v_h, args.cpu_rows, seed=7)
-        result["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-                                  "sample": desc, "seconds": dt}
+        result["cpu_baseline"] = cpu_baseline_entry(w, rate, dt, desc)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if dist is not None:
@@ -422,6 +449,25 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     ms = a.elapsed_time(b) / 5
     mb = op.numel() * 4 + lp.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
     out["merge_S2"] = {"ms": ms, "gbs": mb / ms / 1e6, "frac_of_hbm": mb / ms / 1e6 / hbm}
+    del op, lp, mo, ml
+    # the n_cp-way merge at the GQA 16K shape (8 partials of [16384, 32, 128]): one partial per
+    # virtual rank's view of a row, the most partials the ring-step path combines
+    ws16 = synth.workload("gqa_zigzag_T16k")
+    S, rows = ws16.n_cp, ws16.B * ws16.T
+    op = torch.randn((S, rows, ws16.h, ws16.d), dtype=torch.float32, device=dev)
+    lp = torch.randn((S, ws16.h, rows), dtype=torch.float32, device=dev)
+    mo = torch.empty((rows, ws16.h, ws16.d), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((ws16.h, rows), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        cp.merge(op, lp, mo, ml, stream=stream)
+    a.record(stream)
+    for _ in range(5):
+        cp.merge(op, lp, mo, ml, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / 5
+    mb = op.numel() * 4 + lp.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
+    out[f"merge_S{S}_{ws16.name}"] = {"ms": ms, "gbs": mb / ms / 1e6, "frac_of_hbm": mb / ms / 1e6 / hbm}
     del op, lp, mo, ml
     # the ring-faithful path: permute, n_cp steps with block hops on a copy stream, finalize
     wsr = cp.alloc_workspace(plan.ring_workspace_size(w.B), dev)
