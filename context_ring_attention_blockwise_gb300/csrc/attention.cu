@@ -370,12 +370,15 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
     using C = Cfg<D>;
     int nk = 0, nv = 0, nq = 0;   // K tiles, V tiles, Q pairs issued by this CTA
     bool ok = true;
+    // Q tiles are read once per unit; the K/V tiles of one KV head are re-read by every unit in
+    // flight, so they are the lines L2 should keep.
+    const uint64_t pol_q = l2_evict_first(), pol_kv = l2_evict_last();
     auto load_v = [&](int row) -> bool {
         const int st = nv % C::NS;
         if (nv >= C::NS && !wait(bars.v_empty(st), ((nv / C::NS) - 1) & 1, kSiteVEmpty)) return false;
         mbar_arrive_expect_tx(bars.v_full(st), C::KV_BYTES);
         for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_2d(sV + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmV, bars.v_full(st), pn * 64, row);
+            tma_load_2d_hint(sV + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmV, bars.v_full(st), pn * 64, row, pol_kv);
         ++nv;
         return true;
     };
@@ -399,7 +402,8 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
                 for (int i = 0; i < 2; ++i) {
                     const int qrow = (int)((((int64_t)U.r * P.B + U.b) * P.h + U.head[i]) * P.n + (int64_t)U.qt[i] * 128);
                     for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_2d(sQ + i * C::Q_BYTES + pn * C::PANEL_BYTES, tmQ, bars.q_full(), pn * 64, qrow);
+                        tma_load_2d_hint(sQ + i * C::Q_BYTES + pn * C::PANEL_BYTES, tmQ, bars.q_full(), pn * 64, qrow,
+                                         pol_q);
                 }
                 ++nq;
             }
@@ -407,7 +411,7 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
             if (nk >= C::NS && !wait(bars.k_empty(st), ((nk / C::NS) - 1) & 1, kSiteKEmpty)) { ok = false; break; }
             mbar_arrive_expect_tx(bars.k_full(st), C::KV_BYTES);
             for (int pn = 0; pn < C::PANELS; ++pn)
-                tma_load_2d(sK + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmK, bars.k_full(st), pn * 64, krow);
+                tma_load_2d_hint(sK + st * C::KV_BYTES + pn * C::PANEL_BYTES, tmK, bars.k_full(st), pn * 64, krow, pol_kv);
             ++nk;
             if (j >= 1 && !load_v(prev_row)) { ok = false; break; }     // V runs one tile behind K
             prev_row = krow;
@@ -528,6 +532,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_col = wg ? C::S_COL1 : C::S_COL0, o_col = wg ? C::O_COL1 : C::O_COL0;
     const uint64_t scale2 = f2_pack(P.scale_log2, P.scale_log2);
+    const uint64_t pol_o = l2_evict_first();          // O rows are written once: keep K/V in L2 instead
     int ntile = 0;   // tiles processed by this warpgroup
     bool ok = true;
     for (int it = 0; ok; ++it) {
@@ -729,7 +734,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                     v.y = pack_bf16(__uint_as_float(ot[8 * q4 + 2]) * inv_l, __uint_as_float(ot[8 * q4 + 3]) * inv_l);
                     v.z = pack_bf16(__uint_as_float(ot[8 * q4 + 4]) * inv_l, __uint_as_float(ot[8 * q4 + 5]) * inv_l);
                     v.w = pack_bf16(__uint_as_float(ot[8 * q4 + 6]) * inv_l, __uint_as_float(ot[8 * q4 + 7]) * inv_l);
-                    dst[c * 4 + q4] = v;
+                    st_global_v4_hint(dst + c * 4 + q4, v, pol_o);
                 }
             } else if (orun) {
 #pragma unroll
