@@ -529,7 +529,24 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
                        "includes": "placement, D = <dO, O> prep, dK/dV kernel, dQ kernel",
                        "ring_bytes_recv_per_rank": int(plan.backward_counts(w.B)["bytes_recv"][0]),
                        "ring_bytes_note": "K and V blocks (bf16) plus the circulating dK and dV blocks (fp32 partial sums)"}
-    del wsb, dout, dq, dk, dv
+    del wsb
+    # the backward as ring steps: each step's kernels on the compute stream; K/V and the fp32
+    # dK/dV partial sums hop between the ranks' slots on the copy stream
+    wsr = cp.alloc_workspace(plan.backward_ring_workspace_size(w.B), dev)
+    cp.ring_backward(q, k, v, o, lse, dout, plan, ws=wsr, dq=dq, dk=dk, dv=dv, stream=stream, copy_stream=copy)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(2):
+        cp.ring_backward(q, k, v, o, lse, dout, plan, ws=wsr, dq=dq, dk=dk, dv=dv, stream=stream, copy_stream=copy)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsr)
+    ms = a.elapsed_time(b) / 2
+    tf = 2.5 * flops_eff(w) / (ms * 1e-3) / 1e12
+    out["backward_ring_step_path"] = {"ms": ms, "tflops_eff": tf, "frac_of_bf16_sustained": tf / peak,
+                                      "includes": "placement and prep, n_cp steps of the dK/dV and dQ kernels with "
+                                                  "the K/V and gradient hops and the gradient adds, finalize"}
+    del wsr, dout, dq, dk, dv
     # the head split (Ulysses) as the comparison workload: all-to-all, per-rank attention over
     # every token of h / n_cp heads, all-to-all back; bytes per rank against the ring's
     up = cp.UlyssesPlan(w.T, w.h, w.n_kv, w.d, w.n_cp, w.causal)

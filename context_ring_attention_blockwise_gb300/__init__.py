@@ -28,7 +28,8 @@ SYMBOLS = [
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
     "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked", "cpattn_backward_masked",
     "cpattn_ulysses_plan", "cpattn_ulysses_workspace_size", "cpattn_ulysses_counts", "cpattn_ulysses_forward",
-    "cpattn_backward_counts",
+    "cpattn_backward_counts", "cpattn_backward_ring_workspace_size", "cpattn_backward_begin",
+    "cpattn_backward_ring_step", "cpattn_backward_finalize",
 ]
 
 
@@ -75,6 +76,10 @@ def lib():
     L.cpattn_backward_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_backward.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_backward_counts.argtypes = [_P, i, _P]
+    L.cpattn_backward_ring_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_backward_begin.argtypes = [_P, i, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_backward_ring_step.argtypes = [_P, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, _P]
+    L.cpattn_backward_finalize.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_ulysses_plan.argtypes = [_I64, i, i, i, i, i, ctypes.POINTER(_P)]
     L.cpattn_ulysses_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_ulysses_counts.argtypes = [_P, i, _P]
@@ -137,6 +142,12 @@ class Plan:
     def backward_workspace_size(self, B: int) -> int:
         out = ctypes.c_size_t()
         _check(lib().cpattn_backward_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_backward_workspace_size")
+        return out.value
+
+    def backward_ring_workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_backward_ring_workspace_size(self._h, B, ctypes.byref(out)),
+               "cpattn_backward_ring_workspace_size")
         return out.value
 
     def tile_shape(self):
@@ -296,6 +307,52 @@ def backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = 
                                  _dev_ptr(lse, "lse"), _dev_ptr(dout, "dout"), _dev_ptr(pos, "pos"), float(scale or 0.0),
                                  _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"), _dev_ptr(ws, "ws"),
                                  ws.numel(), _stream_ptr(stream)), "cpattn_backward")
+    return dq, dk, dv
+
+
+def backward_begin(q, k, v, o, lse, dout, plan: Plan, ws, pos=None, stream=None):
+    """cpattn_backward_begin: placement and the backward's side data, before the ring steps."""
+    B = _check_inputs(plan, q, k, v)
+    _check(lib().cpattn_backward_begin(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                       _dev_ptr(o, "o"), _dev_ptr(lse, "lse"), _dev_ptr(dout, "dout"),
+                                       _dev_ptr(pos, "pos"), _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+           "cpattn_backward_begin")
+
+
+def backward_ring_step(plan: Plan, B: int, step: int, ws, scale: float | None = None, compute=None, copy=None):
+    _check(lib().cpattn_backward_ring_step(plan.handle, B, step, float(scale or 0.0), _dev_ptr(ws, "ws"), ws.numel(),
+                                           _stream_ptr(compute), _stream_ptr(copy)), "cpattn_backward_ring_step")
+
+
+def backward_finalize(plan: Plan, B: int, ws, dq, dk, dv, stream=None):
+    _check(lib().cpattn_backward_finalize(plan.handle, B, _dev_ptr(dq, "dq"), _dev_ptr(dk, "dk"), _dev_ptr(dv, "dv"),
+                                          _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+           "cpattn_backward_finalize")
+
+
+def ring_backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | None = None, ws=None, dq=None,
+                  dk=None, dv=None, stream=None, copy_stream=None):
+    """The backward as ring steps: begin, n_cp steps (K/V and the circulating fp32 dK/dV partial
+    sums hop on a copy stream; the last hop returns each block's gradient to its owner), finalize.
+    Same arguments and results as backward()."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    for t, name in ((o, "o"), (dout, "dout")):
+        if tuple(t.shape) != tuple(q.shape) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if tuple(lse.shape) != (B, plan.h, plan.T) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, h, T]")
+    if ws is None:
+        ws = alloc_workspace(plan.backward_ring_workspace_size(B), q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    compute = stream if stream is not None else torch.cuda.current_stream()
+    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device)
+    backward_begin(q, k, v, o, lse, dout, plan, ws, pos=pos, stream=compute)
+    for s in range(plan.n_cp):
+        backward_ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
+    backward_finalize(plan, B, ws, dq, dk, dv, stream=compute)
     return dq, dk, dv
 
 

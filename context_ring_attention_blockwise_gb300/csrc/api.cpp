@@ -183,6 +183,13 @@ cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan) {
         if (p->ev_copy[i]) cudaEventDestroy(p->ev_copy[i]);
     }
     if (p->ev_start) cudaEventDestroy(p->ev_start);
+    for (int i = 0; i < 2; ++i) {
+        if (p->bev_kv[i]) cudaEventDestroy(p->bev_kv[i]);
+        if (p->bev_used[i]) cudaEventDestroy(p->bev_used[i]);
+        if (p->bev_circ[i]) cudaEventDestroy(p->bev_circ[i]);
+    }
+    if (p->bev_ready) cudaEventDestroy(p->bev_ready);
+    if (p->bev_start) cudaEventDestroy(p->bev_start);
     if (p->pinned_orders) cudaFreeHost(p->pinned_orders);
     delete p;
     return CPATTN_OK;
@@ -209,6 +216,14 @@ cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t
     if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
     if (cpattn_status_t s = reject_ulysses(*p)) return s;
     *bytes = cpattn::ws_layout(*p, B).bwd_end;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_backward_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
+    *bytes = cpattn::ws_layout(*p, B).bring_end;
     return CPATTN_OK;
 }
 
@@ -270,61 +285,83 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
 }
 
 namespace {
-cpattn_status_t backward_impl(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
-                              const float* lse, const void* dout, const int32_t* pos, const int32_t* lo, float scale,
-                              void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
-    Plan* p = as_plan(plan);
-    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
-    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
-    if (s) return s;
-    if (!o || !lse || !dout || !dq || !dk || !dv)
-        return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be non-NULL");
-    if (!aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-        return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be 16-byte aligned");
-    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
-    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
-    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
-    if (ws_bytes < w.bwd_end)
-        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(w.bwd_end) + " bytes, got " +
-                                              std::to_string(ws_bytes));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((s = prologue(*p, B, q, k, v, pos, ws, st, lo))) return s;
-    cpattn::BwdPrepArgs pa{};
-    pa.B = B; pa.T = p->T; pa.n = p->n; pa.m = p->m; pa.h = p->h; pa.d = p->d; pa.n_cp = p->n_cp;
-    pa.layout = p->layout; pa.n_qt = p->n_qt;
-    pa.o = o; pa.dout = dout; pa.lse = lse;
-    pa.doL = at<char>(ws, w.doL); pa.nlse2L = at<float>(ws, w.lse2); pa.nDL = at<float>(ws, w.Dl);
-    int e = 0;
-    if (p->n % 128 != 0) {
-        // the padding after a short last tile must hold finite values: zero both side tables
-        const size_t padded = sizeof(float) * (size_t)p->n_cp * B * p->h * (size_t)p->n_qt * 128;
-        e = cudaMemsetAsync(at<char>(ws, w.lse2), 0, padded, st);
-        if (!e) e = cudaMemsetAsync(at<char>(ws, w.Dl), 0, padded, st);
-        if (e) return cuda_fail(e, "cudaMemsetAsync(backward side tables)");
-    }
-    e = cpattn::launch_bwd_prep(pa, st);
-    if (e) return cuda_fail(e, "backward prep kernel");
-    const size_t nu = (size_t)p->n_cp * p->n_qt;
-    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), order_src(*p, 1), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
-    if (!e)
-        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, order_src(*p, 2), sizeof(int32_t) * nu,
-                            cudaMemcpyHostToDevice, st);
-    if (e) return cuda_fail(e, "cudaMemcpyAsync(backward order)");
+// The backward's launch arguments: every pointer into the workspace, the rest from the plan.
+cpattn::BwdLaunch bwd_args(const Plan& p, int B, float scale, void* ws, const int32_t* lo) {
+    cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    const size_t nu = (size_t)p.n_cp * p.n_qt;
     cpattn::BwdLaunch a{};
-    a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.n_kv = p->n_kv; a.d = p->d; a.n_cp = p->n_cp;
-    a.layout = p->layout; a.causal = p->causal; a.n_qt = p->n_qt;
-    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)p->d));
+    a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
+    a.layout = p.layout; a.causal = p.causal; a.n_qt = p.n_qt;
+    a.scale = scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)p.d));
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL); a.doL = at<char>(ws, w.doL);
     a.nlse2L = at<float>(ws, w.lse2); a.nDL = at<float>(ws, w.Dl);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
     a.order_q = at<int32_t>(ws, w.bwd_order); a.order_kv = a.order_q + nu;
     a.loL = lo ? at<int32_t>(ws, w.loL) : nullptr;
     a.tile_lo = lo ? at<int32_t>(ws, w.tile_lo) : nullptr;
-    a.dq = dq; a.dk = dk; a.dv = dv;
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
+    return a;
+}
+
+// Checks, token placement, and the backward's side data in layout order (dO, -lse log2 e, -D)
+// and unit orders: everything before the tcgen05 kernels. `need` is the workspace end required.
+cpattn_status_t backward_prepare(Plan& p, int B, const void* q, const void* k, const void* v, const void* o,
+                                 const float* lse, const void* dout, const int32_t* pos, const int32_t* lo, void* ws,
+                                 size_t ws_bytes, size_t need, cudaStream_t st) {
+    cpattn_status_t s = check_inputs(p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !dout) return fail(CPATTN_ERR_INVALID, "o, lse and dout must be non-NULL");
+    if (!aligned16(o) || !aligned16(lse) || !aligned16(dout))
+        return fail(CPATTN_ERR_INVALID, "o, lse and dout must be 16-byte aligned");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    if (ws_bytes < need)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    if ((s = prologue(p, B, q, k, v, pos, ws, st, lo))) return s;
+    cpattn::BwdPrepArgs pa{};
+    pa.B = B; pa.T = p.T; pa.n = p.n; pa.m = p.m; pa.h = p.h; pa.d = p.d; pa.n_cp = p.n_cp;
+    pa.layout = p.layout; pa.n_qt = p.n_qt;
+    pa.o = o; pa.dout = dout; pa.lse = lse;
+    pa.doL = at<char>(ws, w.doL); pa.nlse2L = at<float>(ws, w.lse2); pa.nDL = at<float>(ws, w.Dl);
+    int e = 0;
+    if (p.n % 128 != 0) {
+        // the padding after a short last tile must hold finite values: zero both side tables
+        const size_t padded = sizeof(float) * (size_t)p.n_cp * B * p.h * (size_t)p.n_qt * 128;
+        e = cudaMemsetAsync(at<char>(ws, w.lse2), 0, padded, st);
+        if (!e) e = cudaMemsetAsync(at<char>(ws, w.Dl), 0, padded, st);
+        if (e) return cuda_fail(e, "cudaMemsetAsync(backward side tables)");
+    }
+    e = cpattn::launch_bwd_prep(pa, st);
+    if (e) return cuda_fail(e, "backward prep kernel");
+    const size_t nu = (size_t)p.n_cp * p.n_qt;
+    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), order_src(p, 1), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
+    if (!e)
+        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, order_src(p, 2), sizeof(int32_t) * nu,
+                            cudaMemcpyHostToDevice, st);
+    if (e) return cuda_fail(e, "cudaMemcpyAsync(backward order)");
+    return CPATTN_OK;
+}
+
+cpattn_status_t backward_impl(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, const int32_t* pos, const int32_t* lo, float scale,
+                              void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!dq || !dk || !dv) return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be non-NULL");
+    if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(CPATTN_ERR_INVALID, "o, lse, dout, dq, dk and dv must be 16-byte aligned");
+    if (cpattn_status_t s0 = reject_ulysses(*p)) return s0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cpattn_status_t s = backward_prepare(*p, B, q, k, v, o, lse, dout, pos, lo, ws, ws_bytes,
+                                         B > 0 ? cpattn::ws_layout(*p, B).bwd_end : 0, st);
+    if (s) return s;
+    cpattn::BwdLaunch a = bwd_args(*p, B, scale, ws, lo);
+    a.dq = dq; a.dk = dk; a.dv = dv;
     std::string why;
-    e = cpattn::launch_backward(a, st, &why);
+    int e = cpattn::launch_backward(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
@@ -474,6 +511,145 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
     int e = cpattn::launch_finalize(a, stream);
     if (e) return cuda_fail(e, "finalize kernel");
     p->next_step = -1;
+    return CPATTN_OK;
+}
+
+// ---- the backward as ring steps ("What context parallelism communicates": each rank keeps the
+// gradient of its own queries; the key/value gradient of a block travels with the block as a
+// second circulating block and returns to its owner) -------------------------------------------
+
+namespace {
+
+// Send right, receive left between two rank-major slot arrays: slot `dst` of rank r <- the
+// block of rank r - 1 in `src` (two contiguous copies per array).
+int ring_hop(const char* src, char* dst, size_t blk, int n_cp, cudaStream_t st) {
+    const size_t all = blk * (size_t)n_cp;
+    int e = 0;
+    if (n_cp > 1) e = cudaMemcpyAsync(dst + blk, src, all - blk, cudaMemcpyDeviceToDevice, st);
+    if (!e) e = cudaMemcpyAsync(dst, src + all - blk, blk, cudaMemcpyDeviceToDevice, st);
+    return e;
+}
+
+cpattn_status_t check_bring_ws(const Plan& p, int B, const void* ws, size_t ws_bytes) {
+    if (cpattn_status_t s = reject_ulysses(p)) return s;
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    const size_t need = cpattn::ws_layout(p, B).bring_end;
+    if (ws_bytes < need)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    return CPATTN_OK;
+}
+
+}  // namespace
+
+cpattn_status_t cpattn_backward_begin(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout, const int32_t* pos, void* ws,
+                                      size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_bring_ws(*p, B, ws, ws_bytes);
+    if (s) return s;
+    s = backward_prepare(*p, B, q, k, v, o, lse, dout, pos, nullptr, ws, ws_bytes, cpattn::ws_layout(*p, B).bring_end,
+                         reinterpret_cast<cudaStream_t>(stream));
+    if (s) return s;
+    p->next_bstep = 0;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_backward_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
+                                          cpattn_stream_t compute, cpattn_stream_t copy) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_bring_ws(*p, B, ws, ws_bytes);
+    if (s) return s;
+    if (step < 0 || step >= p->n_cp) return fail(CPATTN_ERR_INVALID, "step out of range");
+    if (p->next_bstep != step)
+        return fail(CPATTN_ERR_INVALID, "backward ring steps must follow cpattn_backward_begin in order 0..n_cp-1 "
+                                        "(expected step " + std::to_string(p->next_bstep) + ")");
+    cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute), xst = reinterpret_cast<cudaStream_t>(copy);
+    int e = 0;
+    auto mk = [&](CUevent_st*& ev) { if (!ev && !e) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming); };
+    for (int i = 0; i < 2; ++i) { mk(p->bev_kv[i]); mk(p->bev_used[i]); mk(p->bev_circ[i]); }
+    mk(p->bev_ready);
+    mk(p->bev_start);
+    if (e) return cuda_fail(e, "cudaEventCreate");
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    const int slot = step & 1, nxt = (step + 1) & 1;
+
+    if (step == 0) {   // the copy stream must see the placed blocks
+        if ((e = cudaEventRecord(p->bev_start, cst)) || (e = cudaStreamWaitEvent(xst, p->bev_start, 0)))
+            return cuda_fail(e, "stream ordering");
+    } else if ((e = cudaStreamWaitEvent(cst, p->bev_kv[slot], 0))) {   // this step's K, V have arrived
+        return cuda_fail(e, "cudaStreamWaitEvent");
+    }
+    // dK/dV of the visiting blocks against this rank's queries, and this step's dQ
+    cpattn::BwdLaunch a = bwd_args(*p, B, scale, ws, nullptr);
+    a.step = step;
+    if (step > 0) { a.kL = at<char>(ws, w.bstageK[slot]); a.vL = at<char>(ws, w.bstageV[slot]); }
+    a.dk_f32 = at<float>(ws, step == 0 ? w.circK[0] : w.contribK);   // step 0 starts the partial sum
+    a.dv_f32 = at<float>(ws, step == 0 ? w.circV[0] : w.contribV);
+    a.dq_run = at<float>(ws, w.dq_run);
+    std::string why;
+    if ((e = cpattn::launch_backward(a, cst, &why))) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
+    if ((e = cudaEventRecord(p->bev_used[slot], cst))) return cuda_fail(e, "cudaEventRecord");
+    // add the contribution to the partial sum that arrived with the block (the receive is the
+    // only thing this waits for, so the hop overlapped the kernels above)
+    const size_t nkv = (size_t)B * p->T * p->n_kv * p->d;   // floats of one gradient over all ranks
+    if (step > 0) {
+        if ((e = cudaStreamWaitEvent(cst, p->bev_circ[slot], 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+        if ((e = cpattn::launch_add_f32(at<float>(ws, w.circK[slot]), at<float>(ws, w.contribK), (int64_t)nkv, cst)) ||
+            (e = cpattn::launch_add_f32(at<float>(ws, w.circV[slot]), at<float>(ws, w.contribV), (int64_t)nkv, cst)))
+            return cuda_fail(e, "gradient add kernel");
+    }
+    if ((e = cudaEventRecord(p->bev_ready, cst))) return cuda_fail(e, "cudaEventRecord");
+
+    // K, V for the next step: slot nxt of rank r <- the block rank r - 1 holds now (issued before
+    // the gradient hop so that it overlaps this step's kernels)
+    const size_t blk_kv = 2 * (size_t)B * p->n * p->n_kv * p->d, blk_g = 2 * blk_kv;   // bf16, fp32 bytes
+    if (step + 1 < p->n_cp) {
+        if (step >= 1 && (e = cudaStreamWaitEvent(xst, p->bev_used[nxt], 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+        for (int t = 0; t < 2; ++t) {
+            const char* src = step == 0 ? at<char>(ws, t ? w.vL : w.kL) : at<char>(ws, t ? w.bstageV[slot] : w.bstageK[slot]);
+            if ((e = ring_hop(src, at<char>(ws, t ? w.bstageV[nxt] : w.bstageK[nxt]), blk_kv, p->n_cp, xst)))
+                return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
+        }
+        if ((e = cudaEventRecord(p->bev_kv[nxt], xst))) return cuda_fail(e, "cudaEventRecord");
+    }
+    // the partial dK/dV sums move on with their blocks; after the last step this hop returns each
+    // block's gradient to its owner
+    if ((e = cudaStreamWaitEvent(xst, p->bev_ready, 0))) return cuda_fail(e, "cudaStreamWaitEvent");
+    for (int t = 0; t < 2; ++t)
+        if ((e = ring_hop(at<char>(ws, t ? w.circV[slot] : w.circK[slot]), at<char>(ws, t ? w.circV[nxt] : w.circK[nxt]),
+                          blk_g, p->n_cp, xst)))
+            return cuda_fail(e, "cudaMemcpyAsync(gradient hop)");
+    if ((e = cudaEventRecord(p->bev_circ[nxt], xst))) return cuda_fail(e, "cudaEventRecord");
+    p->next_bstep = step + 1;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_backward_finalize(cpattn_plan_t plan, int B, void* dq, void* dk, void* dv, void* ws,
+                                         size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_bring_ws(*p, B, ws, ws_bytes);
+    if (s) return s;
+    if (!dq || !dk || !dv || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(CPATTN_ERR_INVALID, "dq, dk and dv must be non-NULL and 16-byte aligned");
+    if (p->next_bstep != p->n_cp) return fail(CPATTN_ERR_INVALID, "backward finalize needs all n_cp ring steps first");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    const int home = p->n_cp & 1;   // the slot the returning gradients arrived in
+    int e = cudaStreamWaitEvent(st, p->bev_circ[home], 0);
+    if (e) return cuda_fail(e, "cudaStreamWaitEvent");
+    if ((e = cpattn::launch_unpermute_f32(at<float>(ws, w.dq_run), dq, B, p->T, p->n, p->m, p->h, p->d, p->n_cp, p->layout, st)) ||
+        (e = cpattn::launch_unpermute_f32(at<float>(ws, w.circK[home]), dk, B, p->T, p->n, p->m, p->n_kv, p->d, p->n_cp,
+                                          p->layout, st)) ||
+        (e = cpattn::launch_unpermute_f32(at<float>(ws, w.circV[home]), dv, B, p->T, p->n, p->m, p->n_kv, p->d, p->n_cp,
+                                          p->layout, st)))
+        return cuda_fail(e, "gradient unpermute kernel");
+    p->next_bstep = -1;
     return CPATTN_OK;
 }
 

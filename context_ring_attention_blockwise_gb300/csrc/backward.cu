@@ -65,6 +65,13 @@ struct BwdParams {
     uint16_t* dv;
     uint32_t* header;
     uint64_t timeout_ns;
+    // One ring step (step >= 0) instead of the whole walk (-1). K and V rows are then indexed by
+    // the rank holding the block at that step; dK/dV leave as this step's fp32 contribution
+    // [holder][B][n_kv][n][d] and dQ is added into the running fp32 [r][B][h][n][d].
+    int step;
+    float* dk_f32;
+    float* dv_f32;
+    float* dq_run;
 };
 
 struct BWaiter {
@@ -352,11 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const BWaiter wait{abort_flag, P.header, P.timeout_ns};
     const int4 kmm = __ldg(P.tile_mm + src * P.n_qt + kt);
+    // rank whose slot holds this key block's K, V (and receives its dK/dV contribution): the
+    // owner for the whole walk; at ring step s, rank src + s
+    const int kvr = P.step >= 0 ? (src + P.step) % P.n_cp : src;
+    const int s_lo = P.step >= 0 ? P.step : 0, s_hi = P.step >= 0 ? P.step + 1 : P.n_cp;
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: fixed K, V; walk (s, qt, head); stream Q, dO + side data
-            const int krow = (int)((((int64_t)src * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)kt * 128);
+            const int krow = (int)((((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)kt * 128);
             mbar_arrive_expect_tx(bars.fixed_full(), 2 * C::TILE);
             for (int pn = 0; pn < C::PANELS; ++pn) {
                 tma_load_2d(sb + C::OFF_F0 + pn * C::PANEL_BYTES, &tmK, bars.fixed_full(), pn * 64, krow);
@@ -390,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ns;
                 return true;
             };
-            for (int s = 0; s < P.n_cp && ok; ++s) {
+            for (int s = s_lo; s < s_hi && ok; ++s) {
                 const int r = (src + s) % P.n_cp;         // the block's gradient is at rank src + s at step s
                 // Causal: the query tiles whose positions all precede the key tile's first one see
                 // none of it, and they are the tiles before the first whose running maximum (.w,
@@ -624,7 +635,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // tcgen05.ld is a warp-wide instruction: every lane loads, and only the lanes of valid
         // keys store (the last key tile of a block may be short)
-        if (ok) {
+        if (ok && P.dk_f32) {
+            // one ring step: this step's contribution, fp32, in the holder's slot
+            const int64_t krow = (((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + jk;
+            float4* fk = reinterpret_cast<float4*>(P.dk_f32 + krow * D);
+            float4* fv = reinterpret_cast<float4*>(P.dv_f32 + krow * D);
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col0 = (which ? C::COL_A1 : C::COL_A0) + (uint32_t)(wg * (D / 2));
+                const float mul = which ? P.scale : 1.0f;
+                float4* f = which ? fk : fv;
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t t[32];
+                    if (n_steps > 0) {
+                        tmem_ld32(tmem + lane_base + col0 + c * 32, t);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) t[q] = 0u;
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 x = make_float4(__uint_as_float(t[4 * q4]) * mul, __uint_as_float(t[4 * q4 + 1]) * mul,
+                                                     __uint_as_float(t[4 * q4 + 2]) * mul, __uint_as_float(t[4 * q4 + 3]) * mul);
+                        if (key_valid) f[(wg * (D / 2) + c * 32) / 4 + q4] = x;
+                    }
+                }
+            }
+        } else if (ok) {
             const int64_t tn = key_valid ? natural_token(P.layout, src, jk, P.n, P.m, P.n_cp) : 0;
             uint4* gk = reinterpret_cast<uint4*>(P.dk + (((int64_t)b * P.T + tn) * P.n_kv + kvh) * D);
             uint4* gv = reinterpret_cast<uint4*>(P.dv + (((int64_t)b * P.T + tn) * P.n_kv + kvh) * D);
@@ -736,7 +774,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = ns % kRing, st = ns % kNS;
                 if (!(flags & kFlagEmpty)) {
                     if (ns >= kNS && !wait(bars.st_empty(st), ((ns / kNS) - 1) & 1, kBSiteStageEmpty)) return false;
-                    const int krow = (int)((((int64_t)srcr * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)ktt * 128);
+                    // one ring step: the visiting block sits in rank r's slot
+                    const int kvr = P.step >= 0 ? r : srcr;
+                    const int krow = (int)((((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + (int64_t)ktt * 128);
                     mbar_arrive_expect_tx(bars.st_full(st), 2 * C::TILE);
                     const uint32_t s0 = sb + C::OFF_S + (2 * st) * C::TILE, s1 = s0 + C::TILE;
                     for (int pn = 0; pn < C::PANELS; ++pn) {
@@ -750,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ns;
                 return true;
             };
-            for (int s = 0; s < P.n_cp && ok; ++s) {
+            const int s_lo = P.step >= 0 ? P.step : 0, s_hi = P.step >= 0 ? P.step + 1 : P.n_cp;
+            for (int s = s_lo; s < s_hi && ok; ++s) {
                 const int srcr = (r - s + P.n_cp) % P.n_cp;     // the block rank r holds at step s
                 for (int ktt = 0; ktt < P.n_qt && ok; ++ktt) {
                     const int4 kmm = __ldg(P.tile_mm + srcr * P.n_qt + ktt);
@@ -976,7 +1017,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) tc_fence_after();
         }
         // warp-wide TMEM loads; only the lanes of valid query rows store
-        if (ok) {
+        if (ok && P.dq_run) {
+            // one ring step: add this step's dQ into the running fp32 rows of rank r (step 0 writes)
+            float4* f = reinterpret_cast<float4*>(P.dq_run + ((((int64_t)r * P.B + b) * P.h + head) * P.n + jq) * D);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t t[32];
+                if (n_steps > 0) {
+                    tmem_ld32(tmem + lane_base + C::COL_A0 + wg * (D / 2) + c * 32, t);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) t[q] = 0u;
+                }
+                if (q_valid) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const int idx = (wg * (D / 2) + c * 32) / 4 + q4;
+                        float4 x = make_float4(__uint_as_float(t[4 * q4]) * P.scale, __uint_as_float(t[4 * q4 + 1]) * P.scale,
+                                               __uint_as_float(t[4 * q4 + 2]) * P.scale, __uint_as_float(t[4 * q4 + 3]) * P.scale);
+                        if (P.step > 0) {
+                            const float4 y = f[idx];
+                            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+                        }
+                        f[idx] = x;
+                    }
+                }
+            }
+        } else if (ok) {
             const int64_t tn = q_valid ? natural_token(P.layout, r, jq, P.n, P.m, P.n_cp) : 0;
             uint4* g = reinterpret_cast<uint4*>(P.dq + (((int64_t)b * P.T + tn) * P.h + head) * D);
 #pragma unroll
@@ -1039,6 +1106,7 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
     P.header = a.header; P.timeout_ns = a.timeout_ns;
+    P.step = a.step; P.dk_f32 = a.dk_f32; P.dv_f32 = a.dv_f32; P.dq_run = a.dq_run;
     const int64_t kv_units = (int64_t)a.B * a.n_kv * a.n_cp * a.n_qt, q_units = (int64_t)a.B * a.h * a.n_cp * a.n_qt;
     if (kv_units > INT_MAX || q_units > INT_MAX) {
         *why = "too many work units";

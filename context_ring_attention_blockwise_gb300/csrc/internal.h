@@ -49,6 +49,14 @@ struct WsLayout {
     size_t Dl = 0;          // fp32 [n_cp][B][h][n_qt * 128] -D = -<dO, O> of every query row (padding 0)
     size_t bwd_order = 0;   // int32 [2][n_cp * n_qt]: order_q, then order_kv
     size_t bwd_end = 0;
+    // backward ring-step path (after bwd_end): K/V stage slots, the circulating fp32 dK/dV
+    // partial sums (two slots), one step's dK/dV contribution, and the running fp32 dQ; all
+    // [n_cp][B][...][n][d] with the rank index the block's current holder (dQ: its own rank)
+    size_t bstageK[2] = {0, 0}, bstageV[2] = {0, 0};
+    size_t circK[2] = {0, 0}, circV[2] = {0, 0};
+    size_t contribK = 0, contribV = 0;
+    size_t dq_run = 0;
+    size_t bring_end = 0;
 };
 
 struct Plan {
@@ -68,6 +76,14 @@ struct Plan {
     CUevent_st* ev_copy[2] = {nullptr, nullptr};
     CUevent_st* ev_start = nullptr;
     int next_step = -1;             // step expected next on the ring path (-1: permute first)
+    // backward ring-step path state: K/V of a step arrived, a stage slot's kernels done, the
+    // circulating partial ready to send (after the step's add), a partial arrived
+    CUevent_st* bev_kv[2] = {nullptr, nullptr};
+    CUevent_st* bev_used[2] = {nullptr, nullptr};
+    CUevent_st* bev_ready = nullptr;
+    CUevent_st* bev_circ[2] = {nullptr, nullptr};
+    CUevent_st* bev_start = nullptr;
+    int next_bstep = -1;            // step expected next on the backward ring path (-1: begin first)
     // page-locked copy of order, order_q, order_kv (created on first use): an upload from
     // pageable memory may block the calling thread until the stream drains
     int32_t* pinned_orders = nullptr;
@@ -150,7 +166,18 @@ struct BwdLaunch {
     void* dq; void* dk; void* dv;                         // natural order, bf16
     uint32_t* header;
     uint64_t timeout_ns;
+    // one ring step (step >= 0; -1: the whole walk, fused): K/V rows taken from kL/vL indexed by
+    // the holder rank, the dK/dV contribution written as fp32 by holder (dk_f32, dv_f32) and dQ
+    // added into the running fp32 dq_run (written at step 0)
+    int step = -1;
+    float* dk_f32 = nullptr; float* dv_f32 = nullptr; float* dq_run = nullptr;
 };
 int launch_backward(const BwdLaunch& a, void* stream, std::string* why);
+
+// acc[i] += c[i] over n floats (16-byte aligned, n a multiple of 4)
+int launch_add_f32(float* acc, const float* c, int64_t n, void* stream);
+// fp32 [n_cp][B][H][n][d] in layout order -> bf16 [B][T][H][d] in natural order
+int launch_unpermute_f32(const float* src, void* dst, int B, int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
+                         int layout, void* stream);
 
 }  // namespace cpattn

@@ -1,6 +1,7 @@
 // layout_kernels.cu -- the HBM-bound kernels of the path: token placement (gather Q, K, V and
 // position ids into rank-major layout order), the position range of every tile, the final
-// scatter of the ring-step path back to natural order, and the standalone log-sum-exp merge.
+// scatter of the ring-step paths back to natural order, the backward ring-step path's add of a
+// circulating gradient block, and the standalone log-sum-exp merge.
 //
 // Placement: "Context and expert parallelism", section "The causal mask unbalances the
 // sequence" (contiguous, zigzag and round-robin stripes) and section "In PyTorch" (every
@@ -188,6 +189,41 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
             rank_of(layout, t, n, m, n_cp, r, j);
             lse[e] = lse_run[(((int64_t)r * B + b) * h + hd) * n + j];
         }
+    }
+}
+
+// Backward ring-step path: the circulating fp32 dK/dV partial plus this step's contribution,
+// in place. One thread per float4.
+__global__ void __launch_bounds__(256) add_f32_kernel(float4* __restrict__ acc, const float4* __restrict__ c, int64_t n4) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 a = acc[i], b = c[i];
+        acc[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    }
+}
+
+// fp32 [n_cp][B][H][n][d] in layout order -> bf16 [B,T,H,d] in natural order (the backward
+// ring-step path's gradients). One thread per 4 outputs, destination order.
+__global__ void __launch_bounds__(256) unpermute_f32_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, int B,
+                                                            int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
+                                                            int layout) {
+    const int cpr = d / 4;
+    const int64_t no = (int64_t)B * T * H * cpr;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < no; i += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % cpr);
+        int64_t rest = i / cpr;
+        const int hd = (int)(rest % H);
+        rest /= H;
+        const int64_t t = rest % T;
+        const int b = (int)(rest / T);
+        int r;
+        int64_t j;
+        rank_of(layout, t, n, m, n_cp, r, j);
+        const float4 x = src[((((int64_t)r * B + b) * H + hd) * n + j) * cpr + c];
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t*>(&lo);
+        out.y = *reinterpret_cast<uint32_t*>(&hi);
+        dst[i] = out;
     }
 }
 
@@ -391,6 +427,21 @@ int launch_finalize(const FinalizeArgs& a, void* stream) {
     finalize_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(a.o_run), a.lse_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m, a.h,
         a.d, a.n_cp, a.layout);
+    return (int)cudaGetLastError();
+}
+
+int launch_add_f32(float* acc, const float* c, int64_t n, void* stream) {
+    const int64_t n4 = n / 4;
+    add_f32_kernel<<<grid_for(n4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<float4*>(acc), reinterpret_cast<const float4*>(c), n4);
+    return (int)cudaGetLastError();
+}
+
+int launch_unpermute_f32(const float* src, void* dst, int B, int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
+                         int layout, void* stream) {
+    const int64_t work = (int64_t)B * T * H * (d / 4);
+    unpermute_f32_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float4*>(src), static_cast<uint2*>(dst), B, T, n, m, H, d, n_cp, layout);
     return (int)cudaGetLastError();
 }
 

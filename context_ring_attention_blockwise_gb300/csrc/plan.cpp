@@ -59,6 +59,18 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.Dl = take(4 * padded);
     w.bwd_order = take(sizeof(int32_t) * 2 * (size_t)p.n_cp * p.n_qt);
     w.bwd_end = off;
+    for (int s = 0; s < 2; ++s) {
+        w.bstageK[s] = take(2 * (size_t)B * T * p.n_kv * d);
+        w.bstageV[s] = take(2 * (size_t)B * T * p.n_kv * d);
+    }
+    for (int s = 0; s < 2; ++s) {
+        w.circK[s] = take(4 * (size_t)B * T * p.n_kv * d);
+        w.circV[s] = take(4 * (size_t)B * T * p.n_kv * d);
+    }
+    w.contribK = take(4 * (size_t)B * T * p.n_kv * d);
+    w.contribV = take(4 * (size_t)B * T * p.n_kv * d);
+    w.dq_run = take(4 * (size_t)B * T * p.h * d);
+    w.bring_end = off;
     return w;
 }
 

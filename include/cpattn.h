@@ -170,7 +170,8 @@ cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, 
  * block, roughly doubling the traffic): the other n_cp - 1 ranks' K and V blocks in bf16, and the
  * n_cp arrivals of the circulating dK and dV blocks as fp32 partial sums (the last hop returns a
  * rank's own block): 4 B n d_kv (n_cp - 1) + 8 B n d_kv n_cp. bytes_recv [n_cp] (host, written).
- * Host only; the one-GPU backward keeps each block's partial sums in tensor memory. */
+ * Host only. The fused backward keeps each block's partial sums in tensor memory; the ring-step
+ * backward (cpattn_backward_ring_step) moves exactly these bytes between the ranks' slots. */
 cpattn_status_t cpattn_backward_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv);
 cpattn_status_t cpattn_backward_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 cpattn_status_t cpattn_backward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v, const void* o,
@@ -185,6 +186,34 @@ cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q,
                                        const void* o, const float* lse, const void* dout, const int32_t* pos,
                                        const int32_t* lo, float scale, void* dq, void* dk, void* dv, void* ws,
                                        size_t ws_bytes, cpattn_stream_t stream);
+
+/* The backward pass as ring steps ([CEX] "What context parallelism communicates": each rank
+ * keeps the gradient of its own queries; the key and value gradients of a block travel with the
+ * block as a second circulating block and return to its owner). Same result as cpattn_backward
+ * (without document masks), computed step by step with the ring's data movement made explicit:
+ *   cpattn_backward_begin: placement and the backward's side data (arguments as
+ *     cpattn_backward's inputs). ws / ws_bytes at least cpattn_backward_ring_workspace_size(plan,
+ *     B) bytes, 1024-byte aligned.
+ *   cpattn_backward_ring_step, steps 0..n_cp-1 in order, from one host thread per plan: on
+ *     `compute`, every rank r computes, against its own queries, the dK/dV contribution for the
+ *     block it holds (that of rank (r - step) mod n_cp; step 0 its own) and adds its dQ for that
+ *     block into its running fp32 dQ; the contribution is then added to the block's fp32 partial
+ *     sum, which arrived with the block. On `copy`: the K/V hop for the next step (issued first,
+ *     overlapping this step's kernels) and the hop of the partial sums to the right neighbour;
+ *     after the last step that hop returns each block's sums to its owner. Events order the two
+ *     streams so that no slot is overwritten before the step that read it has finished.
+ *   cpattn_backward_finalize: once the returning sums have arrived, dq [B,T,h,d_k] and dk, dv
+ *     [B,T,n_kv,d_k] bf16 in natural order (device, written, 16-byte aligned), on `stream`.
+ * Out-of-order steps or a finalize before the last step return CPATTN_ERR_INVALID. Asynchronous;
+ * device-side timeouts are read by cpattn_check(plan, ws). */
+cpattn_status_t cpattn_backward_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+cpattn_status_t cpattn_backward_begin(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                      const void* o, const float* lse, const void* dout, const int32_t* pos, void* ws,
+                                      size_t ws_bytes, cpattn_stream_t stream);
+cpattn_status_t cpattn_backward_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
+                                          cpattn_stream_t compute, cpattn_stream_t copy);
+cpattn_status_t cpattn_backward_finalize(cpattn_plan_t plan, int B, void* dq, void* dk, void* dv, void* ws,
+                                         size_t ws_bytes, cpattn_stream_t stream);
 
 /* Ulysses, the head split ([CEX] "Ulysses, splitting by heads instead"), as a comparison
  * workload on one GPU with n_cp virtual ranks. Rank r starts with the tokens r n .. r n + n - 1

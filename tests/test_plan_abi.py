@@ -84,6 +84,31 @@ def test_calls_fail_before_launch_on_bad_arguments():
     assert L.cpattn_finalize(p.handle, 1, fake, fake, fake, p.ring_workspace_size(1), None) == 1
 
 
+def test_backward_ring_calls_fail_before_launch():
+    """The ring-step backward checks its order, step range, workspace and pointers on the host."""
+    L = cp.lib()
+    T, h, n_kv, d, n_cp = 512, 2, 2, 64, 4
+    p = cp.Plan(T, h, n_kv, d, n_cp, "contiguous")
+    fake = ctypes.c_void_p(1 << 20)
+    wsb = p.backward_ring_workspace_size(1)
+    # K/V stage slots (2 x bf16 K, V), circulating dK/dV sums (2 x fp32), one step's contribution
+    # (fp32), the running fp32 dQ, on top of the fused backward's workspace
+    kv = T * n_kv * d
+    extra = 2 * 2 * 2 * kv + 2 * 2 * 4 * kv + 2 * 4 * kv + 4 * T * h * d
+    assert p.backward_workspace_size(1) + extra <= wsb < p.backward_workspace_size(1) + extra + 16 * 1024
+    assert L.cpattn_backward_ring_step(p.handle, 1, 0, 0.0, fake, wsb, None, None) == 1       # begin first
+    assert "cpattn_backward_begin" in L.cpattn_last_error().decode()
+    assert L.cpattn_backward_ring_step(p.handle, 1, n_cp, 0.0, fake, wsb, None, None) == 1    # step out of range
+    assert L.cpattn_backward_ring_step(p.handle, 1, 0, 0.0, fake, wsb - 1, None, None) == 3   # small workspace
+    assert L.cpattn_backward_finalize(p.handle, 1, fake, fake, fake, fake, wsb, None) == 1    # steps first
+    assert "ring steps first" in L.cpattn_last_error().decode()
+    assert L.cpattn_backward_finalize(p.handle, 1, None, fake, fake, fake, wsb, None) == 1    # NULL dq
+    assert L.cpattn_backward_begin(p.handle, 1, None, fake, fake, fake, fake, fake, None, fake, wsb, None) == 1
+    assert L.cpattn_backward_begin(p.handle, 1, fake, fake, fake, fake, fake, fake, None, fake, wsb - 1, None) == 3
+    u = cp.UlyssesPlan(T, h, n_kv, d, 2, True)
+    assert L.cpattn_backward_ring_step(u.handle, 1, 0, 0.0, fake, wsb, None, None) == 1       # a Ulysses plan
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path; would touch fake pointers on a GPU")
 def test_no_cpu_fallback_without_a_device():
     p = cp.Plan(512, 2, 2, 64, 4, "contiguous")
