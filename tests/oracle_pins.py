@@ -20,7 +20,8 @@ import synth
 
 CONTIGUOUS, ZIGZAG, STRIPED = 0, 1, 2
 FULL, DIAG, SKIP = 0, 1, 2
-GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_figures.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "pages_figures.json")) as _f:
+    GOLDEN = json.load(_f)
 
 
 def _qkv(seed, B, T, h, n_kv, d, k_mult=1.0):
@@ -46,7 +47,9 @@ def _sdpa(q, k, v, causal, scale=None, mask=None):
 
 
 def _maxabs(a, b):
-    return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+    # a NaN difference (a planted mistake meeting -inf) stays NaN and fails every "<= tol" check
+    with np.errstate(invalid="ignore"):
+        return float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
 
 
 # --------------------------------------------------------------------------------------

@@ -81,7 +81,8 @@ def _mutate(src: str, old: str, new: str, which):
 
 @pytest.mark.parametrize("name,old,new,which", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(name, old, new, which):
-    src = open(oracle.SOURCE).read()
+    with open(oracle.SOURCE) as f:
+        src = f.read()
     mutated = _mutate(src, old, new, which)
     assert mutated != src
     with tempfile.TemporaryDirectory() as tmp:

@@ -22,7 +22,8 @@ def built():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     return sorted(set(re.findall(r"^\s*(?:cpattn_status_t|const char\*)\s+(cpattn_\w+)\(", text, re.M)))
 
 
