@@ -414,6 +414,32 @@ def run_gpu(args, w):
     return 0
 
 
+def ring_timeline(step_fn, n_cp, stream, copy, next_step_bound):
+    """Event timeline of one ring-step pass: timing events on the compute stream after each
+    step's work and on the copy stream after that step's hops. A hop is hidden when it ends
+    before the compute it must precede does: the same step's (next_step_bound = False: the
+    forward's K/V hop for step s + 1 runs beside step s) or the next step's (True: the
+    backward's gradient hop of step s is added at step s + 1)."""
+    import torch
+    t0 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    marks = []
+    for s in range(n_cp):
+        step_fn(s)
+        ce, xe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ce.record(stream)
+        xe.record(copy)
+        marks.append((ce, xe))
+    torch.cuda.synchronize()
+    c_end = [t0.elapsed_time(ce) for ce, _ in marks]
+    x_end = [t0.elapsed_time(xe) for _, xe in marks]
+    # the last step has no hop to hide (forward) or only the return hop, with no later step (backward)
+    slack = [(c_end[s + 1] if next_step_bound else c_end[s]) - x_end[s] for s in range(n_cp - 1)]
+    step_ms = [c_end[0]] + [c_end[s] - c_end[s - 1] for s in range(1, n_cp)]
+    return {"steps": n_cp, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+            "hops_hidden": all(x >= 0 for x in slack), "min_slack_ms": min(slack) if slack else None}
+
+
 def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     """Secondary measurements: the ring-step path at the same workload, and the HBM-bound
     kernels (placement, merge) against the measured copy bandwidth."""
@@ -483,7 +509,15 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     cp.check(plan, wsr)
     ms = a.elapsed_time(b) / 2
     out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12}
-    del wsr
+    # one more pass with an event timeline: does each K/V hop end before the step beside it?
+    o2, lse2 = torch.empty_like(q), torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
+    cp.permute(q, k, v, plan, wsr, stream=stream)
+    out["ring_step_path"]["timeline"] = ring_timeline(
+        lambda s: cp.ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream, copy, False)
+    cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsr)
+    del wsr, o2, lse2
     # document masks: the same workload packed with seeded documents of 2K..16K tokens
     rng = np.random.default_rng(w.seed)
     lengths = []
@@ -546,6 +580,13 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     out["backward_ring_step_path"] = {"ms": ms, "tflops_eff": tf, "frac_of_bf16_sustained": tf / peak,
                                       "includes": "placement and prep, n_cp steps of the dK/dV and dQ kernels with "
                                                   "the K/V and gradient hops and the gradient adds, finalize"}
+    # event timeline: does each step's gradient hop end before the next step's kernels and add?
+    cp.backward_begin(q, k, v, o, lse, dout, plan, wsr, stream=stream)
+    out["backward_ring_step_path"]["timeline"] = ring_timeline(
+        lambda s: cp.backward_ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream, copy, True)
+    cp.backward_finalize(plan, w.B, wsr, dq, dk, dv, stream=stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsr)
     del wsr, dout, dq, dk, dv
     # the head split (Ulysses) as the comparison workload: all-to-all, per-rank attention over
     # every token of h / n_cp heads, all-to-all back; bytes per rank against the ring's
