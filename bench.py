@@ -437,7 +437,8 @@ def ring_timeline(step_fn, n_cp, stream, copy, next_step_bound):
     slack = [(c_end[s + 1] if next_step_bound else c_end[s]) - x_end[s] for s in range(n_cp - 1)]
     step_ms = [c_end[0]] + [c_end[s] - c_end[s - 1] for s in range(1, n_cp)]
     return {"steps": n_cp, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
-            "hops_hidden": all(x >= 0 for x in slack), "min_slack_ms": min(slack) if slack else None}
+            "hops_hidden": all(x >= 0 for x in slack), "min_slack_ms": min(slack) if slack else None,
+            "exposed_ms_total": sum(max(0.0, -x) for x in slack)}
 
 
 def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
