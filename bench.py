@@ -431,12 +431,19 @@ def ring_timeline(step_fn, n_cp, stream, copy, next_step_bound):
         xe.record(copy)
         marks.append((ce, xe))
     torch.cuda.synchronize()
-    c_end = [t0.elapsed_time(ce) for ce, _ in marks]
-    x_end = [t0.elapsed_time(xe) for _, xe in marks]
-    # the last step has no hop to hide (forward) or only the return hop, with no later step (backward)
-    slack = [(c_end[s + 1] if next_step_bound else c_end[s]) - x_end[s] for s in range(n_cp - 1)]
-    step_ms = [c_end[0]] + [c_end[s] - c_end[s - 1] for s in range(1, n_cp)]
-    return {"steps": n_cp, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+    return hop_summary([t0.elapsed_time(ce) for ce, _ in marks], [t0.elapsed_time(xe) for _, xe in marks],
+                       next_step_bound)
+
+
+def hop_summary(c_end, x_end, next_step_bound: bool) -> dict:
+    """From the times (ms from the pass's start) at which each step's compute and its hops
+    ended: per-step compute time, and each hop's slack before the compute it must precede
+    (negative: exposed). The last step has no hop to hide (forward) or only the return hop,
+    with no later step (backward)."""
+    n = len(c_end)
+    slack = [(c_end[s + 1] if next_step_bound else c_end[s]) - x_end[s] for s in range(n - 1)]
+    step_ms = [c_end[0]] + [c_end[s] - c_end[s - 1] for s in range(1, n)]
+    return {"steps": n, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
             "hops_hidden": all(x >= 0 for x in slack), "min_slack_ms": min(slack) if slack else None,
             "exposed_ms_total": sum(max(0.0, -x) for x in slack)}
 

@@ -44,3 +44,16 @@ def test_single_rank_helpers():
     assert bench.reduce_max(3.5, None) == 3.5
     assert bench.whole_job_rate(1.0e12, 1, 1000.0) == pytest.approx(1.0e12)
     assert bench.measured_traffic("no_such_workload") is None
+
+
+def test_hop_summary_slack_and_exposure():
+    """The ring-step timelines' arithmetic: a forward hop must end before its own step's compute,
+    a backward gradient hop before the next step's; the last step's hop is not judged."""
+    c_end = [10.0, 20.0, 30.0]
+    fwd = bench.hop_summary(c_end, [9.0, 20.5, 31.0], next_step_bound=False)
+    assert fwd["steps"] == 3 and fwd["step_ms_min"] == 10.0 and fwd["step_ms_max"] == 10.0
+    assert not fwd["hops_hidden"] and fwd["min_slack_ms"] == -0.5 and fwd["exposed_ms_total"] == 0.5
+    bwd = bench.hop_summary(c_end, [12.0, 25.0, 40.0], next_step_bound=True)
+    assert bwd["hops_hidden"] and bwd["min_slack_ms"] == 5.0 and bwd["exposed_ms_total"] == 0.0
+    one = bench.hop_summary([7.0], [8.0], next_step_bound=False)
+    assert one["hops_hidden"] and one["min_slack_ms"] is None
