@@ -138,6 +138,8 @@ struct Bars {
         mbar_init(mma_done(), 1);
     }
 };
+static_assert(Bars<64>::kCount == Cfg<64>::NBAR && Bars<128>::kCount == Cfg<128>::NBAR,
+              "the shared-memory barrier region holds every barrier");
 
 enum Site : int { kSiteQ = 1, kSiteKFull, kSiteVFull, kSiteKEmpty, kSiteVEmpty, kSiteSFull, kSiteQEmpty,
                   kSitePFull, kSitePvDone, kSiteDrain, kSiteSelfTest, kSiteUnitFull, kSiteUnitEmpty, kSiteOFree };
