@@ -97,7 +97,7 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
 cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                               cpattn_stream_t stream);
 
-/* cpattn_forward for callers that cannot allocate device memory. The paper has no counterpart:
+/* cpattn_forward for callers that cannot allocate device memory. The source pages describe no such call:
  * this call exists for code that may not call cudaMalloc or any allocating routine, such as a
  * host callback, an allocator hook or a plug-in that must leave the process's memory pools alone.
  * Same arguments as cpattn_forward minus the workspace: the scratch is a 64 MiB device array

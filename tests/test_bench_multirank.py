@@ -48,7 +48,7 @@ def test_single_rank_helpers():
 
 def test_hop_summary_slack_and_exposure():
     """The ring-step timelines' arithmetic: a forward hop must end before its own step's compute,
-    a backward gradient hop before the next step's; the last step's hop is not judged."""
+    a backward gradient hop before the next step's; the last step's hop is not counted."""
     c_end = [10.0, 20.0, 30.0]
     fwd = bench.hop_summary(c_end, [9.0, 20.5, 31.0], next_step_bound=False)
     assert fwd["steps"] == 3 and fwd["step_ms_min"] == 10.0 and fwd["step_ms_max"] == 10.0
