@@ -631,7 +631,7 @@ def main():
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per attention launch from ncu, if known")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="query rows the CPU baseline computes")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="query rows the CPU baseline computes (~13 s on 16 cores)")
     ap.add_argument("--ref-rows", type=int, default=8, help="query rows per step of the reference arm")
     args = ap.parse_args()
     w = synth.workload(args.workload)
