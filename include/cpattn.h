@@ -127,7 +127,9 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
  * enqueues the hop to the next step: every rank's slot (step+1) % 2 receives the block its left
  * neighbour holds now (send right, receive left), ordered against the compute stream with
  * events so that a slot is overwritten only after the step that read it has finished. Steps
- * must be issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan. */
+ * must be issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan, with
+ * cpattn_permute and cpattn_finalize on the stream passed here as `compute` (step 0 orders the
+ * copy stream after the compute stream only). */
 cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
                                  cpattn_stream_t compute, cpattn_stream_t copy);
 
@@ -204,8 +206,10 @@ cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q,
  *     streams so that no slot is overwritten before the step that read it has finished.
  *   cpattn_backward_finalize: once the returning sums have arrived, dq [B,T,h,d_k] and dk, dv
  *     [B,T,n_kv,d_k] bf16 in natural order (device, written, 16-byte aligned), on `stream`.
- * Out-of-order steps or a finalize before the last step return CPATTN_ERR_INVALID. Asynchronous;
- * device-side timeouts are read by cpattn_check(plan, ws). */
+ * cpattn_backward_begin and cpattn_backward_finalize must run on the stream passed to the steps
+ * as `compute` (step 0 orders the copy stream after the compute stream only). Out-of-order steps
+ * or a finalize before the last step return CPATTN_ERR_INVALID. Asynchronous; device-side
+ * timeouts are read by cpattn_check(plan, ws). */
 cpattn_status_t cpattn_backward_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 cpattn_status_t cpattn_backward_begin(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                       const void* o, const float* lse, const void* dout, const int32_t* pos, void* ws,
