@@ -435,6 +435,7 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
     if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
     if ((s = prologue(*p, B, q, k, v, pos, ws, reinterpret_cast<cudaStream_t>(stream)))) return s;
     p->next_step = 0;
+    p->ring_B = B;
     return CPATTN_OK;
 }
 
@@ -449,6 +450,7 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
     if (p->next_step != step)
         return fail(CPATTN_ERR_INVALID, "ring steps must follow cpattn_permute in order 0..n_cp-1 (expected step " +
                                             std::to_string(p->next_step) + ")");
+    if (B != p->ring_B) return fail(CPATTN_ERR_INVALID, "B differs from the batch cpattn_permute placed");
     cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute), xst = reinterpret_cast<cudaStream_t>(copy);
     int e;
     for (int i = 0; i < 2; ++i) {
@@ -504,6 +506,7 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
     cpattn_status_t s = check_ws(*p, B, ws, ws_bytes, true);
     if (s) return s;
     if (p->next_step != p->n_cp) return fail(CPATTN_ERR_INVALID, "finalize needs all n_cp ring steps first");
+    if (B != p->ring_B) return fail(CPATTN_ERR_INVALID, "B differs from the batch cpattn_permute placed");
     cpattn::WsLayout w = cpattn::ws_layout(*p, B);
     cpattn::FinalizeArgs a{};
     a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.d = p->d; a.n_cp = p->n_cp; a.layout = p->layout;
@@ -555,6 +558,7 @@ cpattn_status_t cpattn_backward_begin(cpattn_plan_t plan, int B, const void* q, 
                          reinterpret_cast<cudaStream_t>(stream));
     if (s) return s;
     p->next_bstep = 0;
+    p->bring_B = B;
     return CPATTN_OK;
 }
 
@@ -568,6 +572,7 @@ cpattn_status_t cpattn_backward_ring_step(cpattn_plan_t plan, int B, int step, f
     if (p->next_bstep != step)
         return fail(CPATTN_ERR_INVALID, "backward ring steps must follow cpattn_backward_begin in order 0..n_cp-1 "
                                         "(expected step " + std::to_string(p->next_bstep) + ")");
+    if (B != p->bring_B) return fail(CPATTN_ERR_INVALID, "B differs from the batch cpattn_backward_begin placed");
     cudaStream_t cst = reinterpret_cast<cudaStream_t>(compute), xst = reinterpret_cast<cudaStream_t>(copy);
     int e = 0;
     auto mk = [&](CUevent_st*& ev) { if (!ev && !e) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming); };
@@ -638,6 +643,7 @@ cpattn_status_t cpattn_backward_finalize(cpattn_plan_t plan, int B, void* dq, vo
     if (!dq || !dk || !dv || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(CPATTN_ERR_INVALID, "dq, dk and dv must be non-NULL and 16-byte aligned");
     if (p->next_bstep != p->n_cp) return fail(CPATTN_ERR_INVALID, "backward finalize needs all n_cp ring steps first");
+    if (B != p->bring_B) return fail(CPATTN_ERR_INVALID, "B differs from the batch cpattn_backward_begin placed");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cpattn::WsLayout w = cpattn::ws_layout(*p, B);
     const int home = p->n_cp & 1;   // the slot the returning gradients arrived in

@@ -76,6 +76,7 @@ struct Plan {
     CUevent_st* ev_copy[2] = {nullptr, nullptr};
     CUevent_st* ev_start = nullptr;
     int next_step = -1;             // step expected next on the ring path (-1: permute first)
+    int ring_B = 0;                 // batch size cpattn_permute placed (the steps must use the same)
     // backward ring-step path state: K/V of a step arrived, a stage slot's kernels done, the
     // circulating partial ready to send (after the step's add), a partial arrived
     CUevent_st* bev_kv[2] = {nullptr, nullptr};
@@ -84,6 +85,7 @@ struct Plan {
     CUevent_st* bev_circ[2] = {nullptr, nullptr};
     CUevent_st* bev_start = nullptr;
     int next_bstep = -1;            // step expected next on the backward ring path (-1: begin first)
+    int bring_B = 0;                // batch size cpattn_backward_begin placed
     // page-locked copy of order, order_q, order_kv (created on first use): an upload from
     // pageable memory may block the calling thread until the stream drains
     int32_t* pinned_orders = nullptr;

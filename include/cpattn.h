@@ -129,7 +129,8 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
  * events so that a slot is overwritten only after the step that read it has finished. Steps
  * must be issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan, with
  * cpattn_permute and cpattn_finalize on the stream passed here as `compute` (step 0 orders the
- * copy stream after the compute stream only). */
+ * copy stream after the compute stream only), and with the B cpattn_permute placed; otherwise
+ * CPATTN_ERR_INVALID before any launch. */
 cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
                                  cpattn_stream_t compute, cpattn_stream_t copy);
 
@@ -207,9 +208,10 @@ cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q,
  *   cpattn_backward_finalize: once the returning sums have arrived, dq [B,T,h,d_k] and dk, dv
  *     [B,T,n_kv,d_k] bf16 in natural order (device, written, 16-byte aligned), on `stream`.
  * cpattn_backward_begin and cpattn_backward_finalize must run on the stream passed to the steps
- * as `compute` (step 0 orders the copy stream after the compute stream only). Out-of-order steps
- * or a finalize before the last step return CPATTN_ERR_INVALID. Asynchronous; device-side
- * timeouts are read by cpattn_check(plan, ws). */
+ * as `compute` (step 0 orders the copy stream after the compute stream only). Out-of-order steps,
+ * a B other than cpattn_backward_begin's, or a finalize before the last step return
+ * CPATTN_ERR_INVALID before any launch. Asynchronous; device-side timeouts are read by
+ * cpattn_check(plan, ws). */
 cpattn_status_t cpattn_backward_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 cpattn_status_t cpattn_backward_begin(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                       const void* o, const float* lse, const void* dout, const int32_t* pos, void* ws,

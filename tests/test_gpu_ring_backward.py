@@ -133,3 +133,25 @@ def test_ring_backward_workload_sampled():
     _compare(dq[:, rows], rq, "dq (sampled rows)")
     _compare(dk[:, keys], rk, "dk (last keys)")
     _compare(dv[:, keys], rv, "dv (last keys)")
+
+
+def test_ring_paths_refuse_another_batch():
+    """The ring steps and finalize must use the batch size the placement used; another one is
+    refused on the host (CPATTN_ERR_INVALID), even with a workspace large enough for it."""
+    q, k, v, do = _inputs(82, 1, 512, 2, 1, 64)
+    plan = cp.Plan(512, 2, 1, 64, 4, ZIGZAG, True)
+    qd, kd, vd, dod = (to_device_bf16(x) for x in (q, k, v, do))
+    o, lse = cp.forward(qd, kd, vd, plan)
+    copy = torch.cuda.Stream()
+    ws = cp.alloc_workspace(plan.backward_ring_workspace_size(2))
+    cp.backward_begin(qd, kd, vd, o, lse, dod, plan, ws)
+    with pytest.raises(cp.CpattnError) as e:
+        cp.backward_ring_step(plan, 2, 0, ws, copy=copy)
+    assert e.value.status == 1
+    wsf = cp.alloc_workspace(plan.ring_workspace_size(2))
+    cp.permute(qd, kd, vd, plan, wsf)
+    with pytest.raises(cp.CpattnError) as e:
+        cp.ring_step(plan, 2, 0, wsf, copy=copy)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    cp.check(plan, wsf)
