@@ -57,3 +57,18 @@ def test_hop_summary_slack_and_exposure():
     assert bwd["hops_hidden"] and bwd["min_slack_ms"] == 5.0 and bwd["exposed_ms_total"] == 0.0
     one = bench.hop_summary([7.0], [8.0], next_step_bound=False)
     assert one["hops_hidden"] and one["min_slack_ms"] is None
+
+
+@pytest.mark.parametrize("name", sorted(__import__("synth").CONFIGS))
+def test_effective_flops_follow_the_visible_pairs(name):
+    """The bench's FLOP count against the plan's exact visible pairs (bit-exact against the
+    oracle's brute force elsewhere): 4 B h d per pair, with a causal diagonal counted as half, so
+    T^2/2 = T(T+1)/2 - T/2 pairs per (b, head)."""
+    import synth
+    import context_ring_attention_blockwise_gb300 as cp
+    w = synth.workload(name)
+    plan = cp.Plan(w.T, w.h, w.n_kv, w.d, w.n_cp, w.layouts[0], w.causal)
+    exact = int(plan.counts(1)["pairs"].sum())
+    assert exact == (w.T * (w.T + 1) // 2 if w.causal else w.T * w.T)
+    effective = exact - w.T / 2 if w.causal else exact
+    assert bench.flops_eff(w) == 4.0 * w.B * w.h * w.d * effective
