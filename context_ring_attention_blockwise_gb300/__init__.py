@@ -23,7 +23,7 @@ _lib = None
 
 SYMBOLS = [
     "cpattn_plan", "cpattn_plan_destroy", "cpattn_workspace_size", "cpattn_ring_workspace_size", "cpattn_forward",
-    "cpattn_attend", "cpattn_forward_noalloc",
+    "cpattn_attend", "cpattn_forward_noalloc", "cpattn_check_noalloc", "cpattn_selftest_wait_timeout_noalloc",
     "cpattn_permute", "cpattn_ring_step", "cpattn_finalize", "cpattn_merge", "cpattn_plan_counts",
     "cpattn_tile_shape", "cpattn_tile_counts", "cpattn_check", "cpattn_selftest_wait_timeout", "cpattn_last_error", "cpattn_version",
     "cpattn_backward_workspace_size", "cpattn_backward", "cpattn_forward_masked", "cpattn_backward_masked",
@@ -61,6 +61,8 @@ def lib():
     L.cpattn_forward.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_forward_noalloc.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P]
+    L.cpattn_check_noalloc.argtypes = [_P]
+    L.cpattn_selftest_wait_timeout_noalloc.argtypes = [u64, _P]
     L.cpattn_permute.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_ring_step.argtypes = [_P, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, _P]
     L.cpattn_finalize.argtypes = [_P, i, _P, _P, _P, ctypes.c_size_t, _P]
@@ -379,7 +381,8 @@ def forward_masked(q, k, v, plan: Plan, lo, pos=None, scale: float | None = None
 
 def forward_noalloc(q, k, v, plan: Plan, pos=None, scale: float | None = None, out=None, lse=None, stream=None):
     """cpattn_forward_noalloc: the forward with the library's built-in 64 MiB device scratch, for
-    callers that cannot allocate a workspace (outputs may still come from the caller)."""
+    callers that cannot allocate a workspace (outputs may still come from the caller). A device-side
+    timeout is read afterwards by check_noalloc()."""
     torch = _torch()
     B = _check_inputs(plan, q, k, v)
     if out is None:
@@ -390,6 +393,17 @@ def forward_noalloc(q, k, v, plan: Plan, pos=None, scale: float | None = None, o
                                         _dev_ptr(pos, "pos"), float(scale or 0.0), _dev_ptr(out, "o"),
                                         _dev_ptr(lse, "lse"), _stream_ptr(stream)), "cpattn_forward_noalloc")
     return out, lse
+
+
+def check_noalloc(plan: Plan | None = None):
+    """cpattn_check_noalloc: raise CpattnError if a device-side wait of the last allocation-free
+    forward on the current device timed out (call after synchronising its stream)."""
+    _check(lib().cpattn_check_noalloc(plan.handle if plan is not None else None), "cpattn_check_noalloc")
+
+
+def selftest_wait_timeout_noalloc(timeout_ns: int, stream=None):
+    _check(lib().cpattn_selftest_wait_timeout_noalloc(int(timeout_ns), _stream_ptr(stream)),
+           "cpattn_selftest_wait_timeout_noalloc")
 
 
 def permute(q, k, v, plan: Plan, ws, pos=None, stream=None):

@@ -94,16 +94,23 @@ const int32_t* order_src(Plan& p, int which) {
 }
 
 // Reset the header, upload the tile order, place tokens and position ids.
+// upload_by_param: the order table goes to the device inside kernel parameters, so nothing is
+// allocated (no page-locked copy is made) and nothing is staged from pageable memory.
 cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
-                         cudaStream_t st, const int32_t* lo = nullptr) {
+                         cudaStream_t st, const int32_t* lo = nullptr, bool upload_by_param = false) {
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
     e = cudaMemsetAsync(at<char>(ws, w.counts), 0, w.sched + sizeof(uint32_t) * (1 + (size_t)p.n_cp) - w.counts, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(counts)");
-    e = cudaMemcpyAsync(at<char>(ws, w.order), order_src(p, 0), sizeof(int32_t) * p.order.size(),
-                        cudaMemcpyHostToDevice, st);
-    if (e) return cuda_fail(e, "cudaMemcpyAsync(order)");
+    if (upload_by_param) {
+        e = cpattn::launch_upload_i32(at<int32_t>(ws, w.order), p.order.data(), (int64_t)p.order.size(), st);
+        if (e) return cuda_fail(e, "order upload kernel");
+    } else {
+        e = cudaMemcpyAsync(at<char>(ws, w.order), order_src(p, 0), sizeof(int32_t) * p.order.size(),
+                            cudaMemcpyHostToDevice, st);
+        if (e) return cuda_fail(e, "cudaMemcpyAsync(order)");
+    }
     cpattn::PermuteArgs a{};
     a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
     a.layout = p.layout; a.n_qt = p.n_qt;
@@ -267,6 +274,15 @@ cpattn_status_t cpattn_backward_counts(cpattn_plan_t plan, int B, int64_t* bytes
 cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                                cpattn_stream_t stream) {
+    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, ws_bytes, stream, false);
+}
+
+}  // extern "C"
+
+cpattn_status_t cpattn::forward_with_workspace(cpattn_plan_t plan, int B, const void* q, const void* k,
+                                               const void* v, const int32_t* pos, float scale, void* o, float* lse,
+                                               void* ws, size_t ws_bytes, cpattn_stream_t stream,
+                                               bool upload_by_param) {
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
@@ -274,7 +290,7 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
     if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
     if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((s = prologue(*p, B, q, k, v, pos, ws, st))) return s;
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, nullptr, upload_by_param))) return s;
     cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
     a.o = o; a.lse = lse;
@@ -283,6 +299,8 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     return CPATTN_OK;
 }
+
+extern "C" {
 
 namespace {
 // The backward's launch arguments: every pointer into the workspace, the rest from the plan.

@@ -898,10 +898,10 @@ __global__ void unit_tiles_kernel(const Params P) {
 template <int D, bool LB>
 int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     using C = Cfg<D>;
-    static int attr_dev = -1;
+    static PerDeviceOnce attr_once;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (attr_dev != dev) {
+    const int ea = attr_once.run(dev, [&]() -> int {
         cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
@@ -915,8 +915,9 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
                    " registers per thread, too few for its warpgroup register split";
             return (int)cudaErrorInvalidConfiguration;
         }
-        attr_dev = dev;
-    }
+        return 0;
+    });
+    if (ea) return ea;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     CUtensorMap tq, tk, tv;

@@ -1079,17 +1079,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool LB>
 int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     using C = BCfg<D>;
-    static int attr_dev = -1;
+    static PerDeviceOnce attr_once;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (attr_dev != dev) {
+    const int ea = attr_once.run(dev, [&]() -> int {
         cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(bwd_dq_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return (int)e;
-        attr_dev = dev;
-    }
+        return (int)e;
+    });
+    if (ea) return ea;
     CUtensorMap tq, tdo, tk, tv;
     const uint64_t qrows = (uint64_t)a.n_cp * a.B * a.h * a.n, kvrows = (uint64_t)a.n_cp * a.B * a.n_kv * a.n;
     if (!make_map(&tq, a.qL, qrows, D) || !make_map(&tdo, a.doL, qrows, D) || !make_map(&tk, a.kL, kvrows, D) ||

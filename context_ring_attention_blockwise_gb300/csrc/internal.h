@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -94,6 +95,23 @@ struct Plan {
     int u_ncp = 0, u_h = 0, u_nkv = 0;
 };
 
+// One-time set-up per device (kernel attributes), safe when several host threads drive several
+// devices: f() runs under the lock until it succeeds once on a device; devices beyond the table
+// run it on every call.
+struct PerDeviceOnce {
+    static constexpr int kMax = 64;
+    std::mutex mu;
+    bool done[kMax] = {};
+    template <class F>
+    int run(int dev, F&& f) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < kMax && done[dev]) return 0;
+        const int e = f();
+        if (e == 0 && dev >= 0 && dev < kMax) done[dev] = true;
+        return e;
+    }
+};
+
 WsLayout ws_layout(const Plan& p, int B);
 void set_last_error(const std::string& msg);
 int64_t token_of(const Plan& p, int r, int64_t j);   // natural token of (rank, local index)
@@ -138,6 +156,15 @@ int launch_merge(int S, int64_t rows, int h, int d, const float* o_parts, const 
                  float* lse, void* stream);
 
 int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
+
+// Copy n int32 values from host memory to dst by kernel parameters (no host staging buffer).
+int launch_upload_i32(int32_t* dst, const int32_t* host, int64_t n, void* stream);
+
+// cpattn_forward's body. upload_by_param: the unit order reaches the device inside kernel
+// parameters instead of through a page-locked copy (the allocation-free entry point).
+cpattn_status_t forward_with_workspace(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                       const int32_t* pos, float scale, void* o, float* lse, void* ws,
+                                       size_t ws_bytes, cpattn_stream_t stream, bool upload_by_param);
 
 // Ulysses all-to-alls: natural q [B][T][h][d], k/v [B][T][n_kv][d] to per-rank head shards
 // qs [B n_cp][T][hp][d], ks/vs [B n_cp][T][nkvp][d] (batch b n_cp + r'), and the output os

@@ -303,7 +303,33 @@ int grid_for(int64_t work, int threads) {
     return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
+// A small int32 table carried to the device inside the kernel's parameter block: the values are
+// copied when the launch is enqueued, so the upload needs neither a page-locked host buffer nor a
+// host-to-device copy from pageable memory.
+constexpr int kParamInts = 960;
+struct ParamInts {
+    int n;
+    int32_t v[kParamInts];
+};
+
+__global__ void __launch_bounds__(256) upload_i32_kernel(int32_t* __restrict__ dst, const ParamInts vals) {
+    for (int i = threadIdx.x; i < vals.n; i += blockDim.x) dst[i] = vals.v[i];
+}
+
 }  // namespace
+
+int launch_upload_i32(int32_t* dst, const int32_t* host, int64_t n, void* stream) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int64_t off = 0; off < n; off += kParamInts) {
+        ParamInts p;
+        p.n = (int)(n - off < kParamInts ? n - off : kParamInts);
+        for (int i = 0; i < p.n; ++i) p.v[i] = host[off + i];
+        upload_i32_kernel<<<1, 256, 0, st>>>(dst + off, p);
+        const int e = (int)cudaGetLastError();
+        if (e) return e;
+    }
+    return 0;
+}
 
 // ---- Ulysses all-to-alls ("Ulysses, splitting by heads instead") --------------------------
 // Virtual rank r' of n_cp holds, after the first all-to-all, every token of its hp = h / n_cp query

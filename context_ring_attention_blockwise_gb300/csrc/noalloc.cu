@@ -1,17 +1,20 @@
 // noalloc.cu -- cpattn_forward for callers that cannot allocate device memory.
 //
-// Some callers have no way to obtain a workspace: code running where cudaMalloc is forbidden
-// or unavailable (inside a host callback or a custom allocator hook, a plug-in that must not
-// touch the process's memory pools, a real-time loop that may not block on the allocator).
-// For them this file holds the forward's scratch in a statically sized device array that the
-// CUDA runtime places when the library is loaded, so the call itself allocates nothing.
+// Some callers have no way to obtain a workspace: code that runs inside a memory allocator's own
+// hooks (calling the allocator again would recurse), a plug-in loaded into a host process that
+// owns every device memory pool, a real-time loop that may not wait on an allocation. For them
+// this file holds the forward's scratch in a statically sized device array that the CUDA runtime
+// places when the library is loaded, so the call itself allocates nothing: not on the device, and
+// not on the host either (the unit-order table reaches the device inside kernel parameters, not
+// through a page-locked staging copy).
 //
 // The array is kNoAllocScratchBytes (64 MiB) plus alignment slack. Every GPU that loads the
 // library keeps it until the process exits. All calls share it and it keeps whatever the last
 // call left there; the forward's own prologue clears the parts that must start at zero (the
 // error header, the tile counters, the scheduler counters) on every call. Calls whose work
 // overlaps on the GPU (different streams, or different host threads) race on the array; issue
-// them on one stream, one after another.
+// them on one stream, one after another. A device-side timeout of such a call is recorded in the
+// array's header and read back by cpattn_check_noalloc.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,6 +35,36 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+
+// The 1024-byte aligned start of the scratch on the current device. Set-up, once per device with
+// that device current: ask the runtime where it placed the array on this device. The first call
+// of any entry point below on a device does this.
+cpattn_status_t scratch_on_current_device(const char* who, void** ws) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        cpattn::set_last_error(std::string(who) + ": no usable current CUDA device");
+        return CPATTN_ERR_CUDA;
+    }
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_scratch_addr[dev]) {
+            void* ptr = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr) {
+                cpattn::set_last_error(std::string(who) + ": cudaGetSymbolAddress failed: " + cudaGetErrorString(e));
+                return CPATTN_ERR_CUDA;
+            }
+            g_scratch_addr[dev] = ptr;
+        }
+        base = g_scratch_addr[dev];
+    }
+    // The forward wants a 1024-byte aligned workspace; the slack after the array covers it.
+    const uintptr_t p = reinterpret_cast<uintptr_t>(base);
+    *ws = reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
+    return CPATTN_OK;
+}
 
 }  // namespace
 
@@ -54,31 +87,21 @@ extern "C" cpattn_status_t cpattn_forward_noalloc(cpattn_plan_t plan, int B, con
         cpattn::set_last_error(buf);
         return CPATTN_ERR_WORKSPACE;
     }
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cpattn::set_last_error("cpattn_forward_noalloc: no usable current CUDA device");
-        return CPATTN_ERR_CUDA;
-    }
-    void* base = nullptr;
-    {
-        // Set-up, once per device, with that device current: ask the runtime where it placed
-        // the scratch array on this device. The first call on a device does this, so make that
-        // first call before capturing a stream into a graph.
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_addr[dev]) {
-            void* ptr = nullptr;
-            cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-            if (e != cudaSuccess || !ptr) {
-                cpattn::set_last_error(std::string("cpattn_forward_noalloc: cudaGetSymbolAddress failed: ") +
-                                       cudaGetErrorString(e));
-                return CPATTN_ERR_CUDA;
-            }
-            g_scratch_addr[dev] = ptr;
-        }
-        base = g_scratch_addr[dev];
-    }
-    // The forward wants a 1024-byte aligned workspace; the slack after the array covers it.
-    const uintptr_t p = reinterpret_cast<uintptr_t>(base);
-    void* ws = reinterpret_cast<void*>((p + 1023) & ~uintptr_t(1023));
-    return cpattn_forward(plan, B, q, k, v, pos, scale, o, lse, ws, kNoAllocScratchBytes, stream);
+    void* ws = nullptr;
+    if ((s = scratch_on_current_device("cpattn_forward_noalloc", &ws))) return s;
+    // The unit order reaches the scratch inside kernel parameters: no page-locked host copy is made.
+    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, kNoAllocScratchBytes, stream,
+                                          true);
+}
+
+extern "C" cpattn_status_t cpattn_check_noalloc(cpattn_plan_t plan) {
+    void* ws = nullptr;
+    if (cpattn_status_t s = scratch_on_current_device("cpattn_check_noalloc", &ws)) return s;
+    return cpattn_check(plan, ws);
+}
+
+extern "C" cpattn_status_t cpattn_selftest_wait_timeout_noalloc(uint64_t timeout_ns, cpattn_stream_t stream) {
+    void* ws = nullptr;
+    if (cpattn_status_t s = scratch_on_current_device("cpattn_selftest_wait_timeout_noalloc", &ws)) return s;
+    return cpattn_selftest_wait_timeout(ws, kNoAllocScratchBytes, timeout_ns, stream);
 }

@@ -97,21 +97,34 @@ cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const v
 cpattn_status_t cpattn_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                               cpattn_stream_t stream);
 
-/* cpattn_forward for callers that cannot allocate device memory. The source pages describe no such call:
- * this call exists for code that may not call cudaMalloc or any allocating routine, such as a
- * host callback, an allocator hook or a plug-in that must leave the process's memory pools alone.
+/* cpattn_forward for callers that cannot allocate device memory. The source pages describe no
+ * such call: it exists for code that may not call cudaMalloc or any other allocating routine,
+ * such as code running inside a memory allocator's own hooks (where allocating again would
+ * recurse), a plug-in loaded into a host process that owns every device memory pool, or a
+ * real-time loop that may not wait on an allocation.
  * Same arguments as cpattn_forward minus the workspace: the scratch is a 64 MiB device array
  * built into the library, which every GPU that loads the library holds until the process
- * exits. The call itself allocates nothing. A problem whose cpattn_workspace_size exceeds
- * 64 MiB is rejected with CPATTN_ERR_WORKSPACE and a message saying so.
+ * exits. The call allocates nothing, on the device or on the host (the unit order reaches the
+ * device inside kernel parameters). A problem whose cpattn_workspace_size exceeds 64 MiB is
+ * rejected with CPATTN_ERR_WORKSPACE and a message saying so.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *     with that device current; make that first call before capturing a stream.
  *   - All calls share the array and it keeps the last call's contents; each call clears what
  *     must start at zero. Calls that overlap on the GPU (other streams, other threads) race on
- *     it: issue them one after another on one stream. */
+ *     it: issue them one after another on one stream.
+ *   - A device-side timeout is recorded in the array's header: after synchronising the stream,
+ *     cpattn_check_noalloc reports it as cpattn_check does for a caller-owned workspace. */
 cpattn_status_t cpattn_forward_noalloc(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                        const int32_t* pos, float scale, void* o, float* lse,
                                        cpattn_stream_t stream);
+/* cpattn_check for the built-in scratch of cpattn_forward_noalloc on the current device: after
+ * the stream has been synchronised, CPATTN_OK or CPATTN_ERR_TIMEOUT (the message names the wait).
+ * Allocates nothing. */
+cpattn_status_t cpattn_check_noalloc(cpattn_plan_t plan);
+/* cpattn_selftest_wait_timeout on the built-in scratch of the current device: records a timeout
+ * there exactly as a kernel wait that ran out would, so that cpattn_check_noalloc can be tested.
+ * The next cpattn_forward_noalloc clears it. */
+cpattn_status_t cpattn_selftest_wait_timeout_noalloc(uint64_t timeout_ns, cpattn_stream_t stream);
 
 /* Ring-faithful path, step 1: gather Q, K, V and the position ids into layout order inside the
  * workspace (rank-major blocks) and reset the workspace header. Same arguments as

@@ -38,9 +38,9 @@ CONFIGS = {
     "tiny_mha_contig_T512": Workload("tiny_mha_contig_T512", 1, 512, 2, 2, 64, 4, (CONTIGUOUS,), True, 1001,
                                      note="causal MHA, 4 contiguous ranks of 128"),
     "gqa_zigzag_T16k": Workload("gqa_zigzag_T16k", 1, 16384, 32, 8, 128, 8, (ZIGZAG,), True, 1002,
-                                sampled_rows=512, note="causal GQA 4:1, 16 chunks of 1024"),
+                                note="causal GQA 4:1, 16 chunks of 1024"),
     "mha_noncausal_T32k": Workload("mha_noncausal_T32k", 2, 32768, 16, 16, 128, 4, (CONTIGUOUS,), False, 1003,
-                                   k_mult=2.0, sampled_rows=256, note="non-causal MHA, K scaled by 2"),
+                                   k_mult=2.0, sampled_rows=4096, note="non-causal MHA, K scaled by 2"),
     "llama70b_zigzag_T128k": Workload("llama70b_zigzag_T128k", 1, 131072, 64, 8, 128, 16, (ZIGZAG,), True, 1004,
                                       sampled_rows=256, note="70B-shaped causal GQA 8:1, 32 chunks of 4096"),
     "llama405b_tp_T128k": Workload("llama405b_tp_T128k", 1, 131072, 16, 1, 128, 16, (ZIGZAG, STRIPED), True, 1005,

@@ -12,14 +12,29 @@ import context_ring_attention_blockwise_gb300 as cp
 O_TOL = 1e-2      # max-abs error on O (bf16 output from bf16 inputs, fp32 accumulation)
 LSE_TOL = 1e-3    # max-abs error on lse (fp32)
 
+# Per test: how many O elements the bf16-spacing allowance below covers, and how many of them
+# needed it (error above O_TOL). Printed at the end of the session.
+RELAXATION_LOG: list = []
+
+
+def bf16_half_ulp(a: np.ndarray) -> np.ndarray:
+    """Half the spacing of the bf16 grid at |a| (8 significant bits: spacing 2^(e - 7) in [2^e, 2^(e+1)))."""
+    a = np.abs(a)
+    return np.exp2(np.floor(np.log2(np.maximum(a, 1e-30))) - 8)
+
 
 def o_tolerance(ref_o: np.ndarray) -> np.ndarray:
-    """Per-element bound on |O - O_exact|: 1e-2, except where |O_exact| >= 4. There the spacing
-    of the bf16 grid (2^-5 in [4, 8)) is wider than twice 1e-2, so no bf16 value need lie within
-    1e-2 of the exact one; such elements must instead be within one bf16 ulp of it."""
+    """Per-element bound on |O - O_exact|: 1e-2, plus half a bf16 spacing where |O_exact| >= 4.
+
+    The kernel's fp32 result is held to the 1e-2 budget; it is then rounded to bf16 for output,
+    which moves it by at most half the bf16 spacing at its value. Below 4 that half spacing is at
+    most 2^-7 and the 1e-2 bound is kept as stated. From 4 on the half spacing (2^-6 in [4, 8))
+    exceeds 1e-2 / 2, so no bf16 value need lie within 1e-2 of the exact one; there the bound is
+    the budget plus the output rounding: 1e-2 + half a bf16 spacing at |O_exact|. (When rounding
+    crosses into the next binade it lands on the binade's edge, which lies within the 1e-2 budget
+    of the exact value, so the half spacing at |O_exact| is enough.)"""
     a = np.abs(ref_o)
-    ulp = np.exp2(np.floor(np.log2(np.maximum(a, 1e-30))) - 7)
-    return np.where(a >= 4.0, ulp, O_TOL)
+    return np.where(a >= 4.0, O_TOL + bf16_half_ulp(a), O_TOL)
 
 
 def to_device_bf16(bits: np.ndarray) -> torch.Tensor:
@@ -53,23 +68,43 @@ def run(q, k, v, n_cp, layout, causal=True, pos=None, scale=None, path="fused"):
 
 
 def compare(o, lse, ref_o, ref_lse, rows=None, what=""):
-    """Max-abs errors against the oracle; rows selects natural token ids of o/lse."""
+    """Max-abs errors against the oracle; rows selects natural token ids of o/lse. Works through the
+    tokens in chunks so that full-size comparisons stay within a few GB of host memory."""
     if rows is not None:
         o = o[:, rows]
         lse = lse[:, :, rows]
     assert o.shape == ref_o.shape and lse.shape == ref_lse.shape
-    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(lse), fin), f"{what}: -inf pattern of lse differs"
-    err = np.abs(o - ref_o)
-    eo = float(np.max(err)) if o.size else 0.0
     el = float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0
-    over = err > o_tolerance(ref_o)
-    if over.any() or el > LSE_TOL:
-        idx = np.unravel_index(int(np.argmax(err - o_tolerance(ref_o))), err.shape)
+    eo, n_over, n_relaxed, n_needed = 0.0, 0, 0, 0
+    worst = (-np.inf, None)
+    T = o.shape[1]
+    step = max(1, (1 << 24) // max(1, o.shape[0] * int(np.prod(o.shape[2:]))))
+    for t0 in range(0, T, step):
+        oc = np.asarray(o[:, t0:t0 + step], dtype=np.float64)
+        rc = ref_o[:, t0:t0 + step]
+        assert np.all(np.isfinite(oc)), f"{what}: non-finite O"
+        err = np.abs(oc - rc)
+        tol = o_tolerance(rc)
+        if err.size:
+            eo = max(eo, float(err.max()))
+            excess = err - tol
+            k = int(np.argmax(excess))
+            if excess.flat[k] > worst[0]:
+                idx = np.unravel_index(k, err.shape)
+                worst = (float(excess.flat[k]), (idx[0], idx[1] + t0) + tuple(idx[2:]), float(oc[idx]), float(rc[idx]))
+        n_over += int((err > tol).sum())
+        big = np.abs(rc) >= 4.0
+        n_relaxed += int(big.sum())
+        n_needed += int((big & (err > O_TOL)).sum())
+    RELAXATION_LOG.append((what, int(o.size), n_relaxed, n_needed))
+    if n_over or el > LSE_TOL:
         le = np.where(fin, np.abs(np.where(fin, lse, 0) - np.where(fin, ref_lse, 0)), 0)
         li = np.unravel_index(int(np.argmax(le)), le.shape)
-        what += f" [worst lse at (b, head, row) {li}: got {lse[li]:.6f}, exact {ref_lse[li]:.6f}]"
-        raise AssertionError(f"{what}: max|dO| = {eo:.3e} ({int(over.sum())} elements over tolerance; worst at "
-                             f"{idx}: got {o[idx]:.6f}, exact {ref_o[idx]:.6f}), max|dlse| = {el:.3e} (tol {LSE_TOL})")
+        msg = f" [worst lse at (b, head, row) {li}: got {lse[li]:.6f}, exact {ref_lse[li]:.6f}]"
+        raise AssertionError(f"{what}{msg}: max|dO| = {eo:.3e} ({n_over} elements over tolerance; worst at "
+                             f"{worst[1]}: got {worst[2]:.6f}, exact {worst[3]:.6f}), max|dlse| = {el:.3e} "
+                             f"(tol {LSE_TOL}); {n_relaxed} of {o.size} elements have |O_exact| >= 4 and take "
+                             f"the bound 1e-2 + half a bf16 spacing, {n_needed} of them with an error above 1e-2")
     return eo, el

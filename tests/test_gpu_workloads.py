@@ -1,6 +1,7 @@
 """The five benchmark workloads at full size on the GPU, in the launch configuration the bench
-times: sampled rows against the fp64 oracle (all heads, every batch element), and the kernel's
-block-skip decisions bit-exact against the plan."""
+times, against the fp64 oracle (all heads, every batch element): every row of the tiny and the
+16K GQA workloads, 4096 rows of the 32K non-causal one (every chunk boundary among them), and 256
+rows of the two 128K ones; and the kernel's block-skip decisions bit-exact against the plan."""
 import numpy as np
 import pytest
 import torch
