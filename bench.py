@@ -224,15 +224,135 @@ def run_reference(args, w):
 
 
 def config_of(w, args):
+    if args.path == "ring":
+        par = (f"ring over {args.gpus} processes, {w.n_cp // args.gpus} ranks each" if args.gpus > 1
+               else "single GPU, one process holding all ranks")
+    else:
+        par = "replicas" if args.gpus > 1 else "single GPU"
     return {"workload": w.name, "B": w.B, "T": w.T, "h": w.h, "n_kv": w.n_kv, "d_k": w.d, "n_cp": w.n_cp,
             "layout": synth.LAYOUT_NAMES[args.layout], "causal": w.causal, "path": args.path,
             "l2": "inputs larger than L2 (no flush)" if w.T >= 65536 else "L2 flushed between steps",
-            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+            "parallelism": par}
 
 
 # ---------------------------------------------------------------------------------------------
 # The GPU arm
 # ---------------------------------------------------------------------------------------------
+
+def run_gpu_ring(args, w):
+    """The multi-process ring: process p (one per GPU) holds ranks p R .. p R + R - 1 of the n_cp
+    (R = n_cp / processes) and passes the block that crosses to the next process over NCCL; one
+    process holds the whole ring and passes blocks between its own ranks. The work is the whole
+    sequence's once, whatever the number of processes (strong scaling)."""
+    import torch
+    import context_ring_attention_blockwise_gb300 as cp
+    from context_ring_attention_blockwise_gb300 import _build
+    from context_ring_attention_blockwise_gb300.ring import NcclTransport, RingProcess, local_tokens
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if w.n_cp % world:
+        raise SystemExit(f"n_cp = {w.n_cp} is not a multiple of {world} processes")
+    _build.build()
+    dev = torch.device("cuda", local)
+    R = w.n_cp // world
+    toks = local_tokens(w.T, w.n_cp, args.layout, rank * R, R)
+    q_full, k_full, v_full = synth.make_qkv(w)
+    q_h, k_h, v_h = (np.ascontiguousarray(x[:, toks]) for x in (q_full, k_full, v_full))
+    del q_full, k_full, v_full
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = to_dev(q_h), to_dev(k_h), to_dev(v_h)
+    plan = cp.Plan(w.T, w.h, w.n_kv, w.d, w.n_cp, args.layout, w.causal)
+    ring = RingProcess(plan, w.B, rank=rank, world=world, transport=NcclTransport(rank, world) if world > 1 else None,
+                       device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.h, R * plan.T // w.n_cp), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+    for _ in range(args.warmup):
+        ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy)
+    torch.cuda.synchronize()
+    cp.check(plan, ring.backend.ws)
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    cp.check(plan, ring.backend.ws)
+    ms_per_step = reduce_max(a.elapsed_time(b) / args.steps, dist, dev)
+    value = flops_eff(w) / (ms_per_step * 1e-3) / 1e12
+
+    # end to end: this process's shard from pinned host memory and its outputs back, every step
+    qp, kp, vp = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q_h, k_h, v_h))
+    op = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lp = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 8))
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dist, dev)
+    peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    n_grp = plan.counts(w.B)  # host call; keeps the plan's counters in the line
+    uploads = -(-(R * ((w.T // w.n_cp + 127) // 128)) // 960)
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, args),
+            "frac_of_peak": value / world / peak_tf,
+            "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": value / world / peak_tf, "traffic": None,
+                         "kernel": "whole ring path (placement, n_cp steps of ring_attention_kernel, finalize)",
+                         "peak_kind": f"bf16 dense, sustained, {peak_src}",
+                         "peak_burst": float(peaks.get("bf16_tflops", 0.0))},
+            "e2e": {"value": flops_eff(w) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes),
+                    "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4)},
+            "ring": {"processes": world, "ranks_per_process": R,
+                     "kv_bytes_recv_per_rank": int(ring.counters.kv[0] // (args.warmup + args.steps + 1 + e2e_steps)),
+                     "kv_bytes_recv_per_rank_pages": int(n_grp["kv_bytes_recv"][0]),
+                     "transport": "NCCL send/recv" if world > 1 else "none (one process holds the ring)"},
+            # per step: the order upload, placement (pos_tiles, tile_suffix, permute), per ring step
+            # the tile counts and the attention kernel, and the write-back
+            "gpu_launches": (uploads + 3 + 2 * w.n_cp + 1) * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
 
 def run_gpu(args, w):
     import torch
@@ -627,7 +747,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.CONFIGS))
     ap.add_argument("--layout", default=None, help="contiguous|zigzag|striped (default: the workload's first)")
-    ap.add_argument("--path", choices=["fused", "ring"], default="fused")
+    ap.add_argument("--path", choices=["fused", "ring"], default="fused",
+                    help="fused: one persistent launch over every rank and step; ring: the ring across "
+                         "processes (one per GPU), each holding n_cp / processes ranks")
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per attention launch from ncu, if known")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
@@ -640,6 +762,8 @@ def main():
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.path == "ring":
+        return run_gpu_ring(args, w)
     return run_gpu(args, w)
 
 

@@ -30,6 +30,9 @@ SYMBOLS = [
     "cpattn_ulysses_plan", "cpattn_ulysses_workspace_size", "cpattn_ulysses_counts", "cpattn_ulysses_forward",
     "cpattn_backward_counts", "cpattn_backward_ring_workspace_size", "cpattn_backward_begin",
     "cpattn_backward_ring_step", "cpattn_backward_finalize",
+    "cpattn_allgather_workspace_size", "cpattn_allgather_counts", "cpattn_allgather_forward",
+    "cpattn_allgather_gather", "cpattn_allgather_attend",
+    "cpattn_dist_sizes", "cpattn_dist_begin", "cpattn_dist_step", "cpattn_dist_shift", "cpattn_dist_finalize",
 ]
 
 
@@ -86,6 +89,16 @@ def lib():
     L.cpattn_ulysses_workspace_size.argtypes = [_P, i, sz]
     L.cpattn_ulysses_counts.argtypes = [_P, i, _P]
     L.cpattn_ulysses_forward.argtypes = [_P, i, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_allgather_workspace_size.argtypes = [_P, i, sz]
+    L.cpattn_allgather_counts.argtypes = [_P, i, _P]
+    L.cpattn_allgather_forward.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_allgather_gather.argtypes = [_P, i, _P, ctypes.c_size_t, _P]
+    L.cpattn_allgather_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_dist_sizes.argtypes = [_P, i, i, sz, sz, sz, sz]
+    L.cpattn_dist_begin.argtypes = [_P, i, i, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
+    L.cpattn_dist_step.argtypes = [_P, i, i, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
+    L.cpattn_dist_shift.argtypes = [_P, i, i, _P, _P, ctypes.c_size_t, i, _P]
+    L.cpattn_dist_finalize.argtypes = [_P, i, i, i, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_last_error.restype = ctypes.c_char_p
     L.cpattn_last_error.argtypes = []
     L.cpattn_version.restype = ctypes.c_char_p
@@ -151,6 +164,27 @@ class Plan:
         _check(lib().cpattn_backward_ring_workspace_size(self._h, B, ctypes.byref(out)),
                "cpattn_backward_ring_workspace_size")
         return out.value
+
+    def allgather_workspace_size(self, B: int) -> int:
+        out = ctypes.c_size_t()
+        _check(lib().cpattn_allgather_workspace_size(self._h, B, ctypes.byref(out)), "cpattn_allgather_workspace_size")
+        return out.value
+
+    def allgather_counts(self, B: int = 1):
+        import numpy as np
+        recv = np.zeros(self.n_cp, dtype=np.int64)
+        _check(lib().cpattn_allgather_counts(self._h, B, recv.ctypes.data), "cpattn_allgather_counts")
+        return {"bytes_recv": recv}
+
+    def dist_sizes(self, B: int, R: int):
+        """Sizes of one process's part of a multi-process ring holding R ranks: (workspace bytes,
+        slot bytes, the four slot regions' offsets (K, V, positions, tiles), one rank's block bytes
+        in each region)."""
+        ws, slot = ctypes.c_size_t(), ctypes.c_size_t()
+        off, blk = (ctypes.c_size_t * 4)(), (ctypes.c_size_t * 4)()
+        _check(lib().cpattn_dist_sizes(self._h, B, R, ctypes.byref(ws), ctypes.byref(slot), off, blk),
+               "cpattn_dist_sizes")
+        return ws.value, slot.value, tuple(off), tuple(blk)
 
     def tile_shape(self):
         bq, bk = ctypes.c_int(), ctypes.c_int()
@@ -447,6 +481,60 @@ def ring_forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=N
         ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
     finalize(plan, B, ws, out, lse, stream=compute)
     return out, lse
+
+
+def allgather_forward(q, k, v, plan: Plan, pos=None, lo=None, scale: float | None = None, ws=None, out=None,
+                      lse=None, stream=None):
+    """cpattn_allgather_forward: the all-gather variant (every rank gathers the whole K and V, then
+    one attention pass for all ranks' queries). lo: optional per-query lower bound (document masks).
+    Arguments and results as forward()."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if lo is not None and (tuple(lo.shape) != (plan.T,) or lo.dtype != torch.int32):
+        raise ValueError("lo must be an int32 tensor of T entries")
+    if ws is None:
+        ws = alloc_workspace(plan.allgather_workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    _check(lib().cpattn_allgather_forward(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                          _dev_ptr(pos, "pos"), _dev_ptr(lo, "lo"), float(scale or 0.0),
+                                          _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"), ws.numel(),
+                                          _stream_ptr(stream)), "cpattn_allgather_forward")
+    return out, lse
+
+
+def allgather_gather(plan: Plan, B: int, ws, stream=None):
+    _check(lib().cpattn_allgather_gather(plan.handle, B, _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)),
+           "cpattn_allgather_gather")
+
+
+def allgather_attend(plan: Plan, B: int, ws, out, lse, scale: float | None = None, stream=None):
+    _check(lib().cpattn_allgather_attend(plan.handle, B, float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
+                                         _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_allgather_attend")
+
+
+def dist_begin(plan: Plan, B: int, rank0: int, R: int, q, k, v, ws, slot, pos=None, stream=None):
+    """cpattn_dist_begin: this process's R ranks' tokens (rank-major, each rank's local order)."""
+    _check(lib().cpattn_dist_begin(plan.handle, B, rank0, R, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
+                                   _dev_ptr(pos, "pos"), _dev_ptr(ws, "ws"), ws.numel(), _dev_ptr(slot, "slot"),
+                                   slot.numel(), _stream_ptr(stream)), "cpattn_dist_begin")
+
+
+def dist_step(plan: Plan, B: int, rank0: int, R: int, step: int, slot, ws, scale: float | None = None, stream=None):
+    _check(lib().cpattn_dist_step(plan.handle, B, rank0, R, step, float(scale or 0.0), _dev_ptr(slot, "slot"),
+                                  slot.numel(), _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_dist_step")
+
+
+def dist_shift(plan: Plan, B: int, R: int, src_slot, dst_slot, wrap: bool, stream=None):
+    _check(lib().cpattn_dist_shift(plan.handle, B, R, _dev_ptr(src_slot, "src_slot"), _dev_ptr(dst_slot, "dst_slot"),
+                                   dst_slot.numel(), int(bool(wrap)), _stream_ptr(stream)), "cpattn_dist_shift")
+
+
+def dist_finalize(plan: Plan, B: int, rank0: int, R: int, ws, out, lse, stream=None):
+    _check(lib().cpattn_dist_finalize(plan.handle, B, rank0, R, _dev_ptr(out, "o"), _dev_ptr(lse, "lse"),
+                                      _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_dist_finalize")
 
 
 def merge(o_parts, lse_parts, out=None, lse=None, stream=None):

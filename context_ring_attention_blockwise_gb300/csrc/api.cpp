@@ -796,6 +796,309 @@ cpattn_status_t cpattn_merge(int S, int64_t rows, int h, int d, const float* o_p
     return CPATTN_OK;
 }
 
+// ---- the all-gather variant ("What context parallelism communicates": all-gather the keys and
+// values so every rank holds the full K and V, then one ordinary attention pass for the local
+// queries; the gather is exposed, ahead of the kernel) -----------------------------------------
+
+namespace {
+
+cpattn_status_t check_gather_ws(const Plan& p, int B, const void* ws, size_t ws_bytes) {
+    if (cpattn_status_t s = reject_ulysses(p)) return s;
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+    const size_t need = cpattn::ws_layout(p, B).gather_end;
+    if (ws_bytes < need)
+        return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
+                                              std::to_string(ws_bytes));
+    if ((double)p.n_cp * p.n_cp * B * p.n_kv * (double)p.n > 2.0e9)
+        return fail(CPATTN_ERR_UNSUPPORTED, "gathered key/value rows beyond 2e9");
+    return CPATTN_OK;
+}
+
+// Every rank r receives the blocks of all other ranks: its gathered copy is the whole rank-major
+// K (and V) of the layout, which on one GPU is one device-to-device copy per rank and tensor.
+cpattn_status_t gather_kv(const Plan& p, int B, void* ws, cudaStream_t st) {
+    const cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    const size_t all = 2 * (size_t)B * p.T * p.n_kv * p.d;
+    for (int r = 0; r < p.n_cp; ++r)
+        for (int t = 0; t < 2; ++t) {
+            int e = cudaMemcpyAsync(at<char>(ws, t ? w.gV : w.gK) + r * all, at<char>(ws, t ? w.vL : w.kL), all,
+                                    cudaMemcpyDeviceToDevice, st);
+            if (e) return cuda_fail(e, "cudaMemcpyAsync(all-gather)");
+        }
+    return CPATTN_OK;
+}
+
+cpattn_status_t gather_attend(const Plan& p, int B, float scale, const int32_t* lo, void* o, float* lse, void* ws,
+                              cudaStream_t st) {
+    const cpattn::WsLayout w = cpattn::ws_layout(p, B);
+    cpattn::AttnLaunch a = attn_args(p, B, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.kv_k = at<char>(ws, w.gK); a.kv_v = at<char>(ws, w.gV);
+    a.kv_rank_rows = (int64_t)p.n_cp * B * p.n_kv * p.n;
+    a.kv_rows = (uint64_t)p.n_cp * a.kv_rank_rows;
+    a.o = o; a.lse = lse;
+    if (lo) { a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); }
+    std::string why;
+    int e = launch_attn(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+}  // namespace
+
+cpattn_status_t cpattn_allgather_workspace_size(cpattn_plan_t plan, int B, size_t* bytes) {
+    Plan* p = as_plan(plan);
+    if (!p || !bytes || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, bytes and B > 0 required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
+    *bytes = cpattn::ws_layout(*p, B).gather_end;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_allgather_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv) {
+    Plan* p = as_plan(plan);
+    if (!p || B <= 0 || !bytes_recv) return fail(CPATTN_ERR_INVALID, "plan, B > 0 and bytes_recv required");
+    if (cpattn_status_t s = reject_ulysses(*p)) return s;
+    // the other n_cp - 1 ranks' K and V blocks, 2 bytes a number
+    for (int r = 0; r < p->n_cp; ++r)
+        bytes_recv[r] = (int64_t)(p->n_cp - 1) * 2 * 2 * B * p->n * p->n_kv * p->d;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_allgather_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                         const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse,
+                                         void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    if (lo) {
+        if (!p->causal) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query needs a causal plan");
+        if (p->n_qt > 65535) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query supports up to 65535 tiles per rank");
+        if (!aligned16(lo)) return fail(CPATTN_ERR_INVALID, "lo must be 16-byte aligned");
+    }
+    if ((s = check_gather_ws(*p, B, ws, ws_bytes))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, lo))) return s;
+    if ((s = gather_kv(*p, B, ws, st))) return s;
+    return gather_attend(*p, B, scale, lo, o, lse, ws, st);
+}
+
+cpattn_status_t cpattn_allgather_gather(cpattn_plan_t plan, int B, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    cpattn_status_t s = check_gather_ws(*p, B, ws, ws_bytes);
+    if (s) return s;
+    return gather_kv(*p, B, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws,
+                                        size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_gather_ws(*p, B, ws, ws_bytes);
+    if (s) return s;
+    return gather_attend(*p, B, scale, nullptr, o, lse, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---- one process of a multi-process ring ("Pass them around a ring": each rank computes against
+// the block it holds while it sends that block to its right neighbour and receives the next one
+// from its left). A process holds R consecutive ranks rank0 .. rank0 + R - 1; the library does
+// the per-step attention of its ranks and the moves between its own ranks' slots, and the caller
+// moves the one block that crosses to the next process. ----------------------------------------
+
+namespace {
+
+cpattn_status_t check_dist(const Plan& p, int B, int rank0, int R, const void* ws, size_t ws_bytes, const void* slot,
+                           size_t slot_bytes) {
+    if (cpattn_status_t s = reject_ulysses(p)) return s;
+    if (B <= 0) return fail(CPATTN_ERR_INVALID, "B must be positive");
+    if (R <= 0 || rank0 < 0 || rank0 + R > p.n_cp)
+        return fail(CPATTN_ERR_INVALID, "ranks rank0 .. rank0 + R - 1 must lie in 0 .. n_cp - 1");
+    if ((double)B * R * (double)p.n * p.h > 2.0e9) return fail(CPATTN_ERR_UNSUPPORTED, "B*R*n*h beyond 2e9 rows");
+    const cpattn::DistLayout w = cpattn::dist_layout(p, B, R);
+    if (ws) {
+        if ((reinterpret_cast<uintptr_t>(ws) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "workspace must be 1024-byte aligned");
+        if (ws_bytes < w.ws_end)
+            return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(w.ws_end) + " bytes, got " +
+                                                  std::to_string(ws_bytes));
+    }
+    if (slot) {
+        if ((reinterpret_cast<uintptr_t>(slot) & 1023u) != 0) return fail(CPATTN_ERR_WORKSPACE, "slot must be 1024-byte aligned");
+        if (slot_bytes < w.slot_end)
+            return fail(CPATTN_ERR_WORKSPACE, "slot too small: need " + std::to_string(w.slot_end) + " bytes, got " +
+                                                  std::to_string(slot_bytes));
+    }
+    return CPATTN_OK;
+}
+
+cpattn_status_t check_dist_state(const Plan& p, int B, int rank0, int R) {
+    if (p.dist_next < 0) return fail(CPATTN_ERR_INVALID, "cpattn_dist_begin must come first");
+    if (B != p.dist_B || rank0 != p.dist_rank0 || R != p.dist_R)
+        return fail(CPATTN_ERR_INVALID, "B, rank0 and R differ from what cpattn_dist_begin placed");
+    return CPATTN_OK;
+}
+
+}  // namespace
+
+cpattn_status_t cpattn_dist_sizes(cpattn_plan_t plan, int B, int R, size_t* ws_bytes, size_t* slot_bytes,
+                                  size_t* region_offset, size_t* block_bytes) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (cpattn_status_t s = check_dist(*p, B, 0, R, nullptr, 0, nullptr, 0)) return s;
+    const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
+    if (ws_bytes) *ws_bytes = w.ws_end;
+    if (slot_bytes) *slot_bytes = w.slot_end;
+    if (region_offset) {
+        region_offset[0] = w.slot_k; region_offset[1] = w.slot_v;
+        region_offset[2] = w.slot_pos; region_offset[3] = w.slot_tile;
+    }
+    if (block_bytes) {
+        block_bytes[0] = w.blk_k; block_bytes[1] = w.blk_v;
+        block_bytes[2] = w.blk_pos; block_bytes[3] = w.blk_tile;
+    }
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, const void* q, const void* k,
+                                  const void* v, const int32_t* pos, void* ws, size_t ws_bytes, void* slot,
+                                  size_t slot_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!ws || !slot) return fail(CPATTN_ERR_WORKSPACE, "workspace and slot must be non-NULL");
+    cpattn_status_t s = check_dist(*p, B, rank0, R, ws, ws_bytes, slot, slot_bytes);
+    if (s) return s;
+    if (!q || !k || !v) return fail(CPATTN_ERR_INVALID, "q, k and v must be non-NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (pos && !aligned16(pos)))
+        return fail(CPATTN_ERR_INVALID, "q, k, v and pos must be 16-byte aligned");
+    const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
+    if (!e) e = cudaMemsetAsync(at<char>(ws, w.counts), 0, w.sched + sizeof(uint32_t) * (1 + (size_t)R) - w.counts, st);
+    if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
+    // the plan's longest-first order of row groups, restricted to this process's ranks
+    std::vector<int32_t> order;
+    order.reserve((size_t)R * p->n_grp);
+    for (int32_t rg : p->order) {
+        const int r = rg / p->n_grp;
+        if (r >= rank0 && r < rank0 + R) order.push_back((r - rank0) * p->n_grp + rg % p->n_grp);
+    }
+    if ((e = cpattn::launch_upload_i32(at<int32_t>(ws, w.order), order.data(), (int64_t)order.size(), st)))
+        return cuda_fail(e, "order upload kernel");
+    // the process's tokens are rank-major in each rank's local order: placement is the identity
+    // over R ranks, and default positions are the tokens' natural positions in the whole sequence
+    cpattn::PermuteArgs a{};
+    a.B = B; a.T = (int64_t)R * p->n; a.n = p->n; a.m = 0; a.h = p->h; a.n_kv = p->n_kv; a.d = p->d; a.n_cp = R;
+    a.layout = CPATTN_CONTIGUOUS; a.n_qt = p->n_qt;
+    a.q = q; a.k = k; a.v = v; a.pos = pos;
+    a.qL = at<char>(ws, w.qL); a.kL = at<char>(slot, w.slot_k); a.vL = at<char>(slot, w.slot_v);
+    a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    a.dflt_ncp = p->n_cp; a.dflt_layout = p->layout; a.dflt_rank0 = rank0; a.dflt_m = p->m;
+    if ((e = cpattn::launch_permute(a, st))) return cuda_fail(e, "permute kernel");
+    // each block carries its position tables with it around the ring
+    e = cudaMemcpyAsync(at<char>(slot, w.slot_pos), at<char>(ws, w.posL), w.blk_pos * R, cudaMemcpyDeviceToDevice, st);
+    if (!e)
+        e = cudaMemcpyAsync(at<char>(slot, w.slot_tile), at<char>(ws, w.tile_mm), w.blk_tile * R,
+                            cudaMemcpyDeviceToDevice, st);
+    if (e) return cuda_fail(e, "cudaMemcpyAsync(position tables)");
+    p->dist_next = 0; p->dist_B = B; p->dist_rank0 = rank0; p->dist_R = R;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
+                                 const void* slot, size_t slot_bytes, void* ws, size_t ws_bytes,
+                                 cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!ws || !slot) return fail(CPATTN_ERR_WORKSPACE, "workspace and slot must be non-NULL");
+    cpattn_status_t s = check_dist(*p, B, rank0, R, ws, ws_bytes, slot, slot_bytes);
+    if (s) return s;
+    if ((s = check_dist_state(*p, B, rank0, R))) return s;
+    if (step != p->dist_next)
+        return fail(CPATTN_ERR_INVALID, "ring steps must follow cpattn_dist_begin in order 0..n_cp-1 (expected step " +
+                                            std::to_string(p->dist_next) + ")");
+    const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
+    cpattn::AttnLaunch a{};
+    a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.n_kv = p->n_kv; a.d = p->d; a.n_cp = R;
+    a.layout = p->layout; a.causal = p->causal; a.n_qt = p->n_qt; a.pair_heads = p->pair_heads; a.n_grp = p->n_grp;
+    a.sched = at<uint32_t>(ws, w.sched);
+    a.unit_tiles = at<int32_t>(ws, w.unit_tiles);
+    a.walk_tab = at<int32_t>(ws, w.walk_tab);
+    a.walk_nz = at<unsigned long long>(ws, w.walk_nz);
+    a.scale_log2 = resolve_scale(*p, scale);
+    // every local rank attends to the one block it holds: a one-step walk in which the block read
+    // is the holder's own slot entry, with the position tables that travelled with it
+    a.fused = 0; a.step = 0; a.first = step == 0 ? 1 : 0;
+    a.qL = at<char>(ws, w.qL);
+    a.kv_k = const_cast<char*>(static_cast<const char*>(slot) + w.slot_k);
+    a.kv_v = const_cast<char*>(static_cast<const char*>(slot) + w.slot_v);
+    a.kv_by_holder = 1;
+    a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    a.kposL = reinterpret_cast<const int32_t*>(static_cast<const char*>(slot) + w.slot_pos);
+    a.ktile_mm = reinterpret_cast<const int32_t*>(static_cast<const char*>(slot) + w.slot_tile);
+    a.order = at<int32_t>(ws, w.order);
+    a.counts = at<unsigned long long>(ws, w.counts);
+    a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
+    a.header = at<uint32_t>(ws, w.header);
+    a.timeout_ns = 2000000000ull;
+    std::string why;
+    int e = launch_attn(a, reinterpret_cast<cudaStream_t>(stream), &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    p->dist_next = step + 1;
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_dist_shift(cpattn_plan_t plan, int B, int R, const void* src_slot, void* dst_slot,
+                                  size_t slot_bytes, int wrap, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!src_slot || !dst_slot) return fail(CPATTN_ERR_INVALID, "slots must be non-NULL");
+    if (src_slot == dst_slot) return fail(CPATTN_ERR_INVALID, "the two slots must differ");
+    cpattn_status_t s = check_dist(*p, B, 0, R, nullptr, 0, dst_slot, slot_bytes);
+    if (s) return s;
+    if ((s = check_dist(*p, B, 0, R, nullptr, 0, src_slot, slot_bytes))) return s;
+    const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t off[4] = {w.slot_k, w.slot_v, w.slot_pos, w.slot_tile};
+    const size_t blk[4] = {w.blk_k, w.blk_v, w.blk_pos, w.blk_tile};
+    const char* src = static_cast<const char*>(src_slot);
+    char* dst = static_cast<char*>(dst_slot);
+    for (int x = 0; x < 4; ++x) {
+        int e = 0;
+        // local rank i + 1 receives the block local rank i holds now
+        if (R > 1) e = cudaMemcpyAsync(dst + off[x] + blk[x], src + off[x], blk[x] * (R - 1), cudaMemcpyDeviceToDevice, st);
+        // a process holding the whole ring passes its last block to its own first rank
+        if (!e && wrap)
+            e = cudaMemcpyAsync(dst + off[x], src + off[x] + blk[x] * (R - 1), blk[x], cudaMemcpyDeviceToDevice, st);
+        if (e) return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
+    }
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_dist_finalize(cpattn_plan_t plan, int B, int rank0, int R, void* o, float* lse, void* ws,
+                                     size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!ws) return fail(CPATTN_ERR_WORKSPACE, "workspace must be non-NULL");
+    cpattn_status_t s = check_dist(*p, B, rank0, R, ws, ws_bytes, nullptr, 0);
+    if (s) return s;
+    if ((s = check_dist_state(*p, B, rank0, R))) return s;
+    if (p->dist_next != p->n_cp) return fail(CPATTN_ERR_INVALID, "finalize needs all n_cp ring steps first");
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
+    cpattn::FinalizeArgs a{};
+    a.B = B; a.T = (int64_t)R * p->n; a.n = p->n; a.m = 0; a.h = p->h; a.d = p->d; a.n_cp = R;
+    a.layout = CPATTN_CONTIGUOUS;
+    a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run); a.o = o; a.lse = lse;
+    int e = cpattn::launch_finalize(a, stream);
+    if (e) return cuda_fail(e, "finalize kernel");
+    p->dist_next = -1;
+    return CPATTN_OK;
+}
+
 cpattn_status_t cpattn_tile_counts(cpattn_plan_t plan, int B, const void* ws, int64_t* full, int64_t* diag) {
     Plan* p = as_plan(plan);
     if (!p || !ws || B <= 0) return fail(CPATTN_ERR_INVALID, "plan, ws and B > 0 required");

@@ -70,6 +70,8 @@ struct Params {
     float scale_log2;
     const int32_t* posL;
     const int4* tile_mm;
+    const int32_t* kposL;   // key-side positions [.][n] and tiles [.][n_qt], indexed by the rank whose
+    const int4* ktile_mm;   // block is read (posL / tile_mm except in a multi-process ring)
     const int32_t* order;
     const int32_t* loL;    // [n_cp][n] lowest visible key position per query, or NULL
     const int4* tile_lo;   // [n_cp][n_qt] (min, max) of loL over a query tile, or NULL
@@ -86,6 +88,8 @@ struct Params {
     float* lse_run;
     uint32_t* header;
     uint64_t timeout_ns;
+    int first;              // ring step: write the running state instead of merging into it
+    int64_t kv_rank_rows;   // all-gather: K/V rows between consecutive ranks' gathered copies (else 0)
 };
 
 template <int D>
@@ -300,7 +304,7 @@ struct TileWalk {
                 if (src < 0) src += P.n_cp;
             }
             const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
-            const int4 t4 = __ldg(P.tile_mm + src * P.n_qt + kt);
+            const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
             cls0 = (t4.x > qmax0 || t4.y < lmin0) ? CPATTN_TILE_SKIP
                    : (t4.y > qmin0 || t4.x < lmax0) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
             cls1 = (t4.x > qmax1 || t4.y < lmin1) ? CPATTN_TILE_SKIP
@@ -326,7 +330,7 @@ struct TileWalk {
                 // non-decreasing running maximum (.w); skip the block, or start at its first tile
                 // whose running maximum reaches the smallest bound.
                 const int lmin = min(lmin0, lmin1);
-                const int* mm = reinterpret_cast<const int*>(P.tile_mm + src * P.n_qt);
+                const int* mm = reinterpret_cast<const int*>(P.ktile_mm + src * P.n_qt);
                 if (__ldg(mm + 4 * (P.n_qt - 1) + 3) < lmin) {
                     kt = P.n_qt - 1;
                     continue;
@@ -345,7 +349,7 @@ struct TileWalk {
                 mask0 = mask1 = short_tile;
                 return true;
             }
-            const int4 t4 = __ldg(P.tile_mm + src * P.n_qt + kt);
+            const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
             if (t4.z > qmax) {           // this tile and every later one of the block: skipped
                 kt = P.n_qt - 1;
                 continue;
@@ -404,7 +408,8 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
         int j = 0, prev_row = 0;
         while (w.next()) {
             const int holder = P.kv_by_holder ? U.r : w.src;
-            const int krow = (int)((((int64_t)holder * P.B + U.b) * P.n_kv + U.kvh) * P.n + (int64_t)w.kt * 128);
+            const int krow = (int)((int64_t)U.r * P.kv_rank_rows +
+                                   (((int64_t)holder * P.B + U.b) * P.n_kv + U.kvh) * P.n + (int64_t)w.kt * 128);
             if (j == 0) {
                 if (nq >= 1 && !wait(bars.q_empty(), (nq - 1) & 1, kSiteQEmpty)) { ok = false; break; }
                 mbar_arrive_expect_tx(bars.q_full(), 2 * C::Q_BYTES);
@@ -605,7 +610,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                     int kp[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.posL + kbase + c0 + c) : INT_MIN;
+                        kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.kposL + kbase + c0 + c) : INT_MIN;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
                         const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos && (!LB || kp[c] >= qlo);
@@ -685,7 +690,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         }
         flush();
         if (!ok) break;
-        if (j == 0 && !P.fused && P.step > 0) continue;    // nothing visible at this step
+        if (j == 0 && !P.fused && !P.first) continue;     // nothing visible at this step
         if (j > 0) {
             ok = __all_sync(0xffffffffu, wait(bars.pv_done(wg), (ntile - 1) & 1, kSitePvDone));
             if (!ok) break;
@@ -698,7 +703,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         float4* orun = nullptr;               // ring step: fp32 running row in layout order
         int64_t base = 0;
         float wa = 0.f, wb = inv_l, L = lse_v;
-        const bool first = (P.step == 0);
+        const bool first = P.first != 0;
         if (P.fused) {
             int64_t tn;
             if (P.layout == CPATTN_CONTIGUOUS) tn = (int64_t)U.r * P.n + jl;
@@ -921,7 +926,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     CUtensorMap tq, tk, tv;
-    const uint64_t qrows = (uint64_t)a.n_cp * a.B * a.h * a.n, kvrows = (uint64_t)a.n_cp * a.B * a.n_kv * a.n;
+    const uint64_t qrows = (uint64_t)a.n_cp * a.B * a.h * a.n;
+    const uint64_t kvrows = a.kv_rows ? a.kv_rows : (uint64_t)a.n_cp * a.B * a.n_kv * a.n;
     if (!make_map(&tq, a.qL, qrows, D) || !make_map(&tk, a.kv_k, kvrows, D) || !make_map(&tv, a.kv_v, kvrows, D)) {
         *why = "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor shape)";
         return (int)cudaErrorInvalidValue;
@@ -932,6 +938,10 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.fused = a.fused; P.step = a.step; P.kv_by_holder = a.kv_by_holder; P.layout = a.layout;
     P.n = a.n; P.m = a.m; P.T = a.T; P.scale_log2 = a.scale_log2;
     P.posL = a.posL; P.tile_mm = reinterpret_cast<const int4*>(a.tile_mm); P.order = a.order;
+    P.kposL = a.kposL ? a.kposL : a.posL;
+    P.ktile_mm = reinterpret_cast<const int4*>(a.ktile_mm ? a.ktile_mm : a.tile_mm);
+    P.first = a.first >= 0 ? a.first : (a.step == 0);
+    P.kv_rank_rows = a.kv_rank_rows;
     P.unit_tiles = a.unit_tiles;
     P.walk_tab = a.walk_tab;
     P.walk_nz = a.walk_nz;

@@ -44,6 +44,9 @@ struct WsLayout {
     size_t o_run = 0;       // fp32 [n_cp][B][h][n][d] running output (normalised)
     size_t lse_run = 0;     // fp32 [n_cp][B][h][n] running lse
     size_t ring_end = 0;
+    // all-gather variant (after fwd_end, overlapping the ring-step regions): every rank's gathered
+    // copy of the whole K and V, [n_cp holder][n_cp source][B][n_kv][n][d] bf16 each
+    size_t gK = 0, gV = 0, gather_end = 0;
     // backward (after fwd_end; the ring-step regions are not used by the backward)
     size_t doL = 0;         // bf16 [n_cp][B][h][n][d] output gradient in layout order
     size_t lse2 = 0;        // fp32 [n_cp][B][h][n_qt * 128] -lse * log2(e) of the forward (padding 0)
@@ -86,6 +89,8 @@ struct Plan {
     CUevent_st* bev_circ[2] = {nullptr, nullptr};
     CUevent_st* bev_start = nullptr;
     int next_bstep = -1;            // step expected next on the backward ring path (-1: begin first)
+    // multi-process ring (cpattn_dist_*): the step expected next and what cpattn_dist_begin placed
+    int dist_next = -1, dist_B = 0, dist_rank0 = 0, dist_R = 0;
     int bring_B = 0;                // batch size cpattn_backward_begin placed
     // page-locked copy of order, order_q, order_kv (created on first use): an upload from
     // pageable memory may block the calling thread until the stream drains
@@ -113,6 +118,16 @@ struct PerDeviceOnce {
 };
 
 WsLayout ws_layout(const Plan& p, int B);
+
+// One process of a multi-process ring holds R consecutive ranks: its workspace (query side and
+// running state) and its key/value stage slot (the blocks it holds, with their position tables).
+struct DistLayout {
+    size_t header = 0, posL = 0, tile_mm = 0, order = 0, counts = 0, sched = 0, unit_tiles = 0, walk_tab = 0,
+           walk_nz = 0, qL = 0, o_run = 0, lse_run = 0, ws_end = 0;
+    size_t slot_k = 0, slot_v = 0, slot_pos = 0, slot_tile = 0, slot_end = 0;   // offsets in a slot
+    size_t blk_k = 0, blk_v = 0, blk_pos = 0, blk_tile = 0;                     // one rank's block, bytes
+};
+DistLayout dist_layout(const Plan& p, int B, int R);
 void set_last_error(const std::string& msg);
 int64_t token_of(const Plan& p, int r, int64_t j);   // natural token of (rank, local index)
 
@@ -122,6 +137,11 @@ struct PermuteArgs {
     const void* q; const void* k; const void* v; const int32_t* pos;
     void* qL; void* kL; void* vL; int32_t* posL; int32_t* tile_mm;
     const int32_t* lo; int32_t* loL; int32_t* tile_lo;   // optional per-query lower bound (NULL: none)
+    // With pos NULL and dflt_ncp > 0, the position of (rank r, local index j) is its natural token
+    // under a plan of dflt_ncp ranks and layout dflt_layout, for rank dflt_rank0 + r (the tokens
+    // one process of a multi-process ring holds); otherwise it is the natural index here.
+    int dflt_ncp = 0, dflt_layout = 0, dflt_rank0 = 0;
+    int64_t dflt_m = 0;
 };
 int launch_permute(const PermuteArgs& a, void* stream);
 
@@ -143,6 +163,12 @@ struct AttnLaunch {
     float* o_run; float* lse_run;   // ring-step running state
     uint32_t* header;
     uint64_t timeout_ns;
+    // Key-side position tables when they are not posL / tile_mm (indexed like them by the rank
+    // whose block is read): the blocks held by one process of a multi-process ring carry their own.
+    const int32_t* kposL = nullptr; const int32_t* ktile_mm = nullptr;
+    int first = -1;            // ring step: write (1) or merge into (0) the running state; -1: step == 0
+    int64_t kv_rank_rows = 0;  // all-gather: K/V rows between the gathered copies of consecutive ranks
+    uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
 };
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why);
 

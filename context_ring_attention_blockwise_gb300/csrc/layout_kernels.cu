@@ -42,16 +42,23 @@ __device__ __forceinline__ int64_t token_of_dev(int layout, int r, int64_t j, in
 // One 128-thread block per (rank, tile): position ids in layout order and their min/max.
 // With a lower-bound array (document masks) the block also writes each token's bound in layout
 // order and the min/max bound of the tile.
+struct DefaultPos {
+    int n_cp, layout, rank0;   // n_cp == 0: a token's default position is its natural index here
+    int64_t m;
+};
+
 __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restrict__ pos, int32_t* __restrict__ posL,
                                                         int4* __restrict__ tile_mm, const int32_t* __restrict__ lob,
                                                         int32_t* __restrict__ loL, int4* __restrict__ tile_lo,
-                                                        int64_t n, int64_t m, int n_cp, int layout, int n_qt) {
+                                                        int64_t n, int64_t m, int n_cp, int layout, int n_qt,
+                                                        DefaultPos dp) {
     const int r = blockIdx.x / n_qt, tile = blockIdx.x % n_qt;
     const int64_t j = (int64_t)tile * kBlockQ + threadIdx.x;
     int lo = INT_MAX, hi = INT_MIN, blo = INT_MAX, bhi = INT_MIN;
     if (j < n) {
         int64_t t = token_of_dev(layout, r, j, n, m, n_cp);
-        int pv = pos ? pos[t] : (int)t;
+        const int dflt = dp.n_cp > 0 ? (int)token_of_dev(dp.layout, dp.rank0 + r, j, n, dp.m, dp.n_cp) : (int)t;
+        int pv = pos ? pos[t] : dflt;
         posL[(int64_t)r * n + j] = pv;
         lo = hi = pv;
         if (lob) {
@@ -431,9 +438,10 @@ int launch_ulysses_merge(const UlyssesArgs& a, void* stream) {
 
 int launch_permute(const PermuteArgs& a, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const DefaultPos dp{a.dflt_ncp, a.dflt_layout, a.dflt_rank0, a.dflt_m};
     pos_tiles_kernel<<<a.n_cp * a.n_qt, 128, 0, st>>>(a.pos, a.posL, reinterpret_cast<int4*>(a.tile_mm), a.lo, a.loL,
                                                       reinterpret_cast<int4*>(a.tile_lo), a.n, a.m, a.n_cp, a.layout,
-                                                      a.n_qt);
+                                                      a.n_qt, dp);
     int e = (int)cudaGetLastError();
     if (e) return e;
     tile_suffix_kernel<<<(a.n_cp + 127) / 128, 128, 0, st>>>(reinterpret_cast<int4*>(a.tile_mm), a.n_cp, a.n_qt);

@@ -51,6 +51,10 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.o_run = take(4 * (size_t)B * T * p.h * d);
     w.lse_run = take(4 * (size_t)B * T * p.h);
     w.ring_end = off;
+    off = w.fwd_end;
+    w.gK = take(2 * (size_t)p.n_cp * B * T * p.n_kv * d);
+    w.gV = take(2 * (size_t)p.n_cp * B * T * p.n_kv * d);
+    w.gather_end = off;
     // the backward reuses the forward regions and appends its own after them
     off = w.fwd_end;
     const size_t padded = (size_t)p.n_cp * B * p.h * (size_t)p.n_qt * 128;
@@ -71,6 +75,36 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.contribV = take(4 * (size_t)B * T * p.n_kv * d);
     w.dq_run = take(4 * (size_t)B * T * p.h * d);
     w.bring_end = off;
+    return w;
+}
+
+DistLayout dist_layout(const Plan& p, int B, int R) {
+    DistLayout w;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 1024); return at; };
+    const size_t n = (size_t)p.n, d = (size_t)p.d, nq = (size_t)p.n_qt, ng = (size_t)p.n_grp;
+    w.header = take(sizeof(uint32_t) * kHeaderWords);
+    w.posL = take(sizeof(int32_t) * R * n);
+    w.tile_mm = take(sizeof(int32_t) * 4 * R * nq);
+    w.order = take(sizeof(int32_t) * R * ng);
+    w.counts = take(sizeof(uint64_t) * 2 * R * R);
+    w.sched = take(sizeof(uint32_t) * (1 + (size_t)R));
+    w.unit_tiles = take(sizeof(int32_t) * R * ng);
+    w.walk_tab = take(sizeof(int32_t) * R * ng);
+    w.walk_nz = take(sizeof(uint64_t) * R * ng);
+    w.qL = take(2 * (size_t)B * R * n * p.h * d);
+    w.o_run = take(4 * (size_t)B * R * n * p.h * d);
+    w.lse_run = take(4 * (size_t)B * R * n * p.h);
+    w.ws_end = off;
+    w.blk_k = w.blk_v = 2 * (size_t)B * n * p.n_kv * d;
+    w.blk_pos = sizeof(int32_t) * n;
+    w.blk_tile = sizeof(int32_t) * 4 * nq;
+    off = 0;
+    w.slot_k = take(w.blk_k * R);
+    w.slot_v = take(w.blk_v * R);
+    w.slot_pos = take(w.blk_pos * R);
+    w.slot_tile = take(w.blk_tile * R);
+    w.slot_end = off;
     return w;
 }
 

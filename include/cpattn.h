@@ -261,6 +261,79 @@ cpattn_status_t cpattn_ulysses_forward(cpattn_plan_t plan, int B, const void* q,
                                        const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                                        cpattn_stream_t stream);
 
+/* The all-gather variant ([CEX] "Splitting the sequence, and the one layer that objects": gather
+ * the keys and values so that every rank holds the full K and V, then compute attention for the
+ * local queries; [CEX] "What context parallelism communicates": the all-gather moves every block
+ * before the attention kernel runs, so its time is exposed, and it works with one ordinary
+ * attention kernel). On one GPU every virtual rank r gets its own gathered copy of the whole K and
+ * V (rank-major layout order; [n_cp][n_cp][B][n_kv][n][d_k] bf16 in the workspace) by device-to-
+ * device copies, and one attention launch then computes every rank's queries, each rank reading
+ * only its own copy. The result equals cpattn_forward's (same arithmetic in the same order).
+ *   cpattn_allgather_workspace_size: the forward workspace plus the gathered copies
+ *     (2 n_cp times the bf16 K and V of the batch).
+ *   cpattn_allgather_forward: placement, the gather, the attention; arguments as
+ *     cpattn_forward_masked with lo optional (NULL: causal or non-causal as the plan says; else the
+ *     per-query lower bound of cpattn_forward_masked, which needs a causal plan).
+ *   cpattn_allgather_gather / cpattn_allgather_attend: the last two phases alone, on a workspace
+ *     cpattn_permute has filled (lets a caller time the exposed gather beside the attention).
+ *   cpattn_allgather_counts: bytes_recv [n_cp] (host, written), the bytes rank r receives in the
+ *     gather: the other n_cp - 1 ranks' K and V blocks, 4 B n d_kv (n_cp - 1) with d_kv = n_kv d_k,
+ *     the same volume as the ring ([CEX] "What context parallelism communicates": "Both come to").
+ * Device pointers 16-byte aligned, the workspace 1024-byte aligned; asynchronous on `stream`;
+ * device-side timeouts are read by cpattn_check(plan, ws). */
+cpattn_status_t cpattn_allgather_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
+cpattn_status_t cpattn_allgather_counts(cpattn_plan_t plan, int B, int64_t* bytes_recv);
+cpattn_status_t cpattn_allgather_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                         const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse,
+                                         void* ws, size_t ws_bytes, cpattn_stream_t stream);
+cpattn_status_t cpattn_allgather_gather(cpattn_plan_t plan, int B, void* ws, size_t ws_bytes, cpattn_stream_t stream);
+cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws,
+                                        size_t ws_bytes, cpattn_stream_t stream);
+
+/* One process of a ring that spans processes (one process per GPU; [CEX] "Pass them around a
+ * ring": each rank computes its queries against the key/value block it holds while it sends that
+ * block to its right neighbour and receives the next from its left; "When the ring hides its
+ * communication": each transfer overlaps a step of attention). A process holds the R consecutive
+ * ranks rank0 .. rank0 + R - 1 of the plan's n_cp (R = n_cp: the whole ring in one process). The
+ * library computes and moves blocks between the process's own ranks; the caller moves the one
+ * block per step that crosses to the next process (rank rank0 + R - 1 -> rank rank0 + R) with its
+ * own transport (NCCL send/receive, peer copies, or host memory), into the next process's slot.
+ *   Stage slot (device, caller-owned, 1024-byte aligned, two of them for the double buffer): the
+ *     blocks the R ranks hold, in four regions: K and V [R][B][n_kv][n][d_k] bf16, the blocks'
+ *     position ids [R][n] int32 and their tile table [R][n_qt] int32x4 (positions travel with the
+ *     block: [CEX] "In PyTorch"). Region x starts at region_offset[x] of the slot and local rank
+ *     i's block in it at region_offset[x] + i block_bytes[x] (x = K, V, positions, tiles).
+ *   cpattn_dist_sizes: the workspace bytes, slot bytes and the four regions' offsets and block
+ *     bytes (host, written; any pointer may be NULL).
+ *   cpattn_dist_begin: q [B][R n][h][d_k], k, v [B][R n][n_kv][d_k] bf16 (device): the process's
+ *     tokens, rank rank0's n tokens in its local layout order, then rank rank0 + 1's, ...; pos
+ *     [R n] int32 position ids of those tokens or NULL for their natural positions under the
+ *     plan's layout. Places the queries in the workspace and the own blocks in `slot`.
+ *   cpattn_dist_step, steps 0..n_cp-1 in order from one host thread: every local rank attends to
+ *     the block it holds in `slot` (at step s, that of rank (r - s) mod n_cp) and merges the result
+ *     into its fp32 running (O, lse) in the workspace. The slot must not change until the step's
+ *     work on `stream` has finished.
+ *   cpattn_dist_shift: on `stream`, local rank i + 1's block in dst_slot <- local rank i's block
+ *     in src_slot, for i < R - 1, all four regions; with wrap != 0 (a process that holds the whole
+ *     ring) also local rank 0's block <- local rank R - 1's. Otherwise local rank 0's block in
+ *     dst_slot is the caller's to fill with the block the previous process sends.
+ *   cpattn_dist_finalize: after the last step, o [B][R n][h][d_k] bf16 and lse [B][h][R n] fp32 in
+ *     the process's token order (that of q).
+ * Out-of-order steps, or a B, rank0 or R other than cpattn_dist_begin's, return CPATTN_ERR_INVALID
+ * before any launch. Device-side timeouts are recorded in the workspace header (cpattn_check). */
+cpattn_status_t cpattn_dist_sizes(cpattn_plan_t plan, int B, int R, size_t* ws_bytes, size_t* slot_bytes,
+                                  size_t* region_offset /* [4] */, size_t* block_bytes /* [4] */);
+cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, const void* q, const void* k,
+                                  const void* v, const int32_t* pos, void* ws, size_t ws_bytes, void* slot,
+                                  size_t slot_bytes, cpattn_stream_t stream);
+cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
+                                 const void* slot, size_t slot_bytes, void* ws, size_t ws_bytes,
+                                 cpattn_stream_t stream);
+cpattn_status_t cpattn_dist_shift(cpattn_plan_t plan, int B, int R, const void* src_slot, void* dst_slot,
+                                  size_t slot_bytes, int wrap, cpattn_stream_t stream);
+cpattn_status_t cpattn_dist_finalize(cpattn_plan_t plan, int B, int rank0, int R, void* o, float* lse, void* ws,
+                                     size_t ws_bytes, cpattn_stream_t stream);
+
 /* S-way log-sum-exp merge of partial attention results ([CEX] online-softmax paragraph: old
  * totals rescaled to a common maximum). For every row and head:
  *   lse = ln sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) * o_s;  all lse_s = -inf gives (0, -inf).

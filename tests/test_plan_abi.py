@@ -179,3 +179,21 @@ def test_backward_counts_match_oracle(shape):
     assert np.all(got == want)
     fwd = plan.counts(B)["kv_bytes_recv"]
     assert np.all(got > 2 * fwd)
+
+
+@pytest.mark.parametrize("T,h,n_kv,d,n_cp,layout,B", [
+    (131072, 16, 1, 128, 16, "zigzag", 1),       # the 405B per-TP slice: the pages' 63 MB
+    (16384, 32, 8, 128, 8, "zigzag", 1),
+    (32768, 16, 16, 128, 4, "contiguous", 2),
+    (1536, 4, 2, 64, 3, "striped", 3),
+])
+def test_allgather_bytes_match_the_oracle(T, h, n_kv, d, n_cp, layout, B):
+    """All-gather bytes per rank ("What context parallelism communicates": each rank receives the
+    other n_cp - 1 chunks of K and V) bit-exact against the oracle's count for method 1."""
+    plan = cp.Plan(T, h, n_kv, d, n_cp, layout)
+    got = plan.allgather_counts(B)["bytes_recv"]
+    want = B * oracle.get().cp_comm_bytes(T, h * d, n_kv * d, n_cp, oracle.ALLGATHER)
+    assert float(want).is_integer() and np.all(got == int(want))
+    assert np.all(got == plan.counts(B)["kv_bytes_recv"])   # the same volume as the ring
+    if T == 131072 and n_kv == 1:
+        assert int(got[0]) == 62914560
