@@ -295,30 +295,64 @@ def run_gpu_ring(args, w):
     ms_per_step = reduce_max(a.elapsed_time(b) / args.steps, dist, dev)
     value = flops_eff(w) / (ms_per_step * 1e-3) / 1e12
 
-    # end to end: this process's shard from pinned host memory and its outputs back, every step
+    # end to end: this process's shard from pinned host memory and its outputs back, every step,
+    # double-buffered as in the fused path's e2e (upload of step i+1 and readback of step i-1 beside
+    # the forward of step i)
     qp, kp, vp = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q_h, k_h, v_h))
-    op = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    lp = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    bufs = [(q, k, v, o, lse),
+            (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o), torch.empty_like(lse))]
+    outs = [(torch.empty(o.shape, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(lse.shape, dtype=torch.float32).pin_memory()) for _ in range(2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e2e_steps = max(3, min(args.steps, 8))
 
-    def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy)
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+    def e2e_run(n):
+        computed, read = [None, None], [None, None]
+        for i in range(n):
+            sl = i % 2
+            qb, kb, vb, ob, lb = bufs[sl]
+            with torch.cuda.stream(up):
+                if computed[sl] is not None:
+                    up.wait_event(computed[sl])
+                qb.copy_(qp, non_blocking=True)
+                kb.copy_(kp, non_blocking=True)
+                vb.copy_(vp, non_blocking=True)
+                uploaded = torch.cuda.Event()
+                uploaded.record(up)
+            stream.wait_event(uploaded)
+            if read[sl] is not None:
+                stream.wait_event(read[sl])
+            ring.forward(qb, kb, vb, out=ob, lse=lb, stream=stream, copy_stream=copy)
+            computed[sl] = torch.cuda.Event()
+            computed[sl].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[sl])
+                outs[sl][0].copy_(ob, non_blocking=True)
+                outs[sl][1].copy_(lb, non_blocking=True)
+                read[sl] = torch.cuda.Event()
+                read[sl].record(down)
+        for r in read:
+            if r is not None:
+                stream.wait_event(r)
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    up.wait_stream(stream)
+    e2e_run(e2e_steps)
     b.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dist, dev)
+    del bufs, outs
+    # one more pass with an event timeline: does each hop end before the step beside it does?
+    marks = []
+    t0 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy, timeline=marks)
+    torch.cuda.synchronize()
+    timeline = hop_summary([t0.elapsed_time(ce) for ce, _ in marks], [t0.elapsed_time(xe) for _, xe in marks], False)
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     n_grp = plan.counts(w.B)  # host call; keeps the plan's counters in the line
@@ -339,7 +373,8 @@ def run_gpu_ring(args, w):
                     "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes),
                     "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4)},
             "ring": {"processes": world, "ranks_per_process": R,
-                     "kv_bytes_recv_per_rank": int(ring.counters.kv[0] // (args.warmup + args.steps + 1 + e2e_steps)),
+                     "kv_bytes_recv_per_rank": int(ring.counters.kv[0] // (args.warmup + args.steps + 2 + e2e_steps)),
+                     "timeline": timeline,
                      "kv_bytes_recv_per_rank_pages": int(n_grp["kv_bytes_recv"][0]),
                      "transport": "NCCL send/recv" if world > 1 else "none (one process holds the ring)"},
             # per step: the order upload, placement (pos_tiles, tile_suffix, permute), per ring step
@@ -716,6 +751,9 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     torch.cuda.synchronize()
     cp.check(plan, wsr)
     del wsr, dout, dq, dk, dv
+    # the all-gather variant at the 405B per-TP slice (one KV head per rank, the pages' 63 MB case):
+    # the exposed gather beside the attention launch that follows it
+    out["allgather"] = allgather_extra(cp, dev, peaks)
     # the head split (Ulysses) as the comparison workload: all-to-all, per-rank attention over
     # every token of h / n_cp heads, all-to-all back; bytes per rank against the ring's
     up = cp.UlyssesPlan(w.T, w.h, w.n_kv, w.d, w.n_cp, w.causal)
@@ -739,6 +777,51 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     return out
 
 
+def allgather_extra(cp, dev, peaks):
+    """The all-gather variant on the 405B per-TP slice (T = 131072, h = 16, one KV head, 16 ranks):
+    placement, the gather of every rank's copy of K and V (timed alone: the exposed phase), and
+    the attention launch over the gathered copies; beside it the ring's fused launch on the same
+    placement. Bytes per rank from the library's count (the pages' 63 MB)."""
+    import torch
+    w = synth.workload("llama405b_tp_T128k")
+    q_h, k_h, v_h = synth.make_qkv(w)
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = to_dev(q_h), to_dev(k_h), to_dev(v_h)
+    plan = cp.Plan(w.T, w.h, w.n_kv, w.d, w.n_cp, w.layouts[0], w.causal)
+    ws = cp.alloc_workspace(plan.allgather_workspace_size(w.B), dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    cp.allgather_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    reps = 3
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for r in range(reps):
+        cp.permute(q, k, v, plan, ws, stream=stream)
+        ev[r][0].record(stream)
+        cp.allgather_gather(plan, w.B, ws, stream=stream)
+        ev[r][1].record(stream)
+        cp.allgather_attend(plan, w.B, ws, o, lse, stream=stream)
+        ev[r][2].record(stream)
+        cp.attend(plan, w.B, ws, o, lse, stream=stream)
+        ev[r][3].record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    gather_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    attend_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    ring_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ev]))
+    recv = int(plan.allgather_counts(w.B)["bytes_recv"][0])
+    copied = 2 * w.n_cp * (k_h.nbytes + v_h.nbytes)      # read + write of every rank's copy
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    return {"workload": f"{w.name} {synth.LAYOUT_NAMES[w.layouts[0]]}", "gather_ms": gather_ms,
+            "attention_ms": attend_ms, "exposed_frac": gather_ms / (gather_ms + attend_ms),
+            "ring_fused_attention_ms": ring_ms, "bytes_recv_per_rank": recv,
+            "gather_gbs": copied / gather_ms / 1e6, "gather_frac_of_hbm": copied / gather_ms / 1e6 / hbm,
+            "tflops_eff_attention": flops_eff(w) / (attend_ms * 1e-3) / 1e12,
+            "pages": "63 MB per GPU per layer, about 1.3 ms over InfiniBand, against about 27 ms of compute"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -755,8 +838,13 @@ def main():
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--cpu-rows", type=int, default=256, help="query rows the CPU baseline computes (~13 s on 16 cores)")
     ap.add_argument("--ref-rows", type=int, default=8, help="query rows per step of the reference arm")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run the workload's shape at a shorter T (for small profiling captures)")
     args = ap.parse_args()
     w = synth.workload(args.workload)
+    if args.seq_len is not None:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.seq_len, name=f"{w.name}@T{args.seq_len}")
     args.layout = w.layouts[0] if args.layout is None else synth.LAYOUT_IDS[args.layout]
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -156,7 +156,10 @@ class RingProcess:
         self.transport = transport
         self.counters = HopCounters(kv=[0] * self.R, tables=[0] * self.R)
 
-    def forward(self, q, k, v, pos=None, scale=None, out=None, lse=None, stream=None, copy_stream=None):
+    def forward(self, q, k, v, pos=None, scale=None, out=None, lse=None, stream=None, copy_stream=None,
+                timeline=None):
+        """timeline: a list to which each step appends (end of its compute, end of the hop that
+        runs beside it) as timing events on the two streams (device backend only)."""
         import torch
         be, R, n_cp = self.backend, self.R, self.plan.n_cp
         B, h, n = self.B, self.plan.h, self.plan.T // n_cp
@@ -197,6 +200,11 @@ class RingProcess:
                     self.counters.kv[i] += kv_blk
                     self.counters.tables[i] += tab_blk
                 arrived = be.event(copy)
+            if timeline is not None:
+                ce, xe = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ce.record(compute)
+                xe.record(copy)
+                timeline.append((ce, xe))
         be.finalize(out, lse, compute)
         return out, lse
 
