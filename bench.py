@@ -348,6 +348,7 @@ def run_gpu_ring(args, w):
     del bufs, outs
     # one more pass with an event timeline: does each hop end before the step beside it does?
     marks = []
+    kv_before = ring.counters.kv[0]
     t0 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy, timeline=marks)
@@ -373,7 +374,7 @@ def run_gpu_ring(args, w):
                     "h2d_bytes_per_step": int(q_h.nbytes + k_h.nbytes + v_h.nbytes),
                     "d2h_bytes_per_step": int(o.numel() * 2 + lse.numel() * 4)},
             "ring": {"processes": world, "ranks_per_process": R,
-                     "kv_bytes_recv_per_rank": int(ring.counters.kv[0] // (args.warmup + args.steps + 2 + e2e_steps)),
+                     "kv_bytes_recv_per_rank": int(ring.counters.kv[0] - kv_before),
                      "timeline": timeline,
                      "kv_bytes_recv_per_rank_pages": int(n_grp["kv_bytes_recv"][0]),
                      "transport": "NCCL send/recv" if world > 1 else "none (one process holds the ring)"},
