@@ -705,7 +705,21 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     ms = a.elapsed_time(b) / 3
     out["documents"] = {"ms": ms, "documents": len(lengths), "tflops_eff": flops_docs / (ms * 1e-3) / 1e12,
                         "flops": "4 B h d per visible (query, key) pair inside each document"}
-    del od, lsed, lo
+    # the same documents given as ids in shuffled order (the document-id mask: tile classes from
+    # each tile's id range, a bitmask walk, the id compare in the element mask)
+    ids = rng.permutation(len(lengths)).astype(np.int32) * 7 + 1
+    docd = torch.from_numpy(np.repeat(ids, lengths).astype(np.int32)).to(dev)
+    cp.forward_docs(q, k, v, plan, docd, ws=ws, out=od, lse=lsed, stream=stream)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(3):
+        cp.forward_docs(q, k, v, plan, docd, ws=ws, out=od, lse=lsed, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    ms = a.elapsed_time(b) / 3
+    out["document_ids"] = {"ms": ms, "documents": len(lengths), "ids": "shuffled", "tflops_eff": flops_docs / (ms * 1e-3) / 1e12}
+    del od, lsed, lo, docd
     # the backward pass: dq, dk, dv from the forward's o and lse and a synthetic output gradient
     wsb = cp.alloc_workspace(plan.backward_workspace_size(w.B), dev)
     dout = torch.randn(q.shape, dtype=torch.bfloat16, device=dev)

@@ -31,7 +31,7 @@ SYMBOLS = [
     "cpattn_backward_counts", "cpattn_backward_ring_workspace_size", "cpattn_backward_begin",
     "cpattn_backward_ring_step", "cpattn_backward_finalize",
     "cpattn_allgather_workspace_size", "cpattn_allgather_counts", "cpattn_allgather_forward",
-    "cpattn_allgather_gather", "cpattn_allgather_attend",
+    "cpattn_allgather_gather", "cpattn_allgather_attend", "cpattn_forward_docs", "cpattn_allgather_forward_docs",
     "cpattn_dist_sizes", "cpattn_dist_begin", "cpattn_dist_step", "cpattn_dist_shift", "cpattn_dist_finalize",
 ]
 
@@ -93,6 +93,9 @@ def lib():
     L.cpattn_allgather_counts.argtypes = [_P, i, _P]
     L.cpattn_allgather_forward.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_allgather_gather.argtypes = [_P, i, _P, ctypes.c_size_t, _P]
+    L.cpattn_forward_docs.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_allgather_forward_docs.argtypes = [_P, i, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
+                                                ctypes.c_size_t, _P]
     L.cpattn_allgather_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_sizes.argtypes = [_P, i, i, sz, sz, sz, sz]
     L.cpattn_dist_begin.argtypes = [_P, i, i, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
@@ -502,6 +505,29 @@ def allgather_forward(q, k, v, plan: Plan, pos=None, lo=None, scale: float | Non
                                           _dev_ptr(pos, "pos"), _dev_ptr(lo, "lo"), float(scale or 0.0),
                                           _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"), ws.numel(),
                                           _stream_ptr(stream)), "cpattn_allgather_forward")
+    return out, lse
+
+
+def forward_docs(q, k, v, plan: Plan, doc, pos=None, scale: float | None = None, ws=None, out=None, lse=None,
+                 stream=None, allgather: bool = False):
+    """cpattn_forward_docs (or, with allgather=True, cpattn_allgather_forward_docs): the forward
+    under document ids, doc [T] int32 CUDA tensor; key u is visible to query t iff doc[u] == doc[t]
+    (and pos[u] <= pos[t] for a causal plan). Arguments and results as forward()."""
+    torch = _torch()
+    B = _check_inputs(plan, q, k, v)
+    if tuple(doc.shape) != (plan.T,) or doc.dtype != torch.int32:
+        raise ValueError("doc must be an int32 tensor of T entries")
+    if ws is None:
+        ws = alloc_workspace(plan.allgather_workspace_size(B) if allgather else plan.workspace_size(B), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
+    fn = lib().cpattn_allgather_forward_docs if allgather else lib().cpattn_forward_docs
+    _check(fn(plan.handle, B, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"), _dev_ptr(pos, "pos"),
+              _dev_ptr(doc, "doc"), float(scale or 0.0), _dev_ptr(out, "o"), _dev_ptr(lse, "lse"), _dev_ptr(ws, "ws"),
+              ws.numel(), _stream_ptr(stream)),
+           "cpattn_allgather_forward_docs" if allgather else "cpattn_forward_docs")
     return out, lse
 
 

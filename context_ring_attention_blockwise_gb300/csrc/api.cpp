@@ -142,6 +142,7 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.unit_tiles = at<int32_t>(ws, w.unit_tiles);
     a.walk_tab = at<int32_t>(ws, w.walk_tab);
     a.walk_nz = at<unsigned long long>(ws, w.walk_nz);
+    a.walk_bits = at<unsigned long long>(ws, w.walk_bits);
     a.scale_log2 = resolve_scale(p, scale);
     a.qL = at<char>(ws, w.qL);
     a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);
@@ -421,6 +422,30 @@ cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, 
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
     a.o = o; a.lse = lse;
     a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo);
+    std::string why;
+    int e = launch_attn(a, st, &why);
+    if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_forward_docs(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                    const int32_t* pos, const int32_t* doc, float scale, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!doc || !aligned16(doc)) return fail(CPATTN_ERR_INVALID, "doc must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // the ids travel with the tokens like the lower bound does, with their range per tile
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, doc))) return s;
+    cpattn::WsLayout w = cpattn::ws_layout(*p, B);
+    cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
+    a.fused = 1; a.step = 0; a.kv_by_holder = 0;
+    a.o = o; a.lse = lse;
+    a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); a.doc_ids = 1;
     std::string why;
     int e = launch_attn(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
@@ -831,7 +856,7 @@ cpattn_status_t gather_kv(const Plan& p, int B, void* ws, cudaStream_t st) {
 }
 
 cpattn_status_t gather_attend(const Plan& p, int B, float scale, const int32_t* lo, void* o, float* lse, void* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, int doc_ids = 0) {
     const cpattn::WsLayout w = cpattn::ws_layout(p, B);
     cpattn::AttnLaunch a = attn_args(p, B, scale, ws);
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
@@ -839,7 +864,7 @@ cpattn_status_t gather_attend(const Plan& p, int B, float scale, const int32_t* 
     a.kv_rank_rows = (int64_t)p.n_cp * B * p.n_kv * p.n;
     a.kv_rows = (uint64_t)p.n_cp * a.kv_rank_rows;
     a.o = o; a.lse = lse;
-    if (lo) { a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); }
+    if (lo) { a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); a.doc_ids = doc_ids; }
     std::string why;
     int e = launch_attn(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
@@ -884,6 +909,22 @@ cpattn_status_t cpattn_allgather_forward(cpattn_plan_t plan, int B, const void* 
     if ((s = prologue(*p, B, q, k, v, pos, ws, st, lo))) return s;
     if ((s = gather_kv(*p, B, ws, st))) return s;
     return gather_attend(*p, B, scale, lo, o, lse, ws, st);
+}
+
+cpattn_status_t cpattn_allgather_forward_docs(cpattn_plan_t plan, int B, const void* q, const void* k,
+                                              const void* v, const int32_t* pos, const int32_t* doc, float scale,
+                                              void* o, float* lse, void* ws, size_t ws_bytes, cpattn_stream_t stream) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (!doc || !aligned16(doc)) return fail(CPATTN_ERR_INVALID, "doc must be non-NULL and 16-byte aligned");
+    cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
+    if (s) return s;
+    if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
+    if ((s = check_gather_ws(*p, B, ws, ws_bytes))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, doc))) return s;
+    if ((s = gather_kv(*p, B, ws, st))) return s;
+    return gather_attend(*p, B, scale, doc, o, lse, ws, st, 1);
 }
 
 cpattn_status_t cpattn_allgather_gather(cpattn_plan_t plan, int B, void* ws, size_t ws_bytes, cpattn_stream_t stream) {

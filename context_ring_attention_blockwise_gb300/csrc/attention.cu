@@ -8,7 +8,11 @@
 // of rank (r - s) mod n_cp). It skips key tiles no query of the unit can see and masks the partly
 // visible ones ("The causal mask unbalances the sequence"). With document masks for packed
 // sequences ("What context parallelism communicates") every query also has a lowest visible key
-// position; a key is visible iff lo[t] <= pos[u] <= pos[t]. It keeps the online-softmax state of
+// position; a key is visible iff lo[t] <= pos[u] <= pos[t]. With document ids (the same section:
+// "arbitrary masks, such as document masks for packed sequences") a key is visible iff it has the
+// query's id (and, causally, pos[u] <= pos[t]); documents need not be contiguous, and a small kernel
+// records per row group and ring step a bitmask of the key tiles some query can see, which the
+// walkers follow. It keeps the online-softmax state of
 // the paragraph after the ring one on chip across every step: running max, running sum of
 // exponentials, running weighted sum of values, rescaled when a larger score arrives.
 //
@@ -58,9 +62,13 @@ constexpr int kThreads = 384;
 // setmaxnreg: 120 / 184 (128 * 120 + 256 * 184 = 62464 <= 384 * 168); the document-mask walk
 // keeps 192 in the softmax warps (112 / 192, 63488), where 184 spills more. Measured: 120 / 184
 // is 0.4 % faster than 112 / 192 on the plain kernel, 128 / 176 and 104 / 200 are slower.
-template <bool LB>
+// Mask modes of the kernel: causal (or none) from positions alone; a per-query lower bound on the
+// key positions; document ids.
+enum MaskMode : int { kMaskPos = 0, kMaskLower = 1, kMaskDoc = 2 };
+
+template <int M>
 struct RegSplit {
-    static constexpr int low = LB ? 112 : 120, high = LB ? 192 : 184;
+    static constexpr int low = M != kMaskPos ? 112 : 120, high = M != kMaskPos ? 192 : 184;
 };
 
 struct Params {
@@ -80,6 +88,10 @@ struct Params {
     // tiles its walk visits lie in [begin, end) (begin | end << 16), and a bit per non-empty step
     int32_t* walk_tab;               // [n_cp * n_grp][n_cp]
     unsigned long long* walk_nz;     // [n_cp * n_grp], for n_cp <= 64
+    // document ids only, written by unit_tiles_kernel: per row group and ring step, a bit per key
+    // tile that some query of the row group may see ([n_cp * n_grp][n_cp][words], 64 tiles a word)
+    unsigned long long* walk_bits;
+    int words;                       // ceil(n_qt / 64)
     unsigned long long* counts;
     uint32_t* sched;
     uint16_t* o;
@@ -186,17 +198,19 @@ struct Unit {
     int r, b, kvh, rg;   // rank, batch element, KV head, row group r * n_grp + group
     int head[2], qt[2], valid[2];
     int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
-    int2 qlo[2];   // range of the tile's lowest visible key positions; (INT_MIN, INT_MIN) without one
+    int2 qlo[2];   // range of the tile's lowest visible key positions (document ids: range of its ids);
+                   // (INT_MIN, INT_MIN) without one
 };
 
-// The query tiles' position ranges and (LB: with a per-query lower bound) lower-bound ranges.
-template <bool LB>
+// The query tiles' position ranges and (with a per-query lower bound or document ids) the range of
+// the bounds or ids.
+template <int M>
 __device__ __forceinline__ void unit_ranges(const Params& P, Unit& U) {
     for (int i = 0; i < 2; ++i) {
         if (U.valid[i]) {
             const int4 t4 = __ldg(P.tile_mm + U.r * P.n_qt + U.qt[i]);
             U.qmm[i] = make_int2(t4.x, t4.y);
-            if (LB) {
+            if (M != kMaskPos) {
                 const int4 l4 = __ldg(P.tile_lo + U.r * P.n_qt + U.qt[i]);
                 U.qlo[i] = make_int2(l4.x, l4.y);
             } else {
@@ -213,7 +227,7 @@ __device__ __forceinline__ void unit_ranges(const Params& P, Unit& U) {
 // next, so the CTAs running at any moment read the keys and values of one or two KV heads and
 // those stay in L2. Within a KV head, (rank, row group) follow the plan's longest-first order,
 // then the query heads of the group.
-template <bool LB>
+template <int M>
 __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
     Unit U;
     const int per = P.pair_heads ? P.g / 2 : P.g;        // units per (b, kvh, row group)
@@ -240,17 +254,32 @@ __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
         U.valid[0] = 1;
         U.valid[1] = U.qt[1] < P.n_qt;
     }
-    unit_ranges<LB>(P, U);
+    unit_ranges<M>(P, U);
     return U;
+}
+
+// Block class of a key tile for one query tile under document ids: SKIP when no id is shared or (causal)
+// every key follows every query; FULL when both tiles hold one id, the same, and every key precedes
+// every query; otherwise partly visible (the element mask decides).
+__device__ __forceinline__ int doc_class(int causal, int qmin, int qmax, int dqmin, int dqmax, const int4& t4,
+                                         const int4& d4) {
+    if (d4.y < dqmin || d4.x > dqmax) return CPATTN_TILE_SKIP;
+    const int pc = !causal ? CPATTN_TILE_FULL : (t4.x > qmax) ? CPATTN_TILE_SKIP
+                                              : (t4.y > qmin) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
+    if (pc == CPATTN_TILE_SKIP) return CPATTN_TILE_SKIP;
+    const bool one_id = dqmin == dqmax && d4.x == d4.y && d4.x == dqmin;
+    return (pc == CPATTN_TILE_FULL && one_id) ? CPATTN_TILE_FULL : CPATTN_TILE_DIAG;
 }
 
 // The key tiles a unit visits, in ring order, leaving out tiles that both query tiles skip.
 // cls(i): FULL / DIAG / SKIP for query tile i; mask(i): the tile needs the element mask for
 // query tile i (partly visible, skipped by this tile only, or shorter than 128 keys). A block
 // whose remaining tiles all start after every query of the unit is left in one step. LB: the
-// queries also have a lowest visible key position (document masks).
-template <bool LB>
+// queries also have a lowest visible key position (document masks). DOC: document ids; the walk
+// follows the per-step bitmask of visited key tiles.
+template <int M>
 struct TileWalk {
+    static constexpr bool LB = M == kMaskLower, DOC = M == kMaskDoc;
     const Params* p;
     int r, s, s_end, kt, src;
     int qmin0, qmax0, qmin1, qmax1, qmax, cls0, cls1, mask0, mask1;
@@ -276,6 +305,40 @@ struct TileWalk {
             nz = P.n_cp <= 64 ? __ldg(P.walk_nz + rg) : 0ull;
             if (!P.fused && P.n_cp <= 64) nz &= 1ull << P.step;   // one step: only its own bit
         }
+        if (DOC) {
+            // the bitmask walk starts on the last word before its first step
+            s -= 1;
+            wi = P.words - 1;
+            bits = 0ull;
+        }
+    }
+    int wi;
+    unsigned long long bits;
+    // Document ids: the next set bit of the row group's bitmask, step by step.
+    __device__ bool next_bits() {
+        const Params& P = *p;
+        for (;;) {
+            while (bits == 0ull) {
+                if (++wi >= P.words) {
+                    wi = 0;
+                    if (++s >= s_end) return false;
+                }
+                bits = __ldg(P.walk_bits + ((int64_t)rg * P.n_cp + s) * P.words + wi);
+            }
+            kt = wi * 64 + (__ffsll((long long)bits) - 1);
+            bits &= bits - 1ull;
+            src = r - s;
+            if (src < 0) src += P.n_cp;
+            const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
+            const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
+            const int4 d4 = __ldg(P.tile_lo + src * P.n_qt + kt);
+            cls0 = doc_class(P.causal, qmin0, qmax0, lmin0, lmax0, t4, d4);
+            cls1 = doc_class(P.causal, qmin1, qmax1, lmin1, lmax1, t4, d4);
+            if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
+            mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
+            mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
+            return true;
+        }
     }
     // Document masks: the walk of a row group is the same for all its units, and the kernel
     // before this one recorded it per step as a key-tile range (next_scan below): jump from one
@@ -284,6 +347,7 @@ struct TileWalk {
     int rg, kend;
     unsigned long long nz;
     __device__ bool next() {
+        if (DOC) return next_bits();
         if (!LB || !p->causal) return next_scan();
         const Params& P = *p;
         for (;;) {
@@ -376,7 +440,7 @@ struct TileWalk {
 // ---------------------------------------------------------------------------------------------
 // warp 0: scheduler and TMA producer
 // ---------------------------------------------------------------------------------------------
-template <int D, bool LB>
+template <int D, int M>
 __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                          uint32_t sQ, uint32_t sK, uint32_t sV, volatile int* unit_slot, const Bars<D>& bars,
                          const Waiter& wait) {
@@ -402,8 +466,8 @@ __device__ void producer(const Params& P, const CUtensorMap* tmQ, const CUtensor
         unit_slot[slot] = (u < P.num_units) ? u : -1;
         mbar_arrive(bars.unit_full(slot));
         if (u >= P.num_units) break;
-        const Unit U = decode_unit<LB>(P, u);
-        TileWalk<LB> w;
+        const Unit U = decode_unit<M>(P, u);
+        TileWalk<M> w;
         w.init(P, U);
         int j = 0, prev_row = 0;
         while (w.next()) {
@@ -536,7 +600,7 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
 // ---------------------------------------------------------------------------------------------
 // warps 4..11: softmax and epilogue, warpgroup i for query tile i, one thread per row
 // ---------------------------------------------------------------------------------------------
-template <int D, bool LB>
+template <int D, int M>
 __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* unit_slot, const Bars<D>& bars,
                                  const Waiter& wait) {
     using C = Cfg<D>;
@@ -557,14 +621,16 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.unit_empty(slot));
         if (u < 0) break;
-        const Unit U = decode_unit<LB>(P, u);
+        constexpr bool LB = M == kMaskLower, DOC = M == kMaskDoc;
+        const Unit U = decode_unit<M>(P, u);
         const int head = wg ? U.head[1] : U.head[0];
         const int qt = wg ? U.qt[1] : U.qt[0];
         const int member_valid = wg ? U.valid[1] : U.valid[0];
         const int64_t jl = (int64_t)qt * 128 + row;             // local index on rank r
         const bool row_valid = member_valid && jl < P.n;
         const int qpos = row_valid ? __ldg(P.posL + (int64_t)U.r * P.n + jl) : 0;
-        const int qlo = (LB && row_valid) ? __ldg(P.loL + (int64_t)U.r * P.n + jl) : INT_MIN;
+        // the query's lowest visible key position, or its document id
+        const int qlo = ((LB || DOC) && row_valid) ? __ldg(P.loL + (int64_t)U.r * P.n + jl) : INT_MIN;
         // l: sum of the fp32 exponentials (for lse); lr: the same values rounded to bf16 as the PV
         // product sees them (normalises O, so the weights applied to V sum to one exactly).
         float m_used = -INFINITY, l = 0.f, lr = 0.f;
@@ -579,7 +645,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             }
             cnt_full = cnt_diag = 0;
         };
-        TileWalk<LB> w;
+        TileWalk<M> w;
         w.init(P, U);
         int j = 0;
         bool have = w.next();
@@ -607,13 +673,16 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                 // being hoisted (128 live loads would double the register footprint).
 #pragma unroll
                 for (int c0 = 0; c0 < 128; c0 += 16) {
-                    int kp[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.kposL + kbase + c0 + c) : INT_MIN;
+                    int kp[16], kd[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos && (!LB || kp[c] >= qlo);
+                        kp[c] = (c0 + c < kvalid && P.causal) ? __ldg(P.kposL + kbase + c0 + c) : INT_MIN;
+                        if (DOC) kd[c] = (c0 + c < kvalid) ? __ldg(P.loL + kbase + c0 + c) : qlo;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const bool vis = row_valid && (c0 + c < kvalid) && kp[c] <= qpos && (!LB || kp[c] >= qlo) &&
+                                         (!DOC || kd[c] == qlo);
                         if (!vis) x[c0 + c] = -INFINITY;
                     }
                     asm volatile("" ::: "memory");
@@ -771,7 +840,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
     }
 }
 
-template <int D, bool LB>
+template <int D, int M>
 __global__ void __launch_bounds__(kThreads, 1)
     ring_attention_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const Params P) {
@@ -814,12 +883,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Waiter wait{abort_flag, P.header, P.timeout_ns};
 
     if (warp < 4) {
-        setmaxnreg_dec<RegSplit<LB>::low>();
-        if (warp == 0 && lane == 0) producer<D, LB>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
+        setmaxnreg_dec<RegSplit<M>::low>();
+        if (warp == 0 && lane == 0) producer<D, M>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
         if (warp == 1 && lane == 0) mma_issuer<D>(P, tmem, sQ, sK, sV, unit_slot, bars, wait);
     } else {
-        setmaxnreg_inc<RegSplit<LB>::high>();
-        softmax_epilogue<D, LB>(P, tmem, unit_slot, bars, wait);
+        setmaxnreg_inc<RegSplit<M>::high>();
+        softmax_epilogue<D, M>(P, tmem, unit_slot, bars, wait);
     }
     tc_fence_before();
     __syncthreads();
@@ -846,8 +915,9 @@ __global__ void wait_selftest_kernel(uint32_t* header, uint64_t timeout_ns) {
 // One thread per row group (rank r, group): the number of key tiles a unit of that row group
 // visits in this launch, by the same walk the producer and the softmax warps take. Units of one
 // row group differ only in batch element and heads, which do not change the walk.
-template <bool LB>
+template <int M>
 __global__ void unit_tiles_kernel(const Params P) {
+    constexpr bool LB = M == kMaskLower, DOC = M == kMaskDoc;
     const int rg = blockIdx.x * blockDim.x + threadIdx.x;
     if (rg >= P.n_cp * P.n_grp) return;
     Unit U;
@@ -865,9 +935,36 @@ __global__ void unit_tiles_kernel(const Params P) {
         U.valid[0] = 1;
         U.valid[1] = U.qt[1] < P.n_qt;
     }
-    unit_ranges<LB>(P, U);
+    unit_ranges<M>(P, U);
     U.head[0] = U.head[1] = 0;
-    TileWalk<LB> w;
+    if (DOC) {
+        // one bit per key tile some query of the row group may see, for every step of this launch
+        const int s0 = P.fused ? 0 : P.step, s1 = P.fused ? P.n_cp : P.step + 1;
+        int c = 0;
+        for (int s = s0; s < s1; ++s) {
+            int src = U.r - s;
+            if (src < 0) src += P.n_cp;
+            for (int wi = 0; wi < P.words; ++wi) {
+                unsigned long long bits = 0ull;
+                for (int b = 0; b < 64; ++b) {
+                    const int kt = wi * 64 + b;
+                    if (kt >= P.n_qt) break;
+                    const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
+                    const int4 d4 = __ldg(P.tile_lo + src * P.n_qt + kt);
+                    const int c0 = doc_class(P.causal, U.qmm[0].x, U.qmm[0].y, U.qlo[0].x, U.qlo[0].y, t4, d4);
+                    const int c1 = doc_class(P.causal, U.qmm[1].x, U.qmm[1].y, U.qlo[1].x, U.qlo[1].y, t4, d4);
+                    if (c0 != CPATTN_TILE_SKIP || c1 != CPATTN_TILE_SKIP) {
+                        bits |= 1ull << b;
+                        ++c;
+                    }
+                }
+                P.walk_bits[((int64_t)rg * P.n_cp + s) * P.words + wi] = bits;
+            }
+        }
+        P.unit_tiles[rg] = c;
+        return;
+    }
+    TileWalk<M> w;
     w.init(P, U);
     if (LB && P.causal) {                 // the scan, as the table walk will replay it
         w.s = P.fused ? 0 : P.step;
@@ -900,22 +997,22 @@ __global__ void unit_tiles_kernel(const Params P) {
 }
 
 // ---- host side -------------------------------------------------------------------------------
-template <int D, bool LB>
+template <int D, int M>
 int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     using C = Cfg<D>;
     static PerDeviceOnce attr_once;
     int dev = 0;
     cudaGetDevice(&dev);
     const int ea = attr_once.run(dev, [&]() -> int {
-        cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_BYTES);
         if (e != cudaSuccess) return (int)e;
         // setmaxnreg.inc waits until enough registers are free in the block's allocation: the
         // split must fit in what the block is launched with, or the kernel would never proceed.
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, ring_attention_kernel<D, LB>);
+        e = cudaFuncGetAttributes(&fa, ring_attention_kernel<D, M>);
         if (e != cudaSuccess) return (int)e;
-        if ((long)fa.numRegs * kThreads < 128L * RegSplit<LB>::low + 256L * RegSplit<LB>::high) {
+        if ((long)fa.numRegs * kThreads < 128L * RegSplit<M>::low + 256L * RegSplit<M>::high) {
             *why = "attention kernel built with " + std::to_string(fa.numRegs) +
                    " registers per thread, too few for its warpgroup register split";
             return (int)cudaErrorInvalidConfiguration;
@@ -945,6 +1042,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.unit_tiles = a.unit_tiles;
     P.walk_tab = a.walk_tab;
     P.walk_nz = a.walk_nz;
+    P.walk_bits = a.walk_bits;
+    P.words = (a.n_qt + 63) / 64;
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.counts = a.counts; P.sched = a.sched;
     P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
@@ -957,8 +1056,8 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.num_units = (int)units;
     const int grid = (int)(units < sms ? units : sms);
     const int n_rg = a.n_cp * a.n_grp;
-    unit_tiles_kernel<LB><<<(n_rg + 127) / 128, 128, 0, st>>>(P);
-    ring_attention_kernel<D, LB><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
+    unit_tiles_kernel<M><<<(n_rg + 127) / 128, 128, 0, st>>>(P);
+    ring_attention_kernel<D, M><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }
 
@@ -966,9 +1065,18 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
 
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool lb = a.loL != nullptr;   // a per-query lower bound (document masks)
-    if (a.d == 128) return lb ? launch_d<128, true>(a, st, why) : launch_d<128, false>(a, st, why);
-    if (a.d == 64) return lb ? launch_d<64, true>(a, st, why) : launch_d<64, false>(a, st, why);
+    // a per-query lower bound or document ids, both read from loL / tile_lo
+    const int mode = a.loL == nullptr ? kMaskPos : a.doc_ids ? kMaskDoc : kMaskLower;
+    if (mode == kMaskDoc && !a.walk_bits) {
+        *why = "document ids need the walk bitmask region";
+        return (int)cudaErrorInvalidValue;
+    }
+    if (a.d == 128)
+        return mode == kMaskPos ? launch_d<128, kMaskPos>(a, st, why)
+               : mode == kMaskLower ? launch_d<128, kMaskLower>(a, st, why) : launch_d<128, kMaskDoc>(a, st, why);
+    if (a.d == 64)
+        return mode == kMaskPos ? launch_d<64, kMaskPos>(a, st, why)
+               : mode == kMaskLower ? launch_d<64, kMaskLower>(a, st, why) : launch_d<64, kMaskDoc>(a, st, why);
     *why = "unsupported head width";
     return (int)cudaErrorInvalidValue;
 }

@@ -37,6 +37,7 @@ struct WsLayout {
                             // the current launch (written by the attention launch itself)
     size_t walk_tab = 0;    // int32 [n_cp * n_qt][n_cp]: document masks: visited key-tile range per row group and step
     size_t walk_nz = 0;     // uint64 [n_cp * n_qt]: document masks: the steps with visited tiles
+    size_t walk_bits = 0;   // uint64 [n_cp * n_qt][n_cp][ceil(n_qt / 64)]: document ids: visited key tiles
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
@@ -169,6 +170,8 @@ struct AttnLaunch {
     int first = -1;            // ring step: write (1) or merge into (0) the running state; -1: step == 0
     int64_t kv_rank_rows = 0;  // all-gather: K/V rows between the gathered copies of consecutive ranks
     uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
+    int doc_ids = 0;           // loL / tile_lo hold document ids (else a per-query lower bound)
+    unsigned long long* walk_bits = nullptr;   // document ids: [n_cp * n_grp][n_cp][ceil(n_qt / 64)] scratch
 };
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why);
 

@@ -167,6 +167,18 @@ cpattn_status_t cpattn_forward_masked(cpattn_plan_t plan, int B, const void* q, 
                                       const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse, void* ws,
                                       size_t ws_bytes, cpattn_stream_t stream);
 
+/* The forward under document ids ([CEX] "What context parallelism communicates": masks "such as
+ * document masks for packed sequences"): key u is visible to query t iff doc[u] == doc[t] and, for
+ * a causal plan, pos[u] <= pos[t]. Any int32 ids in any order; a document need not be contiguous.
+ * The ids travel with the tokens; each tile's (min, max) id, with the position ranges, classifies
+ * every (query tile, key tile) pair, and the key tiles some query of a row group may see are
+ * recorded per ring step as a bitmask the kernel's walkers follow. A row that sees no key gets
+ * o = 0 and lse = -inf.
+ *   doc [T] int32 (device, natural order, 16-byte aligned); other arguments as cpattn_forward. */
+cpattn_status_t cpattn_forward_docs(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
+                                    const int32_t* pos, const int32_t* doc, float scale, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, cpattn_stream_t stream);
+
 /* Backward pass ([CEX] "What context parallelism communicates": each rank keeps the gradient
  * of its own queries; the key and value gradients travel back to their owners as a second
  * circulating block of the ring, which on one GPU is a key tile's gradient accumulated over
@@ -286,6 +298,10 @@ cpattn_status_t cpattn_allgather_counts(cpattn_plan_t plan, int B, int64_t* byte
 cpattn_status_t cpattn_allgather_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                          const int32_t* pos, const int32_t* lo, float scale, void* o, float* lse,
                                          void* ws, size_t ws_bytes, cpattn_stream_t stream);
+/* cpattn_allgather_forward under document ids (as cpattn_forward_docs): any ids, in any order. */
+cpattn_status_t cpattn_allgather_forward_docs(cpattn_plan_t plan, int B, const void* q, const void* k,
+                                              const void* v, const int32_t* pos, const int32_t* doc, float scale,
+                                              void* o, float* lse, void* ws, size_t ws_bytes, cpattn_stream_t stream);
 cpattn_status_t cpattn_allgather_gather(cpattn_plan_t plan, int B, void* ws, size_t ws_bytes, cpattn_stream_t stream);
 cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, void* o, float* lse, void* ws,
                                         size_t ws_bytes, cpattn_stream_t stream);

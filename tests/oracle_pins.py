@@ -484,6 +484,30 @@ def pin_document_mask(orc):
             start += ln
 
 
+def pin_document_mask_any_ids(orc):
+    """Document ids in any order, documents split into pieces: against SDPA with the boolean mask
+    doc[u] == doc[t] (and pos[u] <= pos[t]) under permuted positions; and one token per document,
+    where every query sees only itself, so O = v_t and lse = scale <q_t, k_t> (closed form)."""
+    B, T, h, n_kv, d = 1, 48, 4, 2, 8
+    q, k, v = _qkv(43, B, T, h, n_kv, d)
+    doc = np.array([5, 5, 2, 2, 2, 9, 5, 5, 9, 9, 2, 0] * 4, dtype=np.int32)   # pieces, ids not increasing
+    pos = np.random.default_rng(3).permutation(T).astype(np.int32)
+    for causal in (True, False):
+        o, lse = orc.attention_docs(q, k, v, doc, causal=causal, pos=pos)
+        same = doc[None, :] == doc[:, None]
+        mask = same & (pos[None, :] <= pos[:, None]) if causal else same
+        ref = _sdpa(q, k, v, False, mask=torch.from_numpy(mask))
+        assert _maxabs(o, ref) < 1e-12, "document ids in any order differ from SDPA with the same mask"
+    one = np.arange(T, dtype=np.int32)[::-1].copy()
+    o, lse = orc.attention_docs(q, k, v, one, causal=False)
+    qf, kf, vf = (_f64(x).numpy() for x in (q, k, v))
+    g = h // n_kv
+    for i in range(h):
+        assert _maxabs(o[:, :, i], vf[:, :, i // g]) == 0.0, "a lone token must return its own value row"
+        s = np.einsum("btc,btc->bt", qf[:, :, i], kf[:, :, i // g]) / np.sqrt(d)
+        assert _maxabs(lse[:, i], s) < 1e-12, "a lone token's lse is its own score"
+
+
 def pin_document_mask_gradients(orc):
     """Gradients under a document mask: against autograd with the boolean mask, and each document's
     gradients computed on its own slice."""
