@@ -32,10 +32,13 @@ METRIC = "ring-attn fwd effective TFLOP/s on 1 GB300; % of dense BF16 tensor pea
 DEFAULT_WORKLOAD = "llama70b_zigzag_T128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one attention launch on a workload, from a one-pass ncu capture of
-# dram__bytes_read.sum and dram__bytes_write.sum, keyed by the sha256 prefix of the attention kernel
-# source it was measured on: a changed kernel reports null until it is measured again.
-MEASURED_TRAFFIC = {"e800f6ab9e7aca98": {"llama70b_zigzag_T128k": 4569794560 + 2133419008}}
+# DRAM bytes (read + write) of one attention launch on a workload and how they were taken, keyed by
+# the sha256 prefix of the attention kernel source they were measured on: a changed kernel reports
+# null until it is measured again. The 70B-shaped 128K launch is too large for a capture with more
+# than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
+# scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
+# to be re-read once two KV heads in flight fill L2.
+MEASURED_TRAFFIC = {}
 
 
 def attention_source_hash() -> str:
@@ -46,7 +49,8 @@ def attention_source_hash() -> str:
 
 
 def measured_traffic(workload_name: str):
-    return MEASURED_TRAFFIC.get(attention_source_hash(), {}).get(workload_name)
+    """(bytes per launch, how it was measured) or (None, None)."""
+    return MEASURED_TRAFFIC.get(attention_source_hash(), {}).get(workload_name, (None, None))
 
 
 def reduce_max(value: float, dist, device=None) -> float:
@@ -546,7 +550,8 @@ def run_gpu(args, w):
             "frac_of_peak": value / world / peak_tf,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": achieved / peak_tf,
-                         "traffic": args.traffic if args.traffic is not None else (None if ring else measured_traffic(w.name)),
+                         "traffic": args.traffic if args.traffic is not None else (None if ring else measured_traffic(w.name)[0]),
+                         "traffic_how": None if ring else measured_traffic(w.name)[1],
                          "kernel": "ring_attention_kernel<128>" if not ring else "whole ring-step path",
                          "peak_kind": f"bf16 dense, sustained, {peak_src}",
                          "peak_burst": float(peaks.get("bf16_tflops", 0.0))},
