@@ -43,7 +43,7 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_single_rank_helpers():
     assert bench.reduce_max(3.5, None) == 3.5
     assert bench.whole_job_rate(1.0e12, 1, 1000.0) == pytest.approx(1.0e12)
-    assert bench.measured_traffic("no_such_workload") is None
+    assert bench.measured_traffic("no_such_workload") == (None, None)
 
 
 def test_hop_summary_slack_and_exposure():
