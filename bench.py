@@ -686,6 +686,27 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
     torch.cuda.synchronize()
     cp.check(plan, wsr)
+    # the same with SMs left free during the attention launches, so that the device-to-device hop
+    # of the next block can run beside the step instead of in its tail
+    for reserve in (4, 8):
+        plan.set_reserved_sms(reserve)
+        cp.ring_forward(q, k, v, plan, ws=wsr, out=o2, lse=lse2, stream=stream, copy_stream=copy)
+        torch.cuda.synchronize()
+        a.record(stream)
+        cp.ring_forward(q, k, v, plan, ws=wsr, out=o2, lse=lse2, stream=stream, copy_stream=copy)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_r = a.elapsed_time(b)
+        cp.permute(q, k, v, plan, wsr, stream=stream)
+        tl = ring_timeline(lambda s: cp.ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream,
+                           copy, False)
+        cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
+        torch.cuda.synchronize()
+        cp.check(plan, wsr)
+        out["ring_step_path"][f"reserved_sms_{reserve}"] = {"ms_per_step": ms_r,
+                                                             "tflops_eff": flops_eff(w) / (ms_r * 1e-3) / 1e12,
+                                                             "timeline": tl}
+    plan.set_reserved_sms(0)
     del wsr, o2, lse2
     # document masks: the same workload packed with seeded documents of 2K..16K tokens
     rng = np.random.default_rng(w.seed)

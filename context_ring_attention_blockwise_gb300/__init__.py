@@ -33,6 +33,7 @@ SYMBOLS = [
     "cpattn_allgather_workspace_size", "cpattn_allgather_counts", "cpattn_allgather_forward",
     "cpattn_allgather_gather", "cpattn_allgather_attend", "cpattn_forward_docs", "cpattn_allgather_forward_docs",
     "cpattn_dist_sizes", "cpattn_dist_begin", "cpattn_dist_step", "cpattn_dist_shift", "cpattn_dist_finalize",
+    "cpattn_plan_set_reserved_sms",
 ]
 
 
@@ -102,6 +103,7 @@ def lib():
     L.cpattn_dist_step.argtypes = [_P, i, i, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_shift.argtypes = [_P, i, i, _P, _P, ctypes.c_size_t, i, _P]
     L.cpattn_dist_finalize.argtypes = [_P, i, i, i, _P, _P, _P, ctypes.c_size_t, _P]
+    L.cpattn_plan_set_reserved_sms.argtypes = [_P, i]
     L.cpattn_last_error.restype = ctypes.c_char_p
     L.cpattn_last_error.argtypes = []
     L.cpattn_version.restype = ctypes.c_char_p
@@ -146,6 +148,11 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+    def set_reserved_sms(self, sms: int):
+        """Leave `sms` SMs free during this plan's forward attention launches (for transfers
+        running beside a ring step)."""
+        _check(lib().cpattn_plan_set_reserved_sms(self._h, int(sms)), "cpattn_plan_set_reserved_sms")
 
     def workspace_size(self, B: int) -> int:
         out = ctypes.c_size_t()

@@ -150,6 +150,7 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.counts = at<unsigned long long>(ws, w.counts);
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
+    a.reserved_sms = p.reserved_sms;
     return a;
 }
 
@@ -180,6 +181,14 @@ cpattn_status_t cpattn_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, cpatt
         return fail(CPATTN_ERR_INVALID, why);
     }
     *out = reinterpret_cast<cpattn_plan_t>(p);
+    return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_set_reserved_sms(cpattn_plan_t plan, int sms) {
+    Plan* p = as_plan(plan);
+    if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
+    if (sms < 0 || sms > 1024) return fail(CPATTN_ERR_INVALID, "reserved SMs must lie in 0..1024");
+    p->reserved_sms = sms;
     return CPATTN_OK;
 }
 
@@ -1085,6 +1094,7 @@ cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, in
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
+    a.reserved_sms = p->reserved_sms;
     std::string why;
     int e = launch_attn(a, reinterpret_cast<cudaStream_t>(stream), &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);

@@ -1054,7 +1054,9 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
         return (int)cudaErrorInvalidValue;
     }
     P.num_units = (int)units;
-    const int grid = (int)(units < sms ? units : sms);
+    // one CTA per SM, leaving the reserved SMs free for concurrent transfers
+    const int avail = sms - a.reserved_sms > 0 ? sms - a.reserved_sms : 1;
+    const int grid = (int)(units < avail ? units : avail);
     const int n_rg = a.n_cp * a.n_grp;
     unit_tiles_kernel<M><<<(n_rg + 127) / 128, 128, 0, st>>>(P);
     ring_attention_kernel<D, M><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);

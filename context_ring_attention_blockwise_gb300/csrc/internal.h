@@ -99,6 +99,8 @@ struct Plan {
     // Ulysses plans (cpattn_ulysses_plan): the attention above is the per-rank problem (T tokens,
     // h / u_ncp query heads, its KV heads, one rank); these are the outer shape. 0 otherwise.
     int u_ncp = 0, u_h = 0, u_nkv = 0;
+    // SMs the persistent attention launches leave free (cpattn_plan_set_reserved_sms)
+    int reserved_sms = 0;
 };
 
 // One-time set-up per device (kernel attributes), safe when several host threads drive several
@@ -171,6 +173,7 @@ struct AttnLaunch {
     int64_t kv_rank_rows = 0;  // all-gather: K/V rows between the gathered copies of consecutive ranks
     uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
     int doc_ids = 0;           // loL / tile_lo hold document ids (else a per-query lower bound)
+    int reserved_sms = 0;      // SMs the persistent grid leaves free for concurrent work
     unsigned long long* walk_bits = nullptr;   // document ids: [n_cp * n_grp][n_cp][ceil(n_qt / 64)] scratch
 };
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why);

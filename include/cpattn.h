@@ -67,6 +67,14 @@ cpattn_status_t cpattn_plan(int64_t T, int h, int n_kv, int d_k, int n_cp, cpatt
                             cpattn_plan_t* out);
 cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan);
 
+/* The attention kernel is persistent: one CTA per SM holds the SM's whole register file until the
+ * work runs out, so work on other streams that needs SMs (a device-to-device copy of the ring's
+ * next block, a communication library's transfer kernel) waits for the launch's tail. With sms > 0
+ * the plan's forward attention launches leave that many SMs free, so such transfers can run beside
+ * the step they must precede ([CEX] "When the ring hides its communication"). Default 0; a value
+ * at or above the device's SM count leaves one CTA. Host only. */
+cpattn_status_t cpattn_plan_set_reserved_sms(cpattn_plan_t plan, int sms);
+
 /* Workspace bytes for cpattn_forward / cpattn_permute with batch B. */
 cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 /* Workspace bytes for the ring-step path (permute + ring_step + finalize): the forward

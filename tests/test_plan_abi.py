@@ -197,3 +197,12 @@ def test_allgather_bytes_match_the_oracle(T, h, n_kv, d, n_cp, layout, B):
     assert np.all(got == plan.counts(B)["kv_bytes_recv"])   # the same volume as the ring
     if T == 131072 and n_kv == 1:
         assert int(got[0]) == 62914560
+
+
+def test_reserved_sms_host_checks():
+    plan = cp.Plan(2048, 4, 2, 128, 4, "zigzag")
+    plan.set_reserved_sms(8)
+    plan.set_reserved_sms(0)
+    L = cp.lib()
+    assert L.cpattn_plan_set_reserved_sms(plan.handle, -1) == 1
+    assert L.cpattn_plan_set_reserved_sms(None, 4) == 1
