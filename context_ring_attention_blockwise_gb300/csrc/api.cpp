@@ -97,7 +97,8 @@ const int32_t* order_src(Plan& p, int which) {
 // upload_by_param: the order table goes to the device inside kernel parameters, so nothing is
 // allocated (no page-locked copy is made) and nothing is staged from pageable memory.
 cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
-                         cudaStream_t st, const int32_t* lo = nullptr, bool upload_by_param = false) {
+                         cudaStream_t st, const int32_t* lo = nullptr, bool upload_by_param = false,
+                         bool v_f16 = true) {
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
@@ -118,6 +119,8 @@ cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const voi
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(ws, w.kL); a.vL = at<char>(ws, w.vL);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
     a.lo = lo; a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo);
+    a.v_f16 = v_f16 ? 1 : 0;
+    a.header = at<uint32_t>(ws, w.header);
     e = cpattn::launch_permute(a, st);
     if (e) return cuda_fail(e, "permute kernel");
     return CPATTN_OK;
@@ -348,7 +351,7 @@ cpattn_status_t backward_prepare(Plan& p, int B, const void* q, const void* k, c
         return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
                                               std::to_string(ws_bytes));
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
-    if ((s = prologue(p, B, q, k, v, pos, ws, st, lo))) return s;
+    if ((s = prologue(p, B, q, k, v, pos, ws, st, lo, false, false))) return s;   // the backward reads bf16 V
     cpattn::BwdPrepArgs pa{};
     pa.B = B; pa.T = p.T; pa.n = p.n; pa.m = p.m; pa.h = p.h; pa.d = p.d; pa.n_cp = p.n_cp;
     pa.layout = p.layout; pa.n_qt = p.n_qt;
@@ -1047,6 +1050,8 @@ cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, c
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(slot, w.slot_k); a.vL = at<char>(slot, w.slot_v);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
     a.dflt_ncp = p->n_cp; a.dflt_layout = p->layout; a.dflt_rank0 = rank0; a.dflt_m = p->m;
+    a.v_f16 = 1;
+    a.header = at<uint32_t>(ws, w.header);
     if ((e = cpattn::launch_permute(a, st))) return cuda_fail(e, "permute kernel");
     // each block carries its position tables with it around the ring
     e = cudaMemcpyAsync(at<char>(slot, w.slot_pos), at<char>(ws, w.posL), w.blk_pos * R, cudaMemcpyDeviceToDevice, st);
@@ -1172,6 +1177,9 @@ cpattn_status_t cpattn_check(cpattn_plan_t plan, const void* ws) {
     uint32_t hdr[2] = {0, 0};
     int e = cudaMemcpy(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost);
     if (e) return cuda_fail(e, "cudaMemcpy(header)");
+    if (hdr[cpattn::kErrFlags] & cpattn::kErrRangeFlag)
+        return fail(CPATTN_ERR_INVALID, "v holds a value outside the fp16 range (|v| > 65504, inf or NaN): the "
+                                        "forward's P V product runs in fp16; the outputs were not computed");
     if (hdr[cpattn::kErrFlags] & cpattn::kErrTimeoutFlag) {
         char buf[128];
         std::snprintf(buf, sizeof buf, "device wait timed out (wait site %u)", hdr[cpattn::kErrWhere]);

@@ -28,9 +28,9 @@
 //   warps 2, 3  idle.
 //   warps 4..7  softmax warpgroup 0 (query tile 0), one thread per row.
 //   warps 8..11 softmax warpgroup 1 (query tile 1). Each thread reads its row of S from TMEM,
-//               masks, takes the max, exponentiates with exp2, sums, writes P (bf16) back over
+//               masks, takes the max, exponentiates with exp2, sums, writes P (fp16) back over
 //               S in TMEM, rescales O lazily, and writes the unit's output.
-// Tensor memory (512 columns): S0 at 0, S1 at 128 (P_i packed bf16x2 over the first 64 columns
+// Tensor memory (512 columns): S0 at 0, S1 at 128 (P_i packed fp16x2 over the first 64 columns
 // of S_i), O0 at 256, O1 at 256 + d_k.
 //
 // MMAs from the issuing thread execute in order. So QK_i of the next tile, which overwrites
@@ -518,7 +518,7 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
                            volatile int* unit_slot, const Bars<D>& bars, const Waiter& wait) {
     using C = Cfg<D>;
     constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);   // A = Q (K-major), B = K (K-major)
-    constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);     // A = P (TMEM), B = V (MN-major)
+    constexpr uint32_t kIdescPV = idesc_f16(128, D, 0, 1);      // A = P (TMEM, fp16), B = V (MN-major, fp16)
     int nk = 0, nv = 0, nq = 0, npv = 0, nunits = 0;   // K, V, Q consumed; PV tiles; units with tiles
     bool ok = true;
     auto issue_qk = [&](int i, int kst) {
@@ -631,9 +631,8 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         const int qpos = row_valid ? __ldg(P.posL + (int64_t)U.r * P.n + jl) : 0;
         // the query's lowest visible key position, or its document id
         const int qlo = ((LB || DOC) && row_valid) ? __ldg(P.loL + (int64_t)U.r * P.n + jl) : INT_MIN;
-        // l: sum of the fp32 exponentials (for lse); lr: the same values rounded to bf16 as the PV
-        // product sees them (normalises O, so the weights applied to V sum to one exactly).
-        float m_used = -INFINITY, l = 0.f, lr = 0.f;
+        // l: sum of the fp32 exponentials (for lse and the normaliser of O)
+        float m_used = -INFINITY, l = 0.f;
         const bool counter = (row == 0) && member_valid;       // one thread tallies computed tiles
         int cnt_s = -1;
         unsigned long long cnt_full = 0, cnt_diag = 0;
@@ -707,29 +706,23 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             if (resc) {
                 alpha = ex2(m_used - m_new);
                 l *= alpha;
-                lr *= alpha;
                 m_used = m_new;
             }
             const float msub = (m_used == -INFINITY) ? 0.f : -m_used;
             const uint64_t neg_m2 = f2_pack(msub, msub);
             uint32_t pk[64];
             uint64_t sum2[4] = {0, 0, 0, 0};                          // packed pairs of +0.0f
-            float rlo[4] = {0.f, 0.f, 0.f, 0.f}, rhi[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 float a0, a1;
                 f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), scale2, neg_m2), a0, a1);
                 const float p0 = ex2(a0), p1 = ex2(a1);
-                pk[c] = pack_bf16(p0, p1);
+                pk[c] = pack_f16(p0, p1);
                 sum2[c & 3] = f2_add(sum2[c & 3], f2_pack(p0, p1));
-                add_bf16x2_f32(rlo[c & 3], rhi[c & 3], pk[c]);
             }
-            float s0, s1, r0, r1;
+            float s0, s1;
             f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s0, s1);
-            r0 = (rlo[0] + rlo[1]) + (rlo[2] + rlo[3]);
-            r1 = (rhi[0] + rhi[1]) + (rhi[2] + rhi[3]);
             l += s0 + s1;
-            lr += r0 + r1;
             // P_i over the first 64 columns of S_i: column c holds keys 2c (low half) and 2c + 1.
             tmem_st64(tmem + lane_base + s_col, pk);
             if (j > 0 && __any_sync(0xffffffffu, resc)) {
@@ -765,7 +758,7 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
             if (!ok) break;
             tc_fence_after();
         }
-        const float inv_l = lr > 0.f ? 1.0f / lr : 0.f;
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
         const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
         // Output in 32-column chunks of O_i (bounded register use while loading and storing).
         uint4* dst = nullptr;                 // fused: bf16 row in natural order

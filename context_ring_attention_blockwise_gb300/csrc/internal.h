@@ -19,7 +19,7 @@ constexpr int kBlockK = 128;   // keys per tile (the QK^T MMA N, the PV MMA K)
 
 // Workspace header words (uint32), written by kernels, read by cpattn_check.
 enum HeaderWord : int { kErrFlags = 0, kErrWhere = 1, kHeaderWords = 64 };
-enum ErrFlag : uint32_t { kErrTimeoutFlag = 1u };
+enum ErrFlag : uint32_t { kErrTimeoutFlag = 1u, kErrRangeFlag = 2u };
 
 // Byte offsets of the regions inside the caller's workspace, all 1024-aligned.
 struct WsLayout {
@@ -145,6 +145,8 @@ struct PermuteArgs {
     // one process of a multi-process ring holds); otherwise it is the natural index here.
     int dflt_ncp = 0, dflt_layout = 0, dflt_rank0 = 0;
     int64_t dflt_m = 0;
+    int v_f16 = 0;   // write V in fp16 (exact for |v| <= 65504) for the forward's fp16 P V product
+    uint32_t* header = nullptr;   // v_f16: a value outside the fp16 range sets kErrRangeFlag here
 };
 int launch_permute(const PermuteArgs& a, void* stream);
 

@@ -3,6 +3,13 @@
 // scatter of the ring-step paths back to natural order, the backward ring-step path's add of a
 // circulating gradient block, and the standalone log-sum-exp merge.
 //
+// For the forward, placement also writes V in fp16: the attention kernel multiplies fp16 P by fp16
+// V (the tensor core wants one type for both operands), so that P carries three more significand
+// bits than bf16 and O is normalised by the plain fp32 sum of the exponentials. bf16 to fp16 is
+// exact for 2^-14 <= |v| <= 65504; below 2^-14 (fp16 subnormals) the absolute error is at most
+// 2^-25, and a value beyond 65504 (or an infinite or NaN one) is recorded in the workspace header
+// for cpattn_check to report.
+//
 // Placement: "Context and expert parallelism", section "The causal mask unbalances the
 // sequence" (contiguous, zigzag and round-robin stripes) and section "In PyTorch" (every
 // position-indexed tensor is sharded with the sequence, so position ids travel with tokens).
@@ -123,7 +130,7 @@ __global__ void __launch_bounds__(256, 4) permute_kernel(const uint4* __restrict
                                                       const uint4* __restrict__ v, uint4* __restrict__ qL,
                                                       uint4* __restrict__ kL, uint4* __restrict__ vL, int B, int64_t T,
                                                       int64_t n, int64_t m, int h, int n_kv, int d, int n_cp,
-                                                      int layout) {
+                                                      int layout, int v_f16, uint32_t* __restrict__ header) {
     const int lg = (d == 128) ? 4 : 3;                      // log2 of the 16-byte pieces per head row
     const int cpr = 1 << lg;
     const int per_row = (h + 2 * n_kv) * cpr;
@@ -151,6 +158,20 @@ __global__ void __launch_bounds__(256, 4) permute_kernel(const uint4* __restrict
                     else if (hh < h + n_kv) { src = k; dst = kL; heads = n_kv; hd = hh - h; }
                     else { src = v; dst = vL; heads = n_kv; hd = hh - h - n_kv; }
                     x[u] = __ldg(src + (rw * heads + hd) * cpr + c);
+                    if (v_f16 && hh >= h + n_kv) {
+                        // bf16 -> fp16: exact for |v| <= 65504 (fp16 has more significand bits)
+                        uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const float lo = __uint_as_float(w[q2] << 16), hi = __uint_as_float(w[q2] & 0xFFFF0000u);
+                            uint32_t r;
+                            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+                            w[q2] = r;
+                            // all-ones exponent: |v| beyond 65504, or an infinite or NaN input
+                            if ((r & 0x7C00u) == 0x7C00u || (r & 0x7C000000u) == 0x7C000000u)
+                                atomicOr(header + kErrFlags, (uint32_t)kErrRangeFlag);
+                        }
+                    }
                     dp[u] = dst + ((rb * heads + hd) * n + j) * cpr + c;
                 }
             }
@@ -452,7 +473,7 @@ int launch_permute(const PermuteArgs& a, void* stream) {
     permute_kernel<<<(int)(rows < cap ? rows : cap), 256, 0, st>>>(
         static_cast<const uint4*>(a.q), static_cast<const uint4*>(a.k), static_cast<const uint4*>(a.v),
         static_cast<uint4*>(a.qL), static_cast<uint4*>(a.kL), static_cast<uint4*>(a.vL), a.B, a.T, a.n, a.m, a.h,
-        a.n_kv, a.d, a.n_cp, a.layout);
+        a.n_kv, a.d, a.n_cp, a.layout, a.v_f16, a.header);
     return (int)cudaGetLastError();
 }
 

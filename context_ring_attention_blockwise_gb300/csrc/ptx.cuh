@@ -45,15 +45,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// acc_lo += low bf16 of pk, acc_hi += high bf16 of pk: each bf16 is widened exactly and added in
-// fp32 (round to nearest), with no integer unpacking of the pair.
-__device__ __forceinline__ void add_bf16x2_f32(float& acc_lo, float& acc_hi, uint32_t pk) {
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
-        : "+f"(acc_lo), "+f"(acc_hi)
-        : "r"(pk));
-}
-
 // ---- TMA -----------------------------------------------------------------------------------
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -211,7 +202,8 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: A (M x K, 16-bit, two elements per 32-bit column) is read from
-// tensor memory at a_tmem; B from shared memory through its descriptor. One thread issues.
+// tensor memory at a_tmem; B from shared memory through its descriptor. One thread issues. kind::f16:
+// the element type, fp16 or bf16 and the same for A and B, comes from the instruction descriptor.
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
@@ -278,6 +270,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 // two floats -> bf16x2 (round to nearest even), `lo` in the low half
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -309,6 +306,11 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and B (bits 7-9
 // and 10-12 = 1), A/B major-ness (bit 15 / 16: 0 = K-major, 1 = MN-major), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
+// fp16 A and B (same type), fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn_major << 15) | ((uint32_t)b_mn_major << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

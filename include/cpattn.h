@@ -24,6 +24,11 @@
  *     message is available from cpattn_last_error() on the same thread.
  *   - Device-side errors (a bounded wait that ran out) are recorded in the workspace header
  *     and reported by cpattn_check. No call traps, asserts on the device or throws.
+ *   - Forward calls multiply the exponentials P by V in fp16 (both tensor-core operands fp16, fp32
+ *     accumulation): V is converted from bf16 during placement, exactly for 2^-14 <= |v| <= 65504
+ *     (below 2^-14 within 2^-25). A V value beyond 65504, infinite or NaN makes the call compute
+ *     nothing; cpattn_check (cpattn_check_noalloc) then returns CPATTN_ERR_INVALID saying so.
+ *     The backward calls keep V in bf16.
  *   - There is no CPU fallback: without a usable sm_103a device, calls return CPATTN_ERR_CUDA.
  */
 #ifndef CPATTN_H

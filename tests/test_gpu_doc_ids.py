@@ -88,7 +88,12 @@ def test_one_token_documents_return_their_own_values():
     plan = cp.Plan(T, h, n_kv, d, n_cp, "striped", False)
     o, lse = run_docs(q, k, v, plan, doc)
     vb = synth.bf16_bits_to_f32(v)
-    assert np.array_equal(o.float().cpu().numpy(), vb), "a lone token must return its own value row"
+    on = o.float().cpu().numpy()
+    # O = P V / l with P = 1 and V in fp16: exact wherever V converts exactly (|v| >= 2^-14), within
+    # the fp16 subnormal spacing below that
+    exact = np.abs(vb) >= 2.0 ** -14
+    assert np.array_equal(on[exact], vb[exact]), "a lone token must return its own value row"
+    assert np.max(np.abs(on - vb)) <= 2.0 ** -24
     ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=False)
     compare(o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, what="one-token documents")
 

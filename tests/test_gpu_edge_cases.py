@@ -78,3 +78,40 @@ def test_tiny_ulysses(case):
     cp.check(plan, ws)
     ref_o, ref_lse = oracle.get().attention(q, k, v, causal=True)
     compare(o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, what=f"tiny ulysses {case}")
+
+
+@pytest.mark.parametrize("bits,what", [(0x47C3, "99840"), (0x7F80, "inf"), (0xFFC0, "NaN")])
+def test_v_outside_the_fp16_range_is_reported(bits, what):
+    """The forward multiplies P by V in fp16: a V value beyond 65504 (or infinite, or NaN) cannot be
+    converted, so the call computes nothing and cpattn_check says why; the next call with values in
+    range clears the record."""
+    T, h, n_kv, d, n_cp = 512, 2, 2, 128, 4
+    q, k, v = inputs(7, 1, T, h, n_kv, d)
+    bad = v.copy()
+    bad[0, 100, 1, 5] = bits
+    plan = cp.Plan(T, h, n_kv, d, n_cp, "zigzag", True)
+    ws = cp.alloc_workspace(plan.workspace_size(1))
+    qd, kd = to_device_bf16(q), to_device_bf16(k)
+    cp.forward(qd, kd, to_device_bf16(bad), plan, ws=ws)
+    torch.cuda.synchronize()
+    with pytest.raises(cp.CpattnError) as e:
+        cp.check(plan, ws)
+    assert e.value.status == 1 and "fp16 range" in str(e.value), what
+    o, lse = cp.forward(qd, kd, to_device_bf16(v), plan, ws=ws)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    ref_o, ref_lse = oracle.get().attention(q, k, v, causal=True)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, what="after an out-of-range call")
+
+
+def test_v_at_the_fp16_limits_is_exact():
+    """V values at 65504 (the largest fp16) and below 2^-14 (fp16 subnormals) go through."""
+    T, h, n_kv, d, n_cp = 256, 2, 1, 64, 2
+    q, k, v = inputs(8, 1, T, h, n_kv, d)
+    v = v.copy()
+    v[0, :, 0, 0] = 0x477F          # 65280, exact in fp16
+    v[0, :, 0, 1] = 0x3880          # 2^-14 * 1.0 = 6.1e-5
+    v[0, :, 0, 2] = 0x3400          # 2^-23: an fp16 subnormal
+    o, lse, plan, ws = run(q, k, v, n_cp, 0)
+    ref_o, ref_lse = oracle.get().attention(q, k, v, causal=True)
+    compare(o, lse, ref_o, ref_lse, what="V at the fp16 limits")
