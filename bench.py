@@ -745,6 +745,20 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     cp.check(plan, ws)
     ms = a.elapsed_time(b) / 3
     out["document_ids"] = {"ms": ms, "documents": len(lengths), "ids": "shuffled", "tflops_eff": flops_docs / (ms * 1e-3) / 1e12}
+    # short documents: 64 of 2048 tokens (the unit boundaries dominate)
+    lo64 = torch.from_numpy((np.arange(w.T) // 2048 * 2048).astype(np.int32)).to(dev)
+    flops64 = 4.0 * w.B * w.h * w.d * (w.T // 2048) * (2048 * 2049 // 2)
+    cp.forward_masked(q, k, v, plan, lo64, ws=ws, out=od, lse=lsed, stream=stream)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(3):
+        cp.forward_masked(q, k, v, plan, lo64, ws=ws, out=od, lse=lsed, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    ms = a.elapsed_time(b) / 3
+    out["documents_64x2k"] = {"ms": ms, "documents": w.T // 2048, "tflops_eff": flops64 / (ms * 1e-3) / 1e12}
+    del lo64
     del od, lsed, lo, docd
     # the backward pass: dq, dk, dv from the forward's o and lse and a synthetic output gradient
     wsb = cp.alloc_workspace(plan.backward_workspace_size(w.B), dev)

@@ -146,6 +146,7 @@ cpattn::AttnLaunch attn_args(const Plan& p, int B, float scale, void* ws) {
     a.walk_tab = at<int32_t>(ws, w.walk_tab);
     a.walk_nz = at<unsigned long long>(ws, w.walk_nz);
     a.walk_bits = at<unsigned long long>(ws, w.walk_bits);
+    a.order_scratch = at<int32_t>(ws, w.order_masked);
     a.scale_log2 = resolve_scale(p, scale);
     a.qL = at<char>(ws, w.qL);
     a.kv_k = at<char>(ws, w.kL); a.kv_v = at<char>(ws, w.vL);

@@ -989,6 +989,23 @@ __global__ void unit_tiles_kernel(const Params P) {
     P.unit_tiles[rg] = c;
 }
 
+// Under a mask the plan's longest-first order (from positions alone) says little about the work of
+// a row group: one block sorts the row groups by the tile counts unit_tiles_kernel just wrote,
+// most tiles first (ties by index), so the persistent CTAs start the heaviest units first.
+constexpr int kSortMax = 8192;
+__global__ void __launch_bounds__(1024) order_by_tiles_kernel(const int32_t* __restrict__ tiles,
+                                                             int32_t* __restrict__ order, int n) {
+    __shared__ int32_t t[kSortMax];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) t[i] = tiles[i];
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ti = t[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) rank += (t[j] > ti) || (t[j] == ti && j < i);
+        order[rank] = i;
+    }
+}
+
 // ---- host side -------------------------------------------------------------------------------
 template <int D, int M>
 int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
@@ -1052,6 +1069,10 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     const int grid = (int)(units < avail ? units : avail);
     const int n_rg = a.n_cp * a.n_grp;
     unit_tiles_kernel<M><<<(n_rg + 127) / 128, 128, 0, st>>>(P);
+    if (M != kMaskPos && a.order_scratch && n_rg <= kSortMax) {
+        order_by_tiles_kernel<<<1, 1024, 0, st>>>(P.unit_tiles, a.order_scratch, n_rg);
+        P.order = a.order_scratch;
+    }
     ring_attention_kernel<D, M><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }

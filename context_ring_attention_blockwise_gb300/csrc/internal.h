@@ -38,6 +38,7 @@ struct WsLayout {
     size_t walk_tab = 0;    // int32 [n_cp * n_qt][n_cp]: document masks: visited key-tile range per row group and step
     size_t walk_nz = 0;     // uint64 [n_cp * n_qt]: document masks: the steps with visited tiles
     size_t walk_bits = 0;   // uint64 [n_cp * n_qt][n_cp][ceil(n_qt / 64)]: document ids: visited key tiles
+    size_t order_masked = 0;  // int32 [n_cp * n_qt]: masks: row groups by the masked walk's tile counts
     size_t qL = 0;          // bf16 [n_cp][B][h][n][d]
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
@@ -176,6 +177,7 @@ struct AttnLaunch {
     uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
     int doc_ids = 0;           // loL / tile_lo hold document ids (else a per-query lower bound)
     int reserved_sms = 0;      // SMs the persistent grid leaves free for concurrent work
+    int32_t* order_scratch = nullptr;  // masks: [n_cp * n_grp] row groups sorted by this launch's tile counts
     unsigned long long* walk_bits = nullptr;   // document ids: [n_cp * n_grp][n_cp][ceil(n_qt / 64)] scratch
 };
 int launch_attention(const AttnLaunch& a, void* stream, std::string* why);

@@ -41,6 +41,7 @@ WsLayout ws_layout(const Plan& p, int B) {
     w.walk_tab = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt * p.n_cp);
     w.walk_nz = take(sizeof(uint64_t) * (size_t)p.n_cp * p.n_qt);
     w.walk_bits = take(sizeof(uint64_t) * (size_t)p.n_cp * p.n_qt * p.n_cp * (((size_t)p.n_qt + 63) / 64));
+    w.order_masked = take(sizeof(int32_t) * (size_t)p.n_cp * p.n_qt);
     w.qL = take(2 * (size_t)B * T * p.h * d);
     w.kL = take(2 * (size_t)B * T * p.n_kv * d);
     w.vL = take(2 * (size_t)B * T * p.n_kv * d);
