@@ -200,6 +200,7 @@ struct Unit {
     int2 qmm[2];   // position range of each query tile; (INT_MAX, INT_MIN) for a missing tile
     int2 qlo[2];   // range of the tile's lowest visible key positions (document ids: range of its ids);
                    // (INT_MIN, INT_MIN) without one
+    unsigned long long qbits[2];   // document ids: a bit per id modulo 64 in the tile; 0 without one
 };
 
 // The query tiles' position ranges and (with a per-query lower bound or document ids) the range of
@@ -213,12 +214,15 @@ __device__ __forceinline__ void unit_ranges(const Params& P, Unit& U) {
             if (M != kMaskPos) {
                 const int4 l4 = __ldg(P.tile_lo + U.r * P.n_qt + U.qt[i]);
                 U.qlo[i] = make_int2(l4.x, l4.y);
+                U.qbits[i] = (unsigned long long)(unsigned)l4.z | ((unsigned long long)(unsigned)l4.w << 32);
             } else {
                 U.qlo[i] = make_int2(INT_MIN, INT_MIN);
+                U.qbits[i] = 0ull;
             }
         } else {
             U.qmm[i] = make_int2(INT_MAX, INT_MIN);
             U.qlo[i] = make_int2(INT_MIN, INT_MIN);
+            U.qbits[i] = 0ull;
         }
     }
 }
@@ -258,12 +262,15 @@ __device__ __forceinline__ Unit decode_unit(const Params& P, int u) {
     return U;
 }
 
-// Block class of a key tile for one query tile under document ids: SKIP when no id is shared or (causal)
-// every key follows every query; FULL when both tiles hold one id, the same, and every key precedes
-// every query; otherwise partly visible (the element mask decides).
-__device__ __forceinline__ int doc_class(int causal, int qmin, int qmax, int dqmin, int dqmax, const int4& t4,
-                                         const int4& d4) {
+// Block class of a key tile for one query tile under document ids: SKIP when no id can be shared (the
+// id ranges are disjoint, or no id modulo 64 is in both tiles) or (causal) every key follows every
+// query; FULL when both tiles hold one id, the same, and every key precedes every query; otherwise
+// partly visible (the element mask decides).
+__device__ __forceinline__ int doc_class(int causal, int qmin, int qmax, int dqmin, int dqmax,
+                                         unsigned long long qbits, const int4& t4, const int4& d4) {
     if (d4.y < dqmin || d4.x > dqmax) return CPATTN_TILE_SKIP;
+    const unsigned long long kbits = (unsigned long long)(unsigned)d4.z | ((unsigned long long)(unsigned)d4.w << 32);
+    if ((qbits & kbits) == 0ull) return CPATTN_TILE_SKIP;
     const int pc = !causal ? CPATTN_TILE_FULL : (t4.x > qmax) ? CPATTN_TILE_SKIP
                                               : (t4.y > qmin) ? CPATTN_TILE_DIAG : CPATTN_TILE_FULL;
     if (pc == CPATTN_TILE_SKIP) return CPATTN_TILE_SKIP;
@@ -284,6 +291,7 @@ struct TileWalk {
     int r, s, s_end, kt, src;
     int qmin0, qmax0, qmin1, qmax1, qmax, cls0, cls1, mask0, mask1;
     int lmin0, lmax0, lmin1, lmax1;   // lower-bound ranges of the two query tiles
+    unsigned long long qbits0, qbits1;   // document ids: the query tiles' id-bit masks
     __device__ int cls(int i) const { return i ? cls1 : cls0; }
     __device__ int mask(int i) const { return i ? mask1 : mask0; }
     __device__ void init(const Params& P, const Unit& U) {
@@ -293,6 +301,7 @@ struct TileWalk {
         qmin1 = U.qmm[1].x; qmax1 = U.qmm[1].y;
         lmin0 = U.qlo[0].x; lmax0 = U.qlo[0].y;
         lmin1 = U.qlo[1].x; lmax1 = U.qlo[1].y;
+        qbits0 = U.qbits[0]; qbits1 = U.qbits[1];
         qmax = max(qmax0, qmax1);
         s = P.fused ? 0 : P.step;
         s_end = P.fused ? P.n_cp : P.step + 1;
@@ -332,8 +341,8 @@ struct TileWalk {
             const int short_tile = (kt == P.n_qt - 1) && (P.n % 128) != 0;
             const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
             const int4 d4 = __ldg(P.tile_lo + src * P.n_qt + kt);
-            cls0 = doc_class(P.causal, qmin0, qmax0, lmin0, lmax0, t4, d4);
-            cls1 = doc_class(P.causal, qmin1, qmax1, lmin1, lmax1, t4, d4);
+            cls0 = doc_class(P.causal, qmin0, qmax0, lmin0, lmax0, qbits0, t4, d4);
+            cls1 = doc_class(P.causal, qmin1, qmax1, lmin1, lmax1, qbits1, t4, d4);
             if (cls0 == CPATTN_TILE_SKIP && cls1 == CPATTN_TILE_SKIP) continue;
             mask0 = (cls0 != CPATTN_TILE_FULL) || short_tile;
             mask1 = (cls1 != CPATTN_TILE_FULL) || short_tile;
@@ -944,8 +953,10 @@ __global__ void unit_tiles_kernel(const Params P) {
                     if (kt >= P.n_qt) break;
                     const int4 t4 = __ldg(P.ktile_mm + src * P.n_qt + kt);
                     const int4 d4 = __ldg(P.tile_lo + src * P.n_qt + kt);
-                    const int c0 = doc_class(P.causal, U.qmm[0].x, U.qmm[0].y, U.qlo[0].x, U.qlo[0].y, t4, d4);
-                    const int c1 = doc_class(P.causal, U.qmm[1].x, U.qmm[1].y, U.qlo[1].x, U.qlo[1].y, t4, d4);
+                    const int c0 =
+                        doc_class(P.causal, U.qmm[0].x, U.qmm[0].y, U.qlo[0].x, U.qlo[0].y, U.qbits[0], t4, d4);
+                    const int c1 =
+                        doc_class(P.causal, U.qmm[1].x, U.qmm[1].y, U.qlo[1].x, U.qlo[1].y, U.qbits[1], t4, d4);
                     if (c0 != CPATTN_TILE_SKIP || c1 != CPATTN_TILE_SKIP) {
                         bits |= 1ull << b;
                         ++c;

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restric
     const int r = blockIdx.x / n_qt, tile = blockIdx.x % n_qt;
     const int64_t j = (int64_t)tile * kBlockQ + threadIdx.x;
     int lo = INT_MAX, hi = INT_MIN, blo = INT_MAX, bhi = INT_MIN;
+    unsigned bm_lo = 0u, bm_hi = 0u;   // document ids: a bit per id modulo 64 present in the tile
     if (j < n) {
         int64_t t = token_of_dev(layout, r, j, n, m, n_cp);
         const int dflt = dp.n_cp > 0 ? (int)token_of_dev(dp.layout, dp.rank0 + r, j, n, dp.m, dp.n_cp) : (int)t;
@@ -72,8 +73,13 @@ __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restric
             const int bv = lob[t];
             loL[(int64_t)r * n + j] = bv;
             blo = bhi = bv;
+            const unsigned bit = (unsigned)bv & 63u;
+            if (bit < 32u) bm_lo = 1u << bit;
+            else bm_hi = 1u << (bit - 32u);
         }
     }
+    bm_lo = __reduce_or_sync(0xffffffffu, bm_lo);
+    bm_hi = __reduce_or_sync(0xffffffffu, bm_hi);
     for (int o = 16; o > 0; o >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
         hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
@@ -81,18 +87,22 @@ __global__ void __launch_bounds__(128) pos_tiles_kernel(const int32_t* __restric
         bhi = max(bhi, __shfl_xor_sync(0xffffffffu, bhi, o));
     }
     __shared__ int slo[4], shi[4], sblo[4], sbhi[4];
+    __shared__ unsigned sbm[4][2];
     if ((threadIdx.x & 31) == 0) {
         slo[threadIdx.x >> 5] = lo; shi[threadIdx.x >> 5] = hi;
         sblo[threadIdx.x >> 5] = blo; sbhi[threadIdx.x >> 5] = bhi;
+        sbm[threadIdx.x >> 5][0] = bm_lo; sbm[threadIdx.x >> 5][1] = bm_hi;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < 4; ++w) {
             lo = min(lo, slo[w]); hi = max(hi, shi[w]);
             blo = min(blo, sblo[w]); bhi = max(bhi, sbhi[w]);
+            bm_lo |= sbm[w][0]; bm_hi |= sbm[w][1];
         }
         tile_mm[blockIdx.x] = make_int4(lo, hi, lo, 0);
-        if (lob) tile_lo[blockIdx.x] = make_int4(blo, bhi, 0, 0);
+        // (min, max) of the bound or id; with document ids, .z/.w hold the 64-bit id-bit mask
+        if (lob) tile_lo[blockIdx.x] = make_int4(blo, bhi, (int)bm_lo, (int)bm_hi);
     }
 }
 
