@@ -38,7 +38,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
 # scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
 # to be re-read once two KV heads in flight fill L2.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"d07995b6184ddaf0": {"llama70b_zigzag_T128k": (4 * (673276416 + 491100416),
+                                                        "one-launch ncu capture at T=32768 (673,276,416 B read + "
+                                                        "491,100,416 B written) scaled by the work units (x4); a lower "
+                                                        "bound at 128K")}}
 
 
 def attention_source_hash() -> str:
