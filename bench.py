@@ -363,7 +363,7 @@ def run_gpu_ring(args, w):
     timeline = hop_summary([t0.elapsed_time(ce) for ce, _ in marks], [t0.elapsed_time(xe) for _, xe in marks], False)
     peaks, peak_src = load_peaks()
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    n_grp = plan.counts(w.B)  # host call; keeps the plan's counters in the line
+    plan_counts = plan.counts(w.B)
     uploads = -(-(R * ((w.T // w.n_cp + 127) // 128)) // 960)
     result = None
     if rank == 0:
@@ -383,7 +383,7 @@ def run_gpu_ring(args, w):
             "ring": {"processes": world, "ranks_per_process": R,
                      "kv_bytes_recv_per_rank": int(ring.counters.kv[0] - kv_before),
                      "timeline": timeline,
-                     "kv_bytes_recv_per_rank_pages": int(n_grp["kv_bytes_recv"][0]),
+                     "kv_bytes_recv_per_rank_pages": int(plan_counts["kv_bytes_recv"][0]),
                      "transport": "NCCL send/recv" if world > 1 else "none (one process holds the ring)"},
             # per step: the order upload, placement (pos_tiles, tile_suffix, permute), per ring step
             # the tile counts and the attention kernel, and the write-back
