@@ -77,6 +77,18 @@ def flops_eff(w) -> float:
     return 4.0 * w.B * w.h * w.d * pairs
 
 
+def clock_adjusted(achieved: float, peak_tf: float, peaks: dict, clocks):
+    """The achieved rate per GHz of the median SM clock during the timed region, and the fraction of
+    the sustained peak scaled to that clock (the peak was measured at the median SM clock the peak
+    file records under load): how close the kernel is to the tensor pipe clock for clock."""
+    peak_mhz = (peaks.get("clocks_under_load") or {}).get("sm_mhz_median")
+    mhz = clocks.get("sm_mhz") if clocks else None
+    if not peak_mhz or not mhz:
+        return None
+    return {"tflops_per_ghz": achieved / (mhz / 1000.0), "peak_sm_mhz": peak_mhz, "run_sm_mhz": mhz,
+            "frac_at_run_clock": achieved / (peak_tf * mhz / peak_mhz)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -553,6 +565,8 @@ def run_gpu(args, w):
             "frac_of_peak": value / world / peak_tf,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": achieved / peak_tf,
+                         "frac_of_burst": achieved / float(peaks.get("bf16_tflops", peak_tf)),
+                         "clock_adjusted": clock_adjusted(achieved, peak_tf, peaks, clocks),
                          "traffic": args.traffic if args.traffic is not None else (None if ring else measured_traffic(w.name)[0]),
                          "traffic_how": None if ring else measured_traffic(w.name)[1],
                          "kernel": "ring_attention_kernel<128>" if not ring else "whole ring-step path",
