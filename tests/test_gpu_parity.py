@@ -167,3 +167,20 @@ def test_wait_timeout_is_reported_not_hung():
     q, k, v = inputs(1, 1, 256, 1, 1, 64)
     o, lse, plan, ws2 = run(q, k, v, 2, 0, True)
     assert np.all(np.isfinite(o))
+
+
+def test_reserved_sms_change_no_result():
+    """Leaving SMs free only changes which CTA runs a unit, not a unit's arithmetic: the fused forward
+    and the ring-step path give bit-identical results with 8 SMs left free."""
+    B, T, h, n_kv, d, n_cp = 1, 2048, 4, 2, 128, 4
+    q, k, v = inputs(71, B, T, h, n_kv, d)
+    qd, kd, vd = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, "zigzag", True)
+    o0, l0 = cp.forward(qd, kd, vd, plan)
+    r0, rl0 = cp.ring_forward(qd, kd, vd, plan)
+    plan.set_reserved_sms(8)
+    o1, l1 = cp.forward(qd, kd, vd, plan)
+    r1, rl1 = cp.ring_forward(qd, kd, vd, plan)
+    torch.cuda.synchronize()
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(l0, l1)
+    assert torch.equal(r0.view(torch.int16), r1.view(torch.int16)) and torch.equal(rl0, rl1)
