@@ -293,7 +293,7 @@ def run_gpu_ring(args, w):
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.h, R * plan.T // w.n_cp), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev, priority=-1)   # ring hops: ahead of the e2e uploads
     for _ in range(args.warmup):
         ring.forward(q, k, v, out=o, lse=lse, stream=stream, copy_stream=copy)
     torch.cuda.synchronize()

@@ -159,14 +159,16 @@ class RingProcess:
     def forward(self, q, k, v, pos=None, scale=None, out=None, lse=None, stream=None, copy_stream=None,
                 timeline=None):
         """timeline: a list to which each step appends (end of its compute, end of the hop that
-        runs beside it) as timing events on the two streams (device backend only)."""
+        runs beside it) as timing events on the two streams (device backend only). Without a
+        copy_stream the hops go to a new high-priority stream: the next step waits on them, so they
+        should not queue behind other copies the caller runs."""
         import torch
         be, R, n_cp = self.backend, self.R, self.plan.n_cp
         B, h, n = self.B, self.plan.h, self.plan.T // n_cp
         on_gpu = getattr(be, "device", None) is not None and be.device.type == "cuda"
         if on_gpu:
             compute = stream if stream is not None else torch.cuda.current_stream(be.device)
-            copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=be.device)
+            copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=be.device, priority=-1)
         else:
             compute = copy = None
         if out is None:
