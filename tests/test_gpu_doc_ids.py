@@ -129,3 +129,30 @@ def test_gqa_16k_document_pieces_sampled_rows():
     ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=True, rows=rows)
     compare(o.index_select(1, idx).float().cpu().numpy(), lse.index_select(2, idx).cpu().numpy(), ref_o, ref_lse,
             what="16K GQA document pieces")
+
+
+def test_many_row_groups_are_ordered_by_their_masked_work():
+    """2048 row groups (T = 262144 over 4 ranks): the device sort of the row groups by their masked
+    tile counts handles two per thread; lower-bound and document-id forms against the oracle on
+    sampled rows."""
+    B, T, h, n_kv, d, n_cp = 1, 262144, 2, 1, 128, 4
+    q, k, v = inputs(36, B, T, h, n_kv, d)
+    doc = pieces(T, 37, 40, lo=2000, hi=20000)
+    starts = np.concatenate([[0], np.flatnonzero(np.diff(doc)) + 1])
+    lengths = np.diff(np.concatenate([starts, [T]]))
+    lo = np.repeat(starts, lengths).astype(np.int32)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, "zigzag", True)
+    rows = synth.sample_rows(T, n_cp, 96, seed=5)
+    idx = torch.from_numpy(rows).cuda()
+    # a run may continue the previous run's id: the lower bound follows runs, the ids follow documents
+    run_id = np.cumsum(np.concatenate([[0], (np.diff(doc) != 0).astype(np.int64)])).astype(np.int32)
+    ref_o, ref_lse = oracle.get().attention_docs(q, k, v, run_id, causal=True, rows=rows)
+    ol, ll = cp.forward_masked(to_device_bf16(q), to_device_bf16(k), to_device_bf16(v), plan,
+                               torch.from_numpy(lo).cuda())
+    torch.cuda.synchronize()
+    compare(ol.index_select(1, idx).float().cpu().numpy(), ll.index_select(2, idx).cpu().numpy(), ref_o, ref_lse,
+            what="2048 row groups, lower bound")
+    od, ld = run_docs(q, k, v, plan, doc)
+    ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=True, rows=rows)
+    compare(od.index_select(1, idx).float().cpu().numpy(), ld.index_select(2, idx).cpu().numpy(), ref_o, ref_lse,
+            what="2048 row groups, document ids")
