@@ -433,7 +433,7 @@ def run_gpu(args, w):
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-    copy = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev, priority=-1)   # ring hops: the next step waits on them
     flush = None
     if w.T < 65536:   # inputs below L2 size: flush between steps
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -394,7 +394,7 @@ def ring_backward(q, k, v, o, lse, dout, plan: Plan, pos=None, scale: float | No
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     compute = stream if stream is not None else torch.cuda.current_stream()
-    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device)
+    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device, priority=-1)
     backward_begin(q, k, v, o, lse, dout, plan, ws, pos=pos, stream=compute)
     for s in range(plan.n_cp):
         backward_ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
@@ -485,7 +485,7 @@ def ring_forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=N
     if lse is None:
         lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
     compute = stream if stream is not None else torch.cuda.current_stream()
-    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device)
+    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device, priority=-1)
     permute(q, k, v, plan, ws, pos=pos, stream=compute)
     for s in range(plan.n_cp):
         ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
