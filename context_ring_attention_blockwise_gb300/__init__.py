@@ -99,7 +99,7 @@ def lib():
                                                 ctypes.c_size_t, _P]
     L.cpattn_allgather_attend.argtypes = [_P, i, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_sizes.argtypes = [_P, i, i, sz, sz, sz, sz]
-    L.cpattn_dist_begin.argtypes = [_P, i, i, i, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
+    L.cpattn_dist_begin.argtypes = [_P, i, i, i, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_step.argtypes = [_P, i, i, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_shift.argtypes = [_P, i, i, _P, _P, ctypes.c_size_t, i, _P]
     L.cpattn_dist_finalize.argtypes = [_P, i, i, i, _P, _P, _P, ctypes.c_size_t, _P]
@@ -548,11 +548,12 @@ def allgather_attend(plan: Plan, B: int, ws, out, lse, scale: float | None = Non
                                          _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_allgather_attend")
 
 
-def dist_begin(plan: Plan, B: int, rank0: int, R: int, q, k, v, ws, slot, pos=None, stream=None):
-    """cpattn_dist_begin: this process's R ranks' tokens (rank-major, each rank's local order)."""
+def dist_begin(plan: Plan, B: int, rank0: int, R: int, q, k, v, ws, slot, pos=None, stream=None, lo=None):
+    """cpattn_dist_begin: this process's R ranks' tokens (rank-major, each rank's local order);
+    lo: their per-query lower bounds (document masks) or None."""
     _check(lib().cpattn_dist_begin(plan.handle, B, rank0, R, _dev_ptr(q, "q"), _dev_ptr(k, "k"), _dev_ptr(v, "v"),
-                                   _dev_ptr(pos, "pos"), _dev_ptr(ws, "ws"), ws.numel(), _dev_ptr(slot, "slot"),
-                                   slot.numel(), _stream_ptr(stream)), "cpattn_dist_begin")
+                                   _dev_ptr(pos, "pos"), _dev_ptr(lo, "lo"), _dev_ptr(ws, "ws"), ws.numel(),
+                                   _dev_ptr(slot, "slot"), slot.numel(), _stream_ptr(stream)), "cpattn_dist_begin")
 
 
 def dist_step(plan: Plan, B: int, rank0: int, R: int, step: int, slot, ws, scale: float | None = None, stream=None):

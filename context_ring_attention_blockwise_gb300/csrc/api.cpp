@@ -1018,16 +1018,18 @@ cpattn_status_t cpattn_dist_sizes(cpattn_plan_t plan, int B, int R, size_t* ws_b
 }
 
 cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, const void* q, const void* k,
-                                  const void* v, const int32_t* pos, void* ws, size_t ws_bytes, void* slot,
-                                  size_t slot_bytes, cpattn_stream_t stream) {
+                                  const void* v, const int32_t* pos, const int32_t* lo, void* ws, size_t ws_bytes,
+                                  void* slot, size_t slot_bytes, cpattn_stream_t stream) {
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     if (!ws || !slot) return fail(CPATTN_ERR_WORKSPACE, "workspace and slot must be non-NULL");
     cpattn_status_t s = check_dist(*p, B, rank0, R, ws, ws_bytes, slot, slot_bytes);
     if (s) return s;
     if (!q || !k || !v) return fail(CPATTN_ERR_INVALID, "q, k and v must be non-NULL");
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (pos && !aligned16(pos)))
-        return fail(CPATTN_ERR_INVALID, "q, k, v and pos must be 16-byte aligned");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || (pos && !aligned16(pos)) || (lo && !aligned16(lo)))
+        return fail(CPATTN_ERR_INVALID, "q, k, v, pos and lo must be 16-byte aligned");
+    if (lo && !p->causal) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query needs a causal plan");
+    if (lo && p->n_qt > 65535) return fail(CPATTN_ERR_UNSUPPORTED, "a lower bound per query supports up to 65535 tiles per rank");
     const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
@@ -1050,6 +1052,8 @@ cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, c
     a.q = q; a.k = k; a.v = v; a.pos = pos;
     a.qL = at<char>(ws, w.qL); a.kL = at<char>(slot, w.slot_k); a.vL = at<char>(slot, w.slot_v);
     a.posL = at<int32_t>(ws, w.posL); a.tile_mm = at<int32_t>(ws, w.tile_mm);
+    // the queries' lower bounds stay with the queries: only the keys' positions travel
+    a.lo = lo; a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo);
     a.dflt_ncp = p->n_cp; a.dflt_layout = p->layout; a.dflt_rank0 = rank0; a.dflt_m = p->m;
     a.v_f16 = 1;
     a.header = at<uint32_t>(ws, w.header);
@@ -1060,7 +1064,7 @@ cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, c
         e = cudaMemcpyAsync(at<char>(slot, w.slot_tile), at<char>(ws, w.tile_mm), w.blk_tile * R,
                             cudaMemcpyDeviceToDevice, st);
     if (e) return cuda_fail(e, "cudaMemcpyAsync(position tables)");
-    p->dist_next = 0; p->dist_B = B; p->dist_rank0 = rank0; p->dist_R = R;
+    p->dist_next = 0; p->dist_B = B; p->dist_rank0 = rank0; p->dist_R = R; p->dist_lo = lo ? 1 : 0;
     return CPATTN_OK;
 }
 
@@ -1098,6 +1102,7 @@ cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, in
     a.order = at<int32_t>(ws, w.order);
     a.counts = at<unsigned long long>(ws, w.counts);
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
+    if (p->dist_lo) { a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); }
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
     a.reserved_sms = p->reserved_sms;

@@ -92,7 +92,7 @@ struct Plan {
     CUevent_st* bev_start = nullptr;
     int next_bstep = -1;            // step expected next on the backward ring path (-1: begin first)
     // multi-process ring (cpattn_dist_*): the step expected next and what cpattn_dist_begin placed
-    int dist_next = -1, dist_B = 0, dist_rank0 = 0, dist_R = 0;
+    int dist_next = -1, dist_B = 0, dist_rank0 = 0, dist_R = 0, dist_lo = 0;
     int bring_B = 0;                // batch size cpattn_backward_begin placed
     // page-locked copy of order, order_q, order_kv (created on first use): an upload from
     // pageable memory may block the calling thread until the stream drains
@@ -127,7 +127,7 @@ WsLayout ws_layout(const Plan& p, int B);
 // running state) and its key/value stage slot (the blocks it holds, with their position tables).
 struct DistLayout {
     size_t header = 0, posL = 0, tile_mm = 0, order = 0, counts = 0, sched = 0, unit_tiles = 0, walk_tab = 0,
-           walk_nz = 0, qL = 0, o_run = 0, lse_run = 0, ws_end = 0;
+           walk_nz = 0, loL = 0, tile_lo = 0, qL = 0, o_run = 0, lse_run = 0, ws_end = 0;
     size_t slot_k = 0, slot_v = 0, slot_pos = 0, slot_tile = 0, slot_end = 0;   // offsets in a slot
     size_t blk_k = 0, blk_v = 0, blk_pos = 0, blk_tile = 0;                     // one rank's block, bytes
 };

@@ -92,8 +92,10 @@ DistLayout dist_layout(const Plan& p, int B, int R) {
     w.counts = take(sizeof(uint64_t) * 2 * R * R);
     w.sched = take(sizeof(uint32_t) * (1 + (size_t)R));
     w.unit_tiles = take(sizeof(int32_t) * R * ng);
-    w.walk_tab = take(sizeof(int32_t) * R * ng);
+    w.walk_tab = take(sizeof(int32_t) * R * ng * R);
     w.walk_nz = take(sizeof(uint64_t) * R * ng);
+    w.loL = take(sizeof(int32_t) * R * n);
+    w.tile_lo = take(sizeof(int32_t) * 4 * R * nq);
     w.qL = take(2 * (size_t)B * R * n * p.h * d);
     w.o_run = take(4 * (size_t)B * R * n * p.h * d);
     w.lse_run = take(4 * (size_t)B * R * n * p.h);

@@ -120,9 +120,9 @@ class LibraryBackend:
         if event is not None:
             stream.wait_event(event)
 
-    def begin(self, q, k, v, pos, slot, stream):
+    def begin(self, q, k, v, pos, slot, stream, lo=None):
         from . import dist_begin
-        dist_begin(self.plan, self.B, self.rank0, self.R, q, k, v, self.ws, slot, pos=pos, stream=stream)
+        dist_begin(self.plan, self.B, self.rank0, self.R, q, k, v, self.ws, slot, pos=pos, stream=stream, lo=lo)
 
     def step(self, s, slot, scale, stream):
         from . import dist_step
@@ -157,11 +157,12 @@ class RingProcess:
         self.counters = HopCounters(kv=[0] * self.R, tables=[0] * self.R)
 
     def forward(self, q, k, v, pos=None, scale=None, out=None, lse=None, stream=None, copy_stream=None,
-                timeline=None):
+                timeline=None, lo=None):
         """timeline: a list to which each step appends (end of its compute, end of the hop that
         runs beside it) as timing events on the two streams (device backend only). Without a
         copy_stream the hops go to a new high-priority stream: the next step waits on them, so they
-        should not queue behind other copies the caller runs."""
+        should not queue behind other copies the caller runs. lo: the tokens' per-query lower
+        bounds (document masks of packed sequences), in the order of q."""
         import torch
         be, R, n_cp = self.backend, self.R, self.plan.n_cp
         B, h, n = self.B, self.plan.h, self.plan.T // n_cp
@@ -178,7 +179,10 @@ class RingProcess:
         slots = be.slots
         kv_blk = be.blocks[0] + be.blocks[1]
         tab_blk = be.blocks[2] + be.blocks[3]
-        be.begin(q, k, v, pos, slots[0], compute)
+        if lo is None:
+            be.begin(q, k, v, pos, slots[0], compute)
+        else:
+            be.begin(q, k, v, pos, slots[0], compute, lo=lo)
         placed = be.event(compute)
         used = [None, None]     # the step that last computed on each slot
         arrived = None          # the hop that filled the slot of the next step

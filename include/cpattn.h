@@ -337,7 +337,9 @@ cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, 
  *   cpattn_dist_begin: q [B][R n][h][d_k], k, v [B][R n][n_kv][d_k] bf16 (device): the process's
  *     tokens, rank rank0's n tokens in its local layout order, then rank rank0 + 1's, ...; pos
  *     [R n] int32 position ids of those tokens or NULL for their natural positions under the
- *     plan's layout. Places the queries in the workspace and the own blocks in `slot`.
+ *     plan's layout; lo [R n] int32 or NULL: the per-query lower bound of cpattn_forward_masked
+ *     (document masks; a causal plan), which stays with the queries while the keys' positions
+ *     travel. Places the queries in the workspace and the own blocks in `slot`.
  *   cpattn_dist_step, steps 0..n_cp-1 in order from one host thread: every local rank attends to
  *     the block it holds in `slot` (at step s, that of rank (r - s) mod n_cp) and merges the result
  *     into its fp32 running (O, lse) in the workspace. The slot must not change until the step's
@@ -353,8 +355,8 @@ cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, 
 cpattn_status_t cpattn_dist_sizes(cpattn_plan_t plan, int B, int R, size_t* ws_bytes, size_t* slot_bytes,
                                   size_t* region_offset /* [4] */, size_t* block_bytes /* [4] */);
 cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, const void* q, const void* k,
-                                  const void* v, const int32_t* pos, void* ws, size_t ws_bytes, void* slot,
-                                  size_t slot_bytes, cpattn_stream_t stream);
+                                  const void* v, const int32_t* pos, const int32_t* lo, void* ws, size_t ws_bytes,
+                                  void* slot, size_t slot_bytes, cpattn_stream_t stream);
 cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
                                  const void* slot, size_t slot_bytes, void* ws, size_t ws_bytes,
                                  cpattn_stream_t stream);

@@ -38,14 +38,15 @@ def _shard(x, tokens):
     return np.ascontiguousarray(x[:, tokens])
 
 
-def _run_process(plan, B, rank, world, q, k, v, pos, transport, scale=None):
+def _run_process(plan, B, rank, world, q, k, v, pos, transport, scale=None, lo=None):
     """This process's rows: natural token ids, o [B, R n, h, d] fp32, lse [B, h, R n]."""
     R = plan.n_cp // world
     toks = local_tokens(plan.T, plan.n_cp, plan.layout, rank * R, R)
     ring = RingProcess(plan, B, rank=rank, world=world, transport=transport, device="cuda")
     posd = None if pos is None else torch.from_numpy(np.ascontiguousarray(pos[toks], dtype=np.int32)).cuda()
+    lod = None if lo is None else torch.from_numpy(np.ascontiguousarray(lo[toks], dtype=np.int32)).cuda()
     o, lse = ring.forward(to_device_bf16(_shard(q, toks)), to_device_bf16(_shard(k, toks)),
-                          to_device_bf16(_shard(v, toks)), pos=posd, scale=scale)
+                          to_device_bf16(_shard(v, toks)), pos=posd, scale=scale, lo=lod)
     torch.cuda.synchronize()
     cp.check(plan, ring.backend.ws)
     return toks, o.float().cpu().numpy(), lse.cpu().numpy(), ring
@@ -92,13 +93,36 @@ def test_one_process_ring_with_position_ids():
     compare(o, lse, ref_o, ref_lse, what="one-process ring, permuted positions")
 
 
+def _documents(T, seed):
+    """Document ids of a packed sequence (runs of 100..900 tokens) and each token's lower bound."""
+    rng = np.random.default_rng(seed)
+    lengths, left = [], T
+    while left > 0:
+        lengths.append(min(left, int(rng.integers(100, 900))))
+        left -= lengths[-1]
+    doc = np.repeat(np.arange(len(lengths)), lengths).astype(np.int32)
+    lo = np.repeat(np.concatenate([[0], np.cumsum(lengths)[:-1]]), lengths).astype(np.int32)
+    return doc, lo
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_one_process_ring_with_document_masks(layout):
+    B, T, h, n_kv, d, n_cp = 1, 2048, 4, 2, 128, 4
+    q, k, v = inputs(93, B, T, h, n_kv, d)
+    doc, lo = _documents(T, 4)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, layout, True)
+    toks, o, lse, _ = _run_process(plan, B, 0, 1, q, k, v, None, None, lo=lo)
+    ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=True, rows=toks)
+    compare(o, lse, ref_o, ref_lse, what=f"one-process ring, document masks, {layout}")
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, case, outdir):
+def _rank_main(rank, world, port, case, outdir, with_docs=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -106,7 +130,8 @@ def _rank_main(rank, world, port, case, outdir):
         torch.cuda.set_device(0)
         q, k, v = inputs(177 + T, B, T, h, n_kv, d)
         plan = cp.Plan(T, h, n_kv, d, n_cp, layout, causal)
-        toks, o, lse, ring = _run_process(plan, B, rank, world, q, k, v, None, HostTransport(rank, world))
+        lo = _documents(T, 6)[1] if with_docs else None
+        toks, o, lse, ring = _run_process(plan, B, rank, world, q, k, v, None, HostTransport(rank, world), lo=lo)
         np.savez(os.path.join(outdir, f"rank{rank}.npz"), toks=toks, o=o, lse=lse, kv=np.array(ring.counters.kv))
         dist.barrier()
     finally:
@@ -131,3 +156,17 @@ def test_two_processes_on_one_gpu_exchange_through_host_memory(case):
         compare(part["o"], part["lse"], ref_o, ref_lse, what=f"process {r} of 2")
         assert np.array_equal(part["o"], ro[:, toks]) and np.array_equal(part["lse"], rl[:, :, toks])
         assert list(part["kv"]) == [oracle.get().kv_bytes_recv(B, n, n_kv, d, n_cp)] * (n_cp // world)
+
+
+def test_two_processes_with_document_masks():
+    B, T, h, n_kv, d, n_cp, layout, causal = CASES[0]
+    world = 2
+    with tempfile.TemporaryDirectory() as outdir:
+        mp.start_processes(_rank_main, args=(world, _free_port(), CASES[0], outdir, True), nprocs=world, join=True,
+                           start_method="spawn")
+        parts = [dict(np.load(os.path.join(outdir, f"rank{r}.npz"))) for r in range(world)]
+    q, k, v = inputs(177 + T, B, T, h, n_kv, d)
+    doc, _ = _documents(T, 6)
+    for r, part in enumerate(parts):
+        ref_o, ref_lse = oracle.get().attention_docs(q, k, v, doc, causal=True, rows=part["toks"])
+        compare(part["o"], part["lse"], ref_o, ref_lse, what=f"process {r} of 2, document masks")
