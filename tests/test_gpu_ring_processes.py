@@ -7,7 +7,9 @@ kernels, and passes the block that crosses to the next process through a transpo
   same kernel over the same blocks in the same order.
 * Two processes on one GPU exchanging the crossing block over gloo through host memory: each
   process's rows against the oracle and bit-identical to the ring-step path. The processes'
-  kernels never wait on each other; only the host exchange orders them."""
+  kernels never wait on each other; only the host exchange orders them.
+* Document masks (a per-query lower bound that stays with the queries) in one and two processes,
+  against the oracle's document-id definition."""
 import os
 import socket
 import tempfile
