@@ -529,6 +529,7 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
     if (step > 0) { a.kv_k = at<char>(ws, w.stageK[slot]); a.kv_v = at<char>(ws, w.stageV[slot]); }
     a.kv_by_holder = 1;
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
+    a.l_run = a.lse_run + (size_t)B * p->T * p->h;
     std::string why;
     if ((e = launch_attn(a, cst, &why))) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
     if ((e = cudaEventRecord(p->ev_step[slot], cst))) return cuda_fail(e, "cudaEventRecord");
@@ -567,6 +568,7 @@ cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, 
     cpattn::FinalizeArgs a{};
     a.B = B; a.T = p->T; a.n = p->n; a.m = p->m; a.h = p->h; a.d = p->d; a.n_cp = p->n_cp; a.layout = p->layout;
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run); a.o = o; a.lse = lse;
+    a.l_run = a.lse_run + (size_t)B * p->T * p->h;
     int e = cpattn::launch_finalize(a, stream);
     if (e) return cuda_fail(e, "finalize kernel");
     p->next_step = -1;
@@ -1102,6 +1104,7 @@ cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, in
     a.order = at<int32_t>(ws, w.order);
     a.counts = at<unsigned long long>(ws, w.counts);
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
+    a.l_run = a.lse_run + (size_t)B * R * p->n * p->h;
     if (p->dist_lo) { a.loL = at<int32_t>(ws, w.loL); a.tile_lo = at<int32_t>(ws, w.tile_lo); }
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
@@ -1155,6 +1158,7 @@ cpattn_status_t cpattn_dist_finalize(cpattn_plan_t plan, int B, int rank0, int R
     a.B = B; a.T = (int64_t)R * p->n; a.n = p->n; a.m = 0; a.h = p->h; a.d = p->d; a.n_cp = R;
     a.layout = CPATTN_CONTIGUOUS;
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run); a.o = o; a.lse = lse;
+    a.l_run = a.lse_run + (size_t)B * R * p->n * p->h;
     int e = cpattn::launch_finalize(a, stream);
     if (e) return cuda_fail(e, "finalize kernel");
     p->dist_next = -1;

@@ -97,7 +97,8 @@ struct Params {
     uint16_t* o;
     float* lse;
     float* o_run;
-    float* lse_run;
+    float* lse_run;         // ring step: running maximum m_run (log2 units)
+    float* l_run;           // ring step: running sum l_run
     uint32_t* header;
     uint64_t timeout_ns;
     int first;              // ring step: write the running state instead of merging into it
@@ -769,12 +770,21 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         }
         const float inv_l = l > 0.f ? 1.0f / l : 0.f;
         const float lse_v = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
-        // Output in 32-column chunks of O_i (bounded register use while loading and storing).
+        // Fused: O_i / l in bf16 at the row's natural position, and its lse.
+        // Ring step: the running row holds O unnormalised relative to its maximum m_run (log2
+        // units, like m_used) with the sum l_run; the finalize kernel divides. This step's (O_i,
+        // m_used, l) joins it in one of three ways:
+        //   write   (the first step, or a running row that has seen no key yet): O_i, m_used, l;
+        //   add     (m_used <= m_run + 8): O_run += 2^(m_used - m_run) O_i by fire-and-forget
+        //           reductions, no read of O_run; l_run grows by the same weight;
+        //   rescale (m_used > m_run + 8, rare once a row has seen its largest scores):
+        //           O_run = 2^(m_run - m_used) O_run + O_i, read back, and m_run = m_used.
+        // A row none of whose keys this step shows is left as it is.
         uint4* dst = nullptr;                 // fused: bf16 row in natural order
-        float4* orun = nullptr;               // ring step: fp32 running row in layout order
-        int64_t base = 0;
-        float wa = 0.f, wb = inv_l, L = lse_v;
-        const bool first = P.first != 0;
+        float* orow = nullptr;                // ring step: fp32 running row in layout order
+        enum { kKeep, kWrite, kAdd, kRescale };
+        int mode = kKeep;
+        float f = 1.f;
         if (P.fused) {
             int64_t tn;
             if (P.layout == CPATTN_CONTIGUOUS) tn = (int64_t)U.r * P.n + jl;
@@ -786,21 +796,29 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                 P.lse[((int64_t)U.b * P.h + head) * P.T + tn] = lse_v;
             }
         } else if (row_valid) {
-            base = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n + jl;
-            orun = reinterpret_cast<float4*>(P.o_run + base * D);
-            if (!first) {
-                const float la = P.lse_run[base];
-                const float M = fmaxf(la, lse_v);
-                if (M == -INFINITY) {
-                    wb = 0.f;
-                    L = -INFINITY;
+            const int64_t base = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n + jl;
+            orow = P.o_run + base * D;
+            float mr = -INFINITY, lr = 0.f;
+            if (P.first == 0 && l > 0.f) {
+                mr = P.lse_run[base];
+                lr = P.l_run[base];
+            }
+            if (P.first != 0 || (l > 0.f && !(lr > 0.f))) {
+                mode = kWrite;
+                P.lse_run[base] = m_used;
+                P.l_run[base] = l;
+            } else if (l > 0.f) {
+                if (m_used <= mr + 8.0f) {
+                    mode = kAdd;
+                    f = ex2(m_used - mr);
+                    P.l_run[base] = lr + f * l;
                 } else {
-                    L = M + logf(expf(la - M) + expf(lse_v - M));
-                    wa = expf(la - L);
-                    wb = expf(lse_v - L) * inv_l;
+                    mode = kRescale;
+                    f = ex2(mr - m_used);
+                    P.lse_run[base] = m_used;
+                    P.l_run[base] = lr * f + l;
                 }
             }
-            P.lse_run[base] = L;
         }
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -821,16 +839,24 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                     v.w = pack_bf16(__uint_as_float(ot[8 * q4 + 6]) * inv_l, __uint_as_float(ot[8 * q4 + 7]) * inv_l);
                     st_global_v4_hint(dst + c * 4 + q4, v, pol_o);
                 }
-            } else if (orun) {
+            } else if (mode == kWrite) {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    reinterpret_cast<uint4*>(orow)[c * 8 + q4] =
+                        make_uint4(ot[4 * q4], ot[4 * q4 + 1], ot[4 * q4 + 2], ot[4 * q4 + 3]);
+            } else if (mode == kAdd) {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    red_add_v4_f32(orow + c * 32 + q4 * 4, __uint_as_float(ot[4 * q4]) * f,
+                                   __uint_as_float(ot[4 * q4 + 1]) * f, __uint_as_float(ot[4 * q4 + 2]) * f,
+                                   __uint_as_float(ot[4 * q4 + 3]) * f);
+            } else if (mode == kRescale) {
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
-                    float4 ob = make_float4(__uint_as_float(ot[4 * q4]) * wb, __uint_as_float(ot[4 * q4 + 1]) * wb,
-                                            __uint_as_float(ot[4 * q4 + 2]) * wb, __uint_as_float(ot[4 * q4 + 3]) * wb);
-                    if (!first) {
-                        const float4 oa = orun[c * 8 + q4];
-                        ob.x += wa * oa.x; ob.y += wa * oa.y; ob.z += wa * oa.z; ob.w += wa * oa.w;
-                    }
-                    orun[c * 8 + q4] = ob;
+                    float4* a = reinterpret_cast<float4*>(orow) + c * 8 + q4;
+                    const float4 oa = *a;
+                    *a = make_float4(oa.x * f + __uint_as_float(ot[4 * q4]), oa.y * f + __uint_as_float(ot[4 * q4 + 1]),
+                                     oa.z * f + __uint_as_float(ot[4 * q4 + 2]), oa.w * f + __uint_as_float(ot[4 * q4 + 3]));
                 }
             }
         }
@@ -1067,7 +1093,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.words = (a.n_qt + 63) / 64;
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.counts = a.counts; P.sched = a.sched;
-    P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run;
+    P.o = static_cast<uint16_t*>(a.o); P.lse = a.lse; P.o_run = a.o_run; P.lse_run = a.lse_run; P.l_run = a.l_run;
     P.header = a.header; P.timeout_ns = a.timeout_ns;
     const int64_t units = (int64_t)a.n_cp * a.n_grp * a.B * (a.pair_heads ? a.h / 2 : a.h);
     if (units > INT_MAX) {

@@ -43,8 +43,9 @@ struct WsLayout {
     size_t kL = 0, vL = 0;  // bf16 [n_cp][B][n_kv][n][d]
     size_t fwd_end = 0;     // end of what cpattn_forward needs
     size_t stageK[2] = {0, 0}, stageV[2] = {0, 0};  // ring stage slots, same shape as kL
-    size_t o_run = 0;       // fp32 [n_cp][B][h][n][d] running output (normalised)
-    size_t lse_run = 0;     // fp32 [n_cp][B][h][n] running lse
+    size_t o_run = 0;       // fp32 [n_cp][B][h][n][d] running output, unnormalised (relative to m_run)
+    size_t lse_run = 0;     // fp32 [n_cp][B][h][n] running maximum m_run (log2 units), then the same
+                            // shape of running sums l_run
     size_t ring_end = 0;
     // all-gather variant (after fwd_end, overlapping the ring-step regions): every rank's gathered
     // copy of the whole K and V, [n_cp holder][n_cp source][B][n_kv][n][d] bf16 each
@@ -166,7 +167,8 @@ struct AttnLaunch {
     const int32_t* loL; const int32_t* tile_lo;   // document-mask lower bounds, or NULL
     unsigned long long* counts;     // tiles computed per (rank, step, class)
     void* o; float* lse;            // fused outputs (natural order)
-    float* o_run; float* lse_run;   // ring-step running state
+    float* o_run; float* lse_run;   // ring-step running state: O (unnormalised), maximum m_run
+    float* l_run = nullptr;         //   and sum l_run (log2 units; see the attention kernel's epilogue)
     uint32_t* header;
     uint64_t timeout_ns;
     // Key-side position tables when they are not posL / tile_mm (indexed like them by the rank
@@ -184,7 +186,7 @@ int launch_attention(const AttnLaunch& a, void* stream, std::string* why);
 
 struct FinalizeArgs {
     int B; int64_t T, n, m; int h, d, n_cp, layout;
-    const float* o_run; const float* lse_run; void* o; float* lse;
+    const float* o_run; const float* lse_run; const float* l_run; void* o; float* lse;
 };
 int launch_finalize(const FinalizeArgs& a, void* stream);
 

@@ -192,11 +192,14 @@ __global__ void __launch_bounds__(256, 4) permute_kernel(const uint4* __restrict
     }
 }
 
-// Ring-step path: running fp32 state [n_cp][B][h][n][d] -> bf16 natural [B,T,h,d]; lse
-// [n_cp][B][h][n] -> [B,h,T]. One thread per 4 outputs, destination order.
-__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ o_run, const float* __restrict__ lse_run,
-                                                       uint2* __restrict__ o, float* __restrict__ lse, int B, int64_t T,
-                                                       int64_t n, int64_t m, int h, int d, int n_cp, int layout) {
+// Ring-step path: the running state [n_cp][B][h][n] (O unnormalised over d columns, its maximum
+// m_run in log2 units and its sum l_run) -> O / l_run in bf16 natural order [B,T,h,d] and
+// lse = (m_run + log2 l_run) ln 2 as [B,h,T]; a row that saw no key gets 0 and -inf. One thread
+// per 4 outputs, destination order.
+__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ o_run, const float* __restrict__ m_run,
+                                                       const float* __restrict__ l_run, uint2* __restrict__ o,
+                                                       float* __restrict__ lse, int B, int64_t T, int64_t n, int64_t m,
+                                                       int h, int d, int n_cp, int layout) {
     const int cpr = d / 4;
     const int64_t no = (int64_t)B * T * h * cpr;
     const int64_t nl = (int64_t)B * h * T;
@@ -211,8 +214,11 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
             int r;
             int64_t j;
             rank_of(layout, t, n, m, n_cp, r, j);
-            const float4 x = o_run[((((int64_t)r * B + b) * h + hd) * n + j) * cpr + c];
-            __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+            const int64_t row = (((int64_t)r * B + b) * h + hd) * n + j;
+            const float4 x = o_run[row * cpr + c];
+            const float lr = l_run[row];
+            const float inv = lr > 0.f ? 1.0f / lr : 0.f;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(x.x * inv, x.y * inv), hi = __floats2bfloat162_rn(x.z * inv, x.w * inv);
             uint2 out;
             out.x = *reinterpret_cast<uint32_t*>(&lo);
             out.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -225,7 +231,9 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
             int r;
             int64_t j;
             rank_of(layout, t, n, m, n_cp, r, j);
-            lse[e] = lse_run[(((int64_t)r * B + b) * h + hd) * n + j];
+            const int64_t row = (((int64_t)r * B + b) * h + hd) * n + j;
+            const float lr = l_run[row];
+            lse[e] = lr > 0.f ? (m_run[row] + log2f(lr)) * 0.69314718055994531f : -INFINITY;
         }
     }
 }
@@ -490,8 +498,8 @@ int launch_permute(const PermuteArgs& a, void* stream) {
 int launch_finalize(const FinalizeArgs& a, void* stream) {
     const int64_t work = (int64_t)a.B * a.T * a.h * (a.d / 4 + 1);
     finalize_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4*>(a.o_run), a.lse_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m, a.h,
-        a.d, a.n_cp, a.layout);
+        reinterpret_cast<const float4*>(a.o_run), a.lse_run, a.l_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m,
+        a.h, a.d, a.n_cp, a.layout);
     return (int)cudaGetLastError();
 }
 

@@ -51,7 +51,7 @@ WsLayout ws_layout(const Plan& p, int B) {
         w.stageV[s] = take(2 * (size_t)B * T * p.n_kv * d);
     }
     w.o_run = take(4 * (size_t)B * T * p.h * d);
-    w.lse_run = take(4 * (size_t)B * T * p.h);
+    w.lse_run = take(2 * 4 * (size_t)B * T * p.h);     // running maximum, then running sum
     w.ring_end = off;
     off = w.fwd_end;
     w.gK = take(2 * (size_t)p.n_cp * B * T * p.n_kv * d);
@@ -98,7 +98,7 @@ DistLayout dist_layout(const Plan& p, int B, int R) {
     w.tile_lo = take(sizeof(int32_t) * 4 * R * nq);
     w.qL = take(2 * (size_t)B * R * n * p.h * d);
     w.o_run = take(4 * (size_t)B * R * n * p.h * d);
-    w.lse_run = take(4 * (size_t)B * R * n * p.h);
+    w.lse_run = take(2 * 4 * (size_t)B * R * n * p.h);     // running maximum, then running sum
     w.ws_end = off;
     w.blk_k = w.blk_v = 2 * (size_t)B * n * p.n_kv * d;
     w.blk_pos = sizeof(int32_t) * n;

@@ -86,6 +86,13 @@ __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t p
                  : "memory");
 }
 
+// Four consecutive fp32 additions into global memory without a return value (a relaxed
+// reduction performed at L2; the address is 16-byte aligned).
+__device__ __forceinline__ void red_add_v4_f32(float* ptr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // ---- tensor memory -------------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");

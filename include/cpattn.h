@@ -83,7 +83,8 @@ cpattn_status_t cpattn_plan_set_reserved_sms(cpattn_plan_t plan, int sms);
 /* Workspace bytes for cpattn_forward / cpattn_permute with batch B. */
 cpattn_status_t cpattn_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 /* Workspace bytes for the ring-step path (permute + ring_step + finalize): the forward
- * workspace plus the two-slot key/value stage and the fp32 running (O, lse) state. */
+ * workspace plus the two-slot key/value stage and the fp32 running state (O unnormalised against
+ * a running maximum, with the running sum). */
 cpattn_status_t cpattn_ring_workspace_size(cpattn_plan_t plan, int B, size_t* bytes);
 
 /* The whole forward pass ([CEX] "Pass them around a ring" and the online-softmax paragraph;
@@ -149,7 +150,8 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
 /* Ring-faithful path, step 2 ([CEX] "Pass them around a ring"): ring step `step` of n_cp for
  * every virtual rank at once. Rank r attends to the key/value block it holds, that of rank
  * (r - step) mod n_cp, read from the stage slot step % 2 (step 0: its own block in place), and
- * merges the partial (O_s, lse_s) into the fp32 running state in the workspace. On `copy` it
+ * merges the partial (O_s with its maximum and sum) into the fp32 running state in the workspace
+ * (the online-softmax merge; cpattn_finalize normalises). On `copy` it
  * enqueues the hop to the next step: every rank's slot (step+1) % 2 receives the block its left
  * neighbour holds now (send right, receive left), ordered against the compute stream with
  * events so that a slot is overwritten only after the step that read it has finished. Steps
@@ -160,8 +162,8 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
 cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scale, void* ws, size_t ws_bytes,
                                  cpattn_stream_t compute, cpattn_stream_t copy);
 
-/* Ring-faithful path, step 3: the running state after the last step, rounded to bf16 and
- * written back in natural token order: o [B,T,h,d_k] bf16, lse [B,h,T] fp32. */
+/* Ring-faithful path, step 3: the running state after the last step, normalised, rounded to
+ * bf16 and written back in natural token order: o [B,T,h,d_k] bf16, lse [B,h,T] fp32. */
 cpattn_status_t cpattn_finalize(cpattn_plan_t plan, int B, void* o, float* lse, void* ws, size_t ws_bytes,
                                 cpattn_stream_t stream);
 
@@ -342,7 +344,7 @@ cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, 
  *     travel. Places the queries in the workspace and the own blocks in `slot`.
  *   cpattn_dist_step, steps 0..n_cp-1 in order from one host thread: every local rank attends to
  *     the block it holds in `slot` (at step s, that of rank (r - s) mod n_cp) and merges the result
- *     into its fp32 running (O, lse) in the workspace. The slot must not change until the step's
+ *     into its fp32 running state in the workspace. The slot must not change until the step's
  *     work on `stream` has finished.
  *   cpattn_dist_shift: on `stream`, local rank i + 1's block in dst_slot <- local rank i's block
  *     in src_slot, for i < R - 1, all four regions; with wrap != 0 (a process that holds the whole
