@@ -1018,10 +1018,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // warp-wide TMEM loads; only the lanes of valid query rows store
         if (ok && P.dq_run) {
-            // one ring step: add this step's dQ into the running fp32 rows of rank r (step 0 writes)
+            // One ring step: add this step's dQ into the running fp32 rows of rank r (step 0
+            // writes). The additions are fire-and-forget reductions, one per element and step (the
+            // steps are ordered by their launches, so the sum is deterministic): no read of the
+            // running rows to wait on. A later step with nothing visible adds nothing.
             float4* f = reinterpret_cast<float4*>(P.dq_run + ((((int64_t)r * P.B + b) * P.h + head) * P.n + jq) * D);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
+            for (int c = 0; c < D / 64 && (n_steps > 0 || P.step == 0); ++c) {
                 uint32_t t[32];
                 if (n_steps > 0) {
                     tmem_ld32(tmem + lane_base + C::COL_A0 + wg * (D / 2) + c * 32, t);
@@ -1035,11 +1038,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int idx = (wg * (D / 2) + c * 32) / 4 + q4;
                         float4 x = make_float4(__uint_as_float(t[4 * q4]) * P.scale, __uint_as_float(t[4 * q4 + 1]) * P.scale,
                                                __uint_as_float(t[4 * q4 + 2]) * P.scale, __uint_as_float(t[4 * q4 + 3]) * P.scale);
-                        if (P.step > 0) {
-                            const float4 y = f[idx];
-                            x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-                        }
-                        f[idx] = x;
+                        if (P.step > 0) red_add_v4_f32(reinterpret_cast<float*>(f + idx), x.x, x.y, x.z, x.w);
+                        else f[idx] = x;
                     }
                 }
             }
