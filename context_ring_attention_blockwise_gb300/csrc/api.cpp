@@ -651,21 +651,15 @@ cpattn_status_t cpattn_backward_ring_step(cpattn_plan_t plan, int B, int step, f
     cpattn::BwdLaunch a = bwd_args(*p, B, scale, ws, nullptr);
     a.step = step;
     if (step > 0) { a.kL = at<char>(ws, w.bstageK[slot]); a.vL = at<char>(ws, w.bstageV[slot]); }
-    a.dk_f32 = at<float>(ws, step == 0 ? w.circK[0] : w.contribK);   // step 0 starts the partial sum
-    a.dv_f32 = at<float>(ws, step == 0 ? w.circV[0] : w.contribV);
+    // step 0 starts the partial dK/dV sums; later steps add into the sums that arrived with the
+    // blocks, so the dK/dV kernel waits for that hop and the dQ kernel runs first, overlapping it
+    a.dk_f32 = at<float>(ws, w.circK[slot]);
+    a.dv_f32 = at<float>(ws, w.circV[slot]);
     a.dq_run = at<float>(ws, w.dq_run);
+    if (step > 0) { a.dkdv_add = 1; a.dkdv_after = p->bev_circ[slot]; }
     std::string why;
     if ((e = cpattn::launch_backward(a, cst, &why))) return why.empty() ? cuda_fail(e, "backward kernels") : fail(CPATTN_ERR_CUDA, why);
     if ((e = cudaEventRecord(p->bev_used[slot], cst))) return cuda_fail(e, "cudaEventRecord");
-    // add the contribution to the partial sum that arrived with the block (the receive is the
-    // only thing this waits for, so the hop overlapped the kernels above)
-    const size_t nkv = (size_t)B * p->T * p->n_kv * p->d;   // floats of one gradient over all ranks
-    if (step > 0) {
-        if ((e = cudaStreamWaitEvent(cst, p->bev_circ[slot], 0))) return cuda_fail(e, "cudaStreamWaitEvent");
-        if ((e = cpattn::launch_add_f32(at<float>(ws, w.circK[slot]), at<float>(ws, w.contribK), (int64_t)nkv, cst)) ||
-            (e = cpattn::launch_add_f32(at<float>(ws, w.circV[slot]), at<float>(ws, w.contribV), (int64_t)nkv, cst)))
-            return cuda_fail(e, "gradient add kernel");
-    }
     if ((e = cudaEventRecord(p->bev_ready, cst))) return cuda_fail(e, "cudaEventRecord");
 
     // K, V for the next step: slot nxt of rank r <- the block rank r - 1 holds now (issued before

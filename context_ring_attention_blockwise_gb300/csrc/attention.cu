@@ -763,6 +763,14 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         flush();
         if (!ok) break;
         if (j == 0 && !P.fused && !P.first) continue;     // nothing visible at this step
+        // ring step: the running row's maximum and sum, loaded before the wait for the last P·V so
+        // that their round trip overlaps it
+        float mr = -INFINITY, lr = 0.f;
+        if (!P.fused && row_valid && P.first == 0 && l > 0.f) {
+            const int64_t base = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n + jl;
+            mr = P.lse_run[base];
+            lr = P.l_run[base];
+        }
         if (j > 0) {
             ok = __all_sync(0xffffffffu, wait(bars.pv_done(wg), (ntile - 1) & 1, kSitePvDone));
             if (!ok) break;
@@ -798,11 +806,6 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
         } else if (row_valid) {
             const int64_t base = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n + jl;
             orow = P.o_run + base * D;
-            float mr = -INFINITY, lr = 0.f;
-            if (P.first == 0 && l > 0.f) {
-                mr = P.lse_run[base];
-                lr = P.l_run[base];
-            }
             if (P.first != 0 || (l > 0.f && !(lr > 0.f))) {
                 mode = kWrite;
                 P.lse_run[base] = m_used;

@@ -67,10 +67,12 @@ struct BwdParams {
     uint64_t timeout_ns;
     // One ring step (step >= 0) instead of the whole walk (-1). K and V rows are then indexed by
     // the rank holding the block at that step; dK/dV leave as this step's fp32 contribution
-    // [holder][B][n_kv][n][d] and dQ is added into the running fp32 [r][B][h][n][d].
+    // [holder][B][n_kv][n][d], written or added into the partial sums there, and dQ is added
+    // into the running fp32 [r][B][h][n][d].
     int step;
     float* dk_f32;
     float* dv_f32;
+    int dkdv_add;           // add the contribution into dk_f32 / dv_f32 by reductions
     float* dq_run;
 };
 
@@ -636,12 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tcgen05.ld is a warp-wide instruction: every lane loads, and only the lanes of valid
         // keys store (the last key tile of a block may be short)
         if (ok && P.dk_f32) {
-            // one ring step: this step's contribution, fp32, in the holder's slot
+            // One ring step: this step's contribution, fp32, in the holder's slot: written (step
+            // 0 starts the partial sums), or added into the partial sums that arrived with the
+            // blocks by fire-and-forget reductions (one per element and step, ordered by the
+            // launches: deterministic); an empty walk adds nothing.
             const int64_t krow = (((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + jk;
             float4* fk = reinterpret_cast<float4*>(P.dk_f32 + krow * D);
             float4* fv = reinterpret_cast<float4*>(P.dv_f32 + krow * D);
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
+            for (int which = 0; which < 2 && (n_steps > 0 || !P.dkdv_add); ++which) {
                 const uint32_t col0 = (which ? C::COL_A1 : C::COL_A0) + (uint32_t)(wg * (D / 2));
                 const float mul = which ? P.scale : 1.0f;
                 float4* f = which ? fk : fv;
@@ -658,7 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q4 = 0; q4 < 8; ++q4) {
                         const float4 x = make_float4(__uint_as_float(t[4 * q4]) * mul, __uint_as_float(t[4 * q4 + 1]) * mul,
                                                      __uint_as_float(t[4 * q4 + 2]) * mul, __uint_as_float(t[4 * q4 + 3]) * mul);
-                        if (key_valid) f[(wg * (D / 2) + c * 32) / 4 + q4] = x;
+                        if (!key_valid) continue;
+                        float4* y = f + (wg * (D / 2) + c * 32) / 4 + q4;
+                        if (P.dkdv_add) red_add_v4_f32(reinterpret_cast<float*>(y), x.x, x.y, x.z, x.w);
+                        else *y = x;
                     }
                 }
             }
@@ -1106,15 +1114,23 @@ int launch_bwd_d(const BwdLaunch& a, cudaStream_t st, std::string* why) {
     P.loL = a.loL; P.tile_lo = reinterpret_cast<const int4*>(a.tile_lo);
     P.dq = static_cast<uint16_t*>(a.dq); P.dk = static_cast<uint16_t*>(a.dk); P.dv = static_cast<uint16_t*>(a.dv);
     P.header = a.header; P.timeout_ns = a.timeout_ns;
-    P.step = a.step; P.dk_f32 = a.dk_f32; P.dv_f32 = a.dv_f32; P.dq_run = a.dq_run;
+    P.step = a.step; P.dk_f32 = a.dk_f32; P.dv_f32 = a.dv_f32; P.dq_run = a.dq_run; P.dkdv_add = a.dkdv_add;
     const int64_t kv_units = (int64_t)a.B * a.n_kv * a.n_cp * a.n_qt, q_units = (int64_t)a.B * a.h * a.n_cp * a.n_qt;
     if (kv_units > INT_MAX || q_units > INT_MAX) {
         *why = "too many work units";
         return (int)cudaErrorInvalidValue;
     }
+    int e = 0;
+    if (a.dkdv_after) {
+        // the dK/dV kernel adds into partial sums that are still arriving: dQ first, then wait
+        bwd_dq_kernel<D, LB><<<(int)q_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+        if ((e = (int)cudaGetLastError())) return e;
+        if ((e = (int)cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(a.dkdv_after), 0))) return e;
+        bwd_dkdv_kernel<D, LB><<<(int)kv_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
+        return (int)cudaGetLastError();
+    }
     bwd_dkdv_kernel<D, LB><<<(int)kv_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
-    int e = (int)cudaGetLastError();
-    if (e) return e;
+    if ((e = (int)cudaGetLastError())) return e;
     bwd_dq_kernel<D, LB><<<(int)q_units, kThreads, C::SMEM_BYTES, st>>>(tq, tdo, tk, tv, P);
     return (int)cudaGetLastError();
 }

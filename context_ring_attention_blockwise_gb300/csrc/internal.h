@@ -57,11 +57,10 @@ struct WsLayout {
     size_t bwd_order = 0;   // int32 [2][n_cp * n_qt]: order_q, then order_kv
     size_t bwd_end = 0;
     // backward ring-step path (after bwd_end): K/V stage slots, the circulating fp32 dK/dV
-    // partial sums (two slots), one step's dK/dV contribution, and the running fp32 dQ; all
-    // [n_cp][B][...][n][d] with the rank index the block's current holder (dQ: its own rank)
+    // partial sums (two slots), and the running fp32 dQ; all [n_cp][B][...][n][d] with the rank
+    // index the block's current holder (dQ: its own rank)
     size_t bstageK[2] = {0, 0}, bstageV[2] = {0, 0};
     size_t circK[2] = {0, 0}, circV[2] = {0, 0};
-    size_t contribK = 0, contribV = 0;
     size_t dq_run = 0;
     size_t bring_end = 0;
 };
@@ -238,11 +237,15 @@ struct BwdLaunch {
     // added into the running fp32 dq_run (written at step 0)
     int step = -1;
     float* dk_f32 = nullptr; float* dv_f32 = nullptr; float* dq_run = nullptr;
+    // dkdv_add: the dK/dV contribution is added into dk_f32 / dv_f32 (the partial sums) by
+    // reductions instead of written; dkdv_after (a cudaEvent_t, or NULL): the dQ kernel is
+    // launched first and the dK/dV kernel after a stream wait on this event
+    int dkdv_add = 0;
+    void* dkdv_after = nullptr;
 };
 int launch_backward(const BwdLaunch& a, void* stream, std::string* why);
 
 // acc[i] += c[i] over n floats (16-byte aligned, n a multiple of 4)
-int launch_add_f32(float* acc, const float* c, int64_t n, void* stream);
 // fp32 [n_cp][B][H][n][d] in layout order -> bf16 [B][T][H][d] in natural order
 int launch_unpermute_f32(const float* src, void* dst, int B, int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
                          int layout, void* stream);

@@ -238,15 +238,6 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
     }
 }
 
-// Backward ring-step path: the circulating fp32 dK/dV partial plus this step's contribution,
-// in place. One thread per float4.
-__global__ void __launch_bounds__(256) add_f32_kernel(float4* __restrict__ acc, const float4* __restrict__ c, int64_t n4) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-        const float4 a = acc[i], b = c[i];
-        acc[i] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    }
-}
-
 // fp32 [n_cp][B][H][n][d] in layout order -> bf16 [B,T,H,d] in natural order (the backward
 // ring-step path's gradients). One thread per 4 outputs, destination order.
 __global__ void __launch_bounds__(256) unpermute_f32_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, int B,
@@ -500,13 +491,6 @@ int launch_finalize(const FinalizeArgs& a, void* stream) {
     finalize_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(a.o_run), a.lse_run, a.l_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m,
         a.h, a.d, a.n_cp, a.layout);
-    return (int)cudaGetLastError();
-}
-
-int launch_add_f32(float* acc, const float* c, int64_t n, void* stream) {
-    const int64_t n4 = n / 4;
-    add_f32_kernel<<<grid_for(n4, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<float4*>(acc), reinterpret_cast<const float4*>(c), n4);
     return (int)cudaGetLastError();
 }
 

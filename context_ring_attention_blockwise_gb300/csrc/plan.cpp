@@ -73,8 +73,6 @@ WsLayout ws_layout(const Plan& p, int B) {
         w.circK[s] = take(4 * (size_t)B * T * p.n_kv * d);
         w.circV[s] = take(4 * (size_t)B * T * p.n_kv * d);
     }
-    w.contribK = take(4 * (size_t)B * T * p.n_kv * d);
-    w.contribV = take(4 * (size_t)B * T * p.n_kv * d);
     w.dq_run = take(4 * (size_t)B * T * p.h * d);
     w.bring_end = off;
     return w;

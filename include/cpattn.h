@@ -240,9 +240,10 @@ cpattn_status_t cpattn_backward_masked(cpattn_plan_t plan, int B, const void* q,
  *   cpattn_backward_ring_step, steps 0..n_cp-1 in order, from one host thread per plan: on
  *     `compute`, every rank r computes, against its own queries, the dK/dV contribution for the
  *     block it holds (that of rank (r - step) mod n_cp; step 0 its own) and adds its dQ for that
- *     block into its running fp32 dQ; the contribution is then added to the block's fp32 partial
- *     sum, which arrived with the block. On `copy`: the K/V hop for the next step (issued first,
- *     overlapping this step's kernels) and the hop of the partial sums to the right neighbour;
+ *     block into its running fp32 dQ; the contribution is added into the block's fp32 partial
+ *     sum, which arrived with the block (the dQ work runs first, while that sum is in flight).
+ *     On `copy`: the K/V hop for the next step (issued first, overlapping this step's kernels)
+ *     and the hop of the partial sums to the right neighbour;
  *     after the last step that hop returns each block's sums to its owner. Events order the two
  *     streams so that no slot is overwritten before the step that read it has finished.
  *   cpattn_backward_finalize: once the returning sums have arrived, dq [B,T,h,d_k] and dk, dv

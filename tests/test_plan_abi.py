@@ -92,10 +92,10 @@ def test_backward_ring_calls_fail_before_launch():
     p = cp.Plan(T, h, n_kv, d, n_cp, "contiguous")
     fake = ctypes.c_void_p(1 << 20)
     wsb = p.backward_ring_workspace_size(1)
-    # K/V stage slots (2 x bf16 K, V), circulating dK/dV sums (2 x fp32), one step's contribution
-    # (fp32), the running fp32 dQ, on top of the fused backward's workspace
+    # K/V stage slots (2 x bf16 K, V), circulating dK/dV sums (2 x fp32) that each step's
+    # contribution is added into, the running fp32 dQ, on top of the fused backward's workspace
     kv = T * n_kv * d
-    extra = 2 * 2 * 2 * kv + 2 * 2 * 4 * kv + 2 * 4 * kv + 4 * T * h * d
+    extra = 2 * 2 * 2 * kv + 2 * 2 * 4 * kv + 4 * T * h * d
     assert p.backward_workspace_size(1) + extra <= wsb < p.backward_workspace_size(1) + extra + 16 * 1024
     assert L.cpattn_backward_ring_step(p.handle, 1, 0, 0.0, fake, wsb, None, None) == 1       # begin first
     assert "cpattn_backward_begin" in L.cpattn_last_error().decode()
