@@ -38,9 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
 # scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
 # to be re-read once two KV heads in flight fill L2.
-MEASURED_TRAFFIC = {"d07995b6184ddaf0": {"llama70b_zigzag_T128k": (4 * (673276416 + 491100416),
-                                                        "one-launch ncu capture at T=32768 (673,276,416 B read + "
-                                                        "491,100,416 B written) scaled by the work units (x4); a lower "
+MEASURED_TRAFFIC = {"b2a4120e4af4f338": {"llama70b_zigzag_T128k": (4 * (673353728 + 490607616),
+                                                        "one-launch ncu capture at T=32768 (673,353,728 B read + "
+                                                        "490,607,616 B written) scaled by the work units (x4); a lower "
                                                         "bound at 128K")}}
 
 
@@ -597,7 +597,7 @@ def ring_timeline(step_fn, n_cp, stream, copy, next_step_bound):
     step's work and on the copy stream after that step's hops. A hop is hidden when it ends
     before the compute it must precede does: the same step's (next_step_bound = False: the
     forward's K/V hop for step s + 1 runs beside step s) or the next step's (True: the
-    backward's gradient hop of step s is added at step s + 1)."""
+    backward's gradient hop of step s is added into at step s + 1)."""
     import torch
     t0 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -813,9 +813,11 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     ms = a.elapsed_time(b) / 2
     tf = 2.5 * flops_eff(w) / (ms * 1e-3) / 1e12
     out["backward_ring_step_path"] = {"ms": ms, "tflops_eff": tf, "frac_of_bf16_sustained": tf / peak,
-                                      "includes": "placement and prep, n_cp steps of the dK/dV and dQ kernels with "
-                                                  "the K/V and gradient hops and the gradient adds, finalize"}
-    # event timeline: does each step's gradient hop end before the next step's kernels and add?
+                                      "includes": "placement and prep, n_cp steps of the dQ and dK/dV kernels (the "
+                                                  "contributions reduced into the circulating sums) with the K/V and "
+                                                  "gradient hops, finalize"}
+    # event timeline: does each step's gradient hop end before the next step's work is done? (Its
+    # dK/dV kernel waits for that hop; the dQ kernel before it overlaps the hop.)
     cp.backward_begin(q, k, v, o, lse, dout, plan, wsr, stream=stream)
     out["backward_ring_step_path"]["timeline"] = ring_timeline(
         lambda s: cp.backward_ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream, copy, True)
