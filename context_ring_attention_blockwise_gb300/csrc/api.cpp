@@ -70,48 +70,19 @@ cpattn_status_t check_ws(const Plan& p, int B, const void* ws, size_t ws_bytes, 
 template <class T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
-// The plan's unit orders as the source of an asynchronous upload: a page-locked copy made on
-// first use (order, then order_q, then order_kv), or the plan's own vectors when page-locked
-// memory cannot be had (the upload is then still correct, only possibly host-synchronous).
-const int32_t* order_src(Plan& p, int which) {
-    static std::mutex mu;   // calls on one plan from several threads create the copy once
-    std::lock_guard<std::mutex> lock(mu);
-    const size_t n0 = p.order.size(), n1 = p.order_q.size(), n2 = p.order_kv.size();
-    if (!p.pinned_orders) {
-        void* h = nullptr;
-        if (cudaHostAlloc(&h, sizeof(int32_t) * (n0 + n1 + n2), cudaHostAllocDefault) == cudaSuccess) {
-            int32_t* d = static_cast<int32_t*>(h);
-            std::copy(p.order.begin(), p.order.end(), d);
-            std::copy(p.order_q.begin(), p.order_q.end(), d + n0);
-            std::copy(p.order_kv.begin(), p.order_kv.end(), d + n0 + n1);
-            p.pinned_orders = d;
-        } else {
-            cudaGetLastError();   // not sticky; clear it so later checks do not see it
-        }
-    }
-    if (p.pinned_orders) return p.pinned_orders + (which == 0 ? 0 : which == 1 ? n0 : n0 + n1);
-    return which == 0 ? p.order.data() : which == 1 ? p.order_q.data() : p.order_kv.data();
-}
-
-// Reset the header, upload the tile order, place tokens and position ids.
-// upload_by_param: the order table goes to the device inside kernel parameters, so nothing is
-// allocated (no page-locked copy is made) and nothing is staged from pageable memory.
+// Reset the header, upload the tile order, place tokens and position ids. The order table goes
+// to the device inside kernel parameters: nothing is allocated, nothing is staged from host
+// memory, and no copy engine is involved (a host-to-device copy here would queue behind whatever
+// large upload the caller has in flight on the same engine, delaying the whole forward).
 cpattn_status_t prologue(Plan& p, int B, const void* q, const void* k, const void* v, const int32_t* pos, void* ws,
-                         cudaStream_t st, const int32_t* lo = nullptr, bool upload_by_param = false,
-                         bool v_f16 = true) {
+                         cudaStream_t st, const int32_t* lo = nullptr, bool v_f16 = true) {
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
     int e = cudaMemsetAsync(at<char>(ws, w.header), 0, sizeof(uint32_t) * cpattn::kHeaderWords, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(header)");
     e = cudaMemsetAsync(at<char>(ws, w.counts), 0, w.sched + sizeof(uint32_t) * (1 + (size_t)p.n_cp) - w.counts, st);
     if (e) return cuda_fail(e, "cudaMemsetAsync(counts)");
-    if (upload_by_param) {
-        e = cpattn::launch_upload_i32(at<int32_t>(ws, w.order), p.order.data(), (int64_t)p.order.size(), st);
-        if (e) return cuda_fail(e, "order upload kernel");
-    } else {
-        e = cudaMemcpyAsync(at<char>(ws, w.order), order_src(p, 0), sizeof(int32_t) * p.order.size(),
-                            cudaMemcpyHostToDevice, st);
-        if (e) return cuda_fail(e, "cudaMemcpyAsync(order)");
-    }
+    e = cpattn::launch_upload_i32(at<int32_t>(ws, w.order), p.order.data(), (int64_t)p.order.size(), st);
+    if (e) return cuda_fail(e, "order upload kernel");
     cpattn::PermuteArgs a{};
     a.B = B; a.T = p.T; a.n = p.n; a.m = p.m; a.h = p.h; a.n_kv = p.n_kv; a.d = p.d; a.n_cp = p.n_cp;
     a.layout = p.layout; a.n_qt = p.n_qt;
@@ -211,7 +182,6 @@ cpattn_status_t cpattn_plan_destroy(cpattn_plan_t plan) {
     }
     if (p->bev_ready) cudaEventDestroy(p->bev_ready);
     if (p->bev_start) cudaEventDestroy(p->bev_start);
-    if (p->pinned_orders) cudaFreeHost(p->pinned_orders);
     delete p;
     return CPATTN_OK;
 }
@@ -288,15 +258,14 @@ cpattn_status_t cpattn_backward_counts(cpattn_plan_t plan, int B, int64_t* bytes
 cpattn_status_t cpattn_forward(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                const int32_t* pos, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
                                cpattn_stream_t stream) {
-    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, ws_bytes, stream, false);
+    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, ws_bytes, stream);
 }
 
 }  // extern "C"
 
 cpattn_status_t cpattn::forward_with_workspace(cpattn_plan_t plan, int B, const void* q, const void* k,
                                                const void* v, const int32_t* pos, float scale, void* o, float* lse,
-                                               void* ws, size_t ws_bytes, cpattn_stream_t stream,
-                                               bool upload_by_param) {
+                                               void* ws, size_t ws_bytes, cpattn_stream_t stream) {
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     cpattn_status_t s = check_inputs(*p, B, q, k, v, pos);
@@ -304,7 +273,7 @@ cpattn_status_t cpattn::forward_with_workspace(cpattn_plan_t plan, int B, const 
     if (!o || !lse || !aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_INVALID, "o and lse must be non-NULL and 16-byte aligned");
     if ((s = check_ws(*p, B, ws, ws_bytes, false))) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if ((s = prologue(*p, B, q, k, v, pos, ws, st, nullptr, upload_by_param))) return s;
+    if ((s = prologue(*p, B, q, k, v, pos, ws, st, nullptr))) return s;
     cpattn::AttnLaunch a = attn_args(*p, B, scale, ws);
     a.fused = 1; a.step = 0; a.kv_by_holder = 0;
     a.o = o; a.lse = lse;
@@ -352,7 +321,7 @@ cpattn_status_t backward_prepare(Plan& p, int B, const void* q, const void* k, c
         return fail(CPATTN_ERR_WORKSPACE, "workspace too small: need " + std::to_string(need) + " bytes, got " +
                                               std::to_string(ws_bytes));
     cpattn::WsLayout w = cpattn::ws_layout(p, B);
-    if ((s = prologue(p, B, q, k, v, pos, ws, st, lo, false, false))) return s;   // the backward reads bf16 V
+    if ((s = prologue(p, B, q, k, v, pos, ws, st, lo, false))) return s;   // the backward reads bf16 V
     cpattn::BwdPrepArgs pa{};
     pa.B = B; pa.T = p.T; pa.n = p.n; pa.m = p.m; pa.h = p.h; pa.d = p.d; pa.n_cp = p.n_cp;
     pa.layout = p.layout; pa.n_qt = p.n_qt;
@@ -369,11 +338,9 @@ cpattn_status_t backward_prepare(Plan& p, int B, const void* q, const void* k, c
     e = cpattn::launch_bwd_prep(pa, st);
     if (e) return cuda_fail(e, "backward prep kernel");
     const size_t nu = (size_t)p.n_cp * p.n_qt;
-    e = cudaMemcpyAsync(at<char>(ws, w.bwd_order), order_src(p, 1), sizeof(int32_t) * nu, cudaMemcpyHostToDevice, st);
-    if (!e)
-        e = cudaMemcpyAsync(at<char>(ws, w.bwd_order) + sizeof(int32_t) * nu, order_src(p, 2), sizeof(int32_t) * nu,
-                            cudaMemcpyHostToDevice, st);
-    if (e) return cuda_fail(e, "cudaMemcpyAsync(backward order)");
+    e = cpattn::launch_upload_i32(at<int32_t>(ws, w.bwd_order), p.order_q.data(), (int64_t)nu, st);
+    if (!e) e = cpattn::launch_upload_i32(at<int32_t>(ws, w.bwd_order) + nu, p.order_kv.data(), (int64_t)nu, st);
+    if (e) return cuda_fail(e, "backward order upload kernel");
     return CPATTN_OK;
 }
 

@@ -94,9 +94,6 @@ struct Plan {
     // multi-process ring (cpattn_dist_*): the step expected next and what cpattn_dist_begin placed
     int dist_next = -1, dist_B = 0, dist_rank0 = 0, dist_R = 0, dist_lo = 0;
     int bring_B = 0;                // batch size cpattn_backward_begin placed
-    // page-locked copy of order, order_q, order_kv (created on first use): an upload from
-    // pageable memory may block the calling thread until the stream drains
-    int32_t* pinned_orders = nullptr;
     // Ulysses plans (cpattn_ulysses_plan): the attention above is the per-rank problem (T tokens,
     // h / u_ncp query heads, its KV heads, one rank); these are the outer shape. 0 otherwise.
     int u_ncp = 0, u_h = 0, u_nkv = 0;
@@ -197,11 +194,11 @@ int launch_wait_selftest(uint32_t* header, uint64_t timeout_ns, void* stream);
 // Copy n int32 values from host memory to dst by kernel parameters (no host staging buffer).
 int launch_upload_i32(int32_t* dst, const int32_t* host, int64_t n, void* stream);
 
-// cpattn_forward's body. upload_by_param: the unit order reaches the device inside kernel
-// parameters instead of through a page-locked copy (the allocation-free entry point).
+// cpattn_forward's body, on a given workspace (the caller's, or the allocation-free entry
+// point's static scratch).
 cpattn_status_t forward_with_workspace(cpattn_plan_t plan, int B, const void* q, const void* k, const void* v,
                                        const int32_t* pos, float scale, void* o, float* lse, void* ws,
-                                       size_t ws_bytes, cpattn_stream_t stream, bool upload_by_param);
+                                       size_t ws_bytes, cpattn_stream_t stream);
 
 // Ulysses all-to-alls: natural q [B][T][h][d], k/v [B][T][n_kv][d] to per-rank head shards
 // qs [B n_cp][T][hp][d], ks/vs [B n_cp][T][nkvp][d] (batch b n_cp + r'), and the output os

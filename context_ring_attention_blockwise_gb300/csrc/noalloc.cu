@@ -89,9 +89,9 @@ extern "C" cpattn_status_t cpattn_forward_noalloc(cpattn_plan_t plan, int B, con
     }
     void* ws = nullptr;
     if ((s = scratch_on_current_device("cpattn_forward_noalloc", &ws))) return s;
-    // The unit order reaches the scratch inside kernel parameters: no page-locked host copy is made.
-    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, kNoAllocScratchBytes, stream,
-                                          true);
+    // The unit order reaches the scratch inside kernel parameters (as for every forward): no
+    // host copy is made.
+    return cpattn::forward_with_workspace(plan, B, q, k, v, pos, scale, o, lse, ws, kNoAllocScratchBytes, stream);
 }
 
 extern "C" cpattn_status_t cpattn_check_noalloc(cpattn_plan_t plan) {
