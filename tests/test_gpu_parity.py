@@ -78,6 +78,32 @@ def test_ring_step_path_matches_oracle_and_fused(layout, causal):
     assert np.max(np.abs(orr - of)) <= 2 * 2 ** -8 * max(1.0, float(np.max(np.abs(of))))
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_ring_step_running_maximum_jumps(causal):
+    """The ring-step merge keeps each row's output unnormalised against a running maximum and adds
+    a step's output by reductions while the step's maximum stays within 2^8 of it; a larger jump
+    takes the rescale path (the running row read back and scaled down). Rank 3's keys are scaled
+    by 8, so every query meeting that block after its own step sees its scores jump by far more
+    than 8 (log2 units): contiguous ranks 0..2 meet it at steps 1..3, after their own blocks. (For
+    the causal case the positions are reversed, so that block holds the earliest positions and
+    every query sees it.) Both paths against the oracle and against the fused forward."""
+    T, h, n_kv, d, n_cp = 1024, 4, 2, 128, 4
+    q, k, v = inputs(57, 1, T, h, n_kv, d)
+    k8 = synth.normal_bf16(57, synth.TAG_K, (1, T, n_kv, d), mult=8.0)
+    n = T // n_cp
+    k[:, 3 * n:] = k8[:, 3 * n:]
+    if causal:   # make the late block visible to earlier ranks: reverse the positions
+        pos = np.arange(T)[::-1].astype(np.int32).copy()
+    else:
+        pos = None
+    ref_o, ref_lse = oracle.get().attention(q, k, v, causal=causal, pos=pos)
+    of, lf, _, _ = run(q, k, v, n_cp, 0, causal, pos=pos, path="fused")
+    orr, lr, _, _ = run(q, k, v, n_cp, 0, causal, pos=pos, path="ring")
+    compare(orr, lr, ref_o, ref_lse, what="ring-step path, running maximum jumps")
+    compare(of, lf, ref_o, ref_lse, what="fused path, large keys")
+    assert np.max(np.abs(orr - of)) <= 2 * 2 ** -8 * max(1.0, float(np.max(np.abs(of))))
+
+
 def test_ring_step_calls_one_by_one():
     """permute, then each ring step as its own C-ABI call on a compute and a copy stream, then
     finalize: the result equals the oracle for every rank's rows."""
