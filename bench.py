@@ -685,28 +685,48 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
     mb = op.numel() * 4 + lp.numel() * 4 + mo.numel() * 2 + ml.numel() * 4
     out[f"merge_S{S}_{ws16.name}"] = {"ms": ms, "gbs": mb / ms / 1e6, "frac_of_hbm": mb / ms / 1e6 / hbm}
     del op, lp, mo, ml
-    # the ring-faithful path: permute, n_cp steps with block hops on a copy stream, finalize
+    # the ring-faithful path: permute, n_cp steps, finalize. By default each step's kernel moves
+    # the blocks for the next step itself (its idle warps copy while the attention runs), so the
+    # hop ends with the step; the same path with the hops on a copy stream follows.
     wsr = cp.alloc_workspace(plan.ring_workspace_size(w.B), dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
-    cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy)
-    torch.cuda.synchronize()
-    a.record(stream)
-    for _ in range(2):
-        cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy)
-    b.record(stream)
-    torch.cuda.synchronize()
-    cp.check(plan, wsr)
-    ms = a.elapsed_time(b) / 2
-    out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12}
-    # one more pass with an event timeline: does each K/V hop end before the step beside it?
+
+    def ring_pass_ms(copy_stream, passes=2):
+        cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy_stream)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(passes):
+            cp.ring_forward(q, k, v, plan, ws=wsr, out=o, lse=lse, stream=stream, copy_stream=copy_stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        cp.check(plan, wsr)
+        return a.elapsed_time(b) / passes
+
+    ms = ring_pass_ms(None)
     o2, lse2 = torch.empty_like(q), torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
     cp.permute(q, k, v, plan, wsr, stream=stream)
-    out["ring_step_path"]["timeline"] = ring_timeline(
-        lambda s: cp.ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream, copy, False)
+    tl = ring_timeline(lambda s: cp.ring_step(plan, w.B, s, wsr, compute=stream, copy=None), plan.n_cp, stream,
+                       stream, False)
     cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
     torch.cuda.synchronize()
     cp.check(plan, wsr)
+    # the hop is part of each step's kernel, so it cannot end after its step: no separate copy
+    # to time (the step times above include it)
+    tl.update({"hops_hidden": True, "min_slack_ms": None, "exposed_ms_total": 0.0,
+               "hop": "in the step's kernel: its two idle warps per CTA copy every rank's block into the next slot"})
+    out["ring_step_path"] = {"ms_per_step": ms, "tflops_eff": flops_eff(w) / (ms * 1e-3) / 1e12, "timeline": tl}
+    # the hops on a copy stream instead, with an event timeline: does each K/V hop end before the
+    # step beside it?
+    ms_c = ring_pass_ms(copy)
+    cp.permute(q, k, v, plan, wsr, stream=stream)
+    tl_c = ring_timeline(lambda s: cp.ring_step(plan, w.B, s, wsr, compute=stream, copy=copy), plan.n_cp, stream, copy,
+                         False)
+    cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
+    torch.cuda.synchronize()
+    cp.check(plan, wsr)
+    out["ring_step_path"]["copy_stream"] = {"ms_per_step": ms_c, "tflops_eff": flops_eff(w) / (ms_c * 1e-3) / 1e12,
+                                            "timeline": tl_c}
     # the same with SMs left free during the attention launches, so that the device-to-device hop
     # of the next block can run beside the step instead of in its tail
     for reserve in (4, 8):
@@ -724,7 +744,7 @@ def extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks):
         cp.finalize(plan, w.B, wsr, o2, lse2, stream=stream)
         torch.cuda.synchronize()
         cp.check(plan, wsr)
-        out["ring_step_path"][f"reserved_sms_{reserve}"] = {"ms_per_step": ms_r,
+        out["ring_step_path"]["copy_stream"][f"reserved_sms_{reserve}"] = {"ms_per_step": ms_r,
                                                              "tflops_eff": flops_eff(w) / (ms_r * 1e-3) / 1e12,
                                                              "timeline": tl}
     plan.set_reserved_sms(0)

@@ -464,8 +464,11 @@ def attend(plan: Plan, B: int, ws, out, lse, scale: float | None = None, stream=
 
 
 def ring_step(plan: Plan, B: int, step: int, ws, scale: float | None = None, compute=None, copy=None):
+    """One ring step. copy: a stream for the hop to the next step, or None: the step's own kernel
+    moves the blocks (one pass uses one kind of hop throughout)."""
     _check(lib().cpattn_ring_step(plan.handle, B, step, float(scale or 0.0), _dev_ptr(ws, "ws"), ws.numel(),
-                                  _stream_ptr(compute), _stream_ptr(copy)), "cpattn_ring_step")
+                                  _stream_ptr(compute), None if copy is None else _stream_ptr(copy)),
+           "cpattn_ring_step")
 
 
 def finalize(plan: Plan, B: int, ws, out, lse, stream=None):
@@ -475,7 +478,8 @@ def finalize(plan: Plan, B: int, ws, out, lse, stream=None):
 
 def ring_forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=None, out=None, lse=None,
                  stream=None, copy_stream=None):
-    """The ring-faithful path: permute, n_cp ring steps (block hops on a copy stream), finalize."""
+    """The ring-faithful path: permute, n_cp ring steps, finalize. Each step's hop to the next
+    runs inside the step's kernel, or on copy_stream when one is given."""
     torch = _torch()
     B = _check_inputs(plan, q, k, v)
     if ws is None:
@@ -485,10 +489,9 @@ def ring_forward(q, k, v, plan: Plan, pos=None, scale: float | None = None, ws=N
     if lse is None:
         lse = torch.empty((B, plan.h, plan.T), dtype=torch.float32, device=q.device)
     compute = stream if stream is not None else torch.cuda.current_stream()
-    copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=q.device, priority=-1)
     permute(q, k, v, plan, ws, pos=pos, stream=compute)
     for s in range(plan.n_cp):
-        ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy)
+        ring_step(plan, B, s, ws, scale=scale, compute=compute, copy=copy_stream)
     finalize(plan, B, ws, out, lse, stream=compute)
     return out, lse
 

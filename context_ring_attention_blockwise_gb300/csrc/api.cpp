@@ -483,8 +483,16 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
     if (!p->ev_start && (e = cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming))) return cuda_fail(e, "cudaEventCreate");
     cpattn::WsLayout w = cpattn::ws_layout(*p, B);
     const int slot = step & 1, nxt = (step + 1) & 1;
+    const bool hop_in_kernel = xst == nullptr;   // no copy stream: the step's kernel moves the blocks
+    if (step == 0) p->ring_hop_kernel = hop_in_kernel ? 1 : 0;
+    else if (p->ring_hop_kernel != (hop_in_kernel ? 1 : 0))
+        return fail(CPATTN_ERR_INVALID, "a ring pass keeps one kind of hop: a copy stream at every step, or none");
+    const size_t blk = 2 * (size_t)B * p->n * p->n_kv * p->d;    // one rank's block, bytes
+    const size_t all = blk * p->n_cp;
 
-    if (step == 0) {   // the copy stream must see the permuted blocks
+    if (hop_in_kernel) {
+        // everything runs on the compute stream, in order: nothing to wait for
+    } else if (step == 0) {   // the copy stream must see the permuted blocks
         if ((e = cudaEventRecord(p->ev_start, cst))) return cuda_fail(e, "cudaEventRecord");
         if ((e = cudaStreamWaitEvent(xst, p->ev_start, 0))) return cuda_fail(e, "cudaStreamWaitEvent");
     } else if ((e = cudaStreamWaitEvent(cst, p->ev_copy[slot], 0))) {
@@ -497,16 +505,24 @@ cpattn_status_t cpattn_ring_step(cpattn_plan_t plan, int B, int step, float scal
     a.kv_by_holder = 1;
     a.o_run = at<float>(ws, w.o_run); a.lse_run = at<float>(ws, w.lse_run);
     a.l_run = a.lse_run + (size_t)B * p->T * p->h;
+    if (hop_in_kernel && step + 1 < p->n_cp) {
+        // Send right, receive left, inside this step's kernel: slot nxt of rank r <- the block
+        // rank r-1 holds now (its idle warps copy while the attention runs).
+        a.hop_src_k = step == 0 ? at<char>(ws, w.kL) : at<char>(ws, w.stageK[slot]);
+        a.hop_src_v = step == 0 ? at<char>(ws, w.vL) : at<char>(ws, w.stageV[slot]);
+        a.hop_dst_k = at<char>(ws, w.stageK[nxt]);
+        a.hop_dst_v = at<char>(ws, w.stageV[nxt]);
+        a.hop_words = (int64_t)(all / 16);
+        a.hop_blk = (int64_t)(blk / 16);
+    }
     std::string why;
     if ((e = launch_attn(a, cst, &why))) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
-    if ((e = cudaEventRecord(p->ev_step[slot], cst))) return cuda_fail(e, "cudaEventRecord");
+    if (!hop_in_kernel && (e = cudaEventRecord(p->ev_step[slot], cst))) return cuda_fail(e, "cudaEventRecord");
 
-    if (step + 1 < p->n_cp) {
+    if (!hop_in_kernel && step + 1 < p->n_cp) {
         // Send right, receive left: slot nxt of rank r <- the block rank r-1 holds now. Blocks
         // are rank-major, so the hop is two contiguous copies per tensor.
         if (step >= 1 && (e = cudaStreamWaitEvent(xst, p->ev_step[nxt], 0))) return cuda_fail(e, "cudaStreamWaitEvent");
-        const size_t blk = 2 * (size_t)B * p->n * p->n_kv * p->d;    // one rank's block, bytes
-        const size_t all = blk * p->n_cp;
         for (int t = 0; t < 2; ++t) {
             const char* src = (step == 0) ? at<char>(ws, t ? w.vL : w.kL) : at<char>(ws, t ? w.stageV[slot] : w.stageK[slot]);
             char* dst = at<char>(ws, t ? w.stageV[nxt] : w.stageK[nxt]);

@@ -103,6 +103,13 @@ struct Params {
     uint64_t timeout_ns;
     int first;              // ring step: write the running state instead of merging into it
     int64_t kv_rank_rows;   // all-gather: K/V rows between consecutive ranks' gathered copies (else 0)
+    // ring step with the hop in this kernel: each rank's key/value block moves into the next
+    // rank's slot (rank-major blocks of hop_blk 16-byte words; hop_words per tensor, 0: no hop)
+    const uint4* hop_src_k;
+    const uint4* hop_src_v;
+    uint4* hop_dst_k;
+    uint4* hop_dst_v;
+    int64_t hop_words, hop_blk;
 };
 
 template <int D>
@@ -608,6 +615,42 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
 }
 
 // ---------------------------------------------------------------------------------------------
+// warps 2..3 of a ring step (otherwise idle): the hop to the next step ("Pass them around a ring":
+// send right, receive left). Word w of a tensor's rank-major blocks moves to w + hop_blk, the
+// last rank's block wrapping to rank 0. The CTAs split the two tensors' words evenly; the 64
+// threads of a CTA take consecutive words (coalesced), four loads in flight per thread. The
+// source is read-only in this launch and the destination slot is read only by the next step.
+// ---------------------------------------------------------------------------------------------
+__device__ void ring_hop_copy(const Params& P, int t) {
+    const int64_t total = 2 * P.hop_words;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t beg = (int64_t)blockIdx.x * per;
+    const int64_t end = beg + per < total ? beg + per : total;
+    const uint64_t pol = l2_evict_first();       // the next step reads the slot long after this one
+    for (int64_t w0 = beg + t; w0 < end; w0 += 4 * 64) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w = w0 + u * 64;
+            if (w < end) {
+                const bool isv = w >= P.hop_words;
+                v[u] = __ldg((isv ? P.hop_src_v : P.hop_src_k) + (isv ? w - P.hop_words : w));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w = w0 + u * 64;
+            if (w < end) {
+                const bool isv = w >= P.hop_words;
+                int64_t o = (isv ? w - P.hop_words : w) + P.hop_blk;
+                if (o >= P.hop_words) o -= P.hop_words;
+                st_global_v4_hint((isv ? P.hop_dst_v : P.hop_dst_k) + o, v[u], pol);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // warps 4..11: softmax and epilogue, warpgroup i for query tile i, one thread per row
 // ---------------------------------------------------------------------------------------------
 template <int D, int M>
@@ -917,6 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_dec<RegSplit<M>::low>();
         if (warp == 0 && lane == 0) producer<D, M>(P, &tmQ, &tmK, &tmV, sQ, sK, sV, unit_slot, bars, wait);
         if (warp == 1 && lane == 0) mma_issuer<D>(P, tmem, sQ, sK, sV, unit_slot, bars, wait);
+        if (warp >= 2 && P.hop_words > 0) ring_hop_copy(P, (int)threadIdx.x - 64);
     } else {
         setmaxnreg_inc<RegSplit<M>::high>();
         softmax_epilogue<D, M>(P, tmem, unit_slot, bars, wait);
@@ -1089,6 +1133,9 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.ktile_mm = reinterpret_cast<const int4*>(a.ktile_mm ? a.ktile_mm : a.tile_mm);
     P.first = a.first >= 0 ? a.first : (a.step == 0);
     P.kv_rank_rows = a.kv_rank_rows;
+    P.hop_src_k = static_cast<const uint4*>(a.hop_src_k); P.hop_src_v = static_cast<const uint4*>(a.hop_src_v);
+    P.hop_dst_k = static_cast<uint4*>(a.hop_dst_k); P.hop_dst_v = static_cast<uint4*>(a.hop_dst_v);
+    P.hop_words = a.hop_words; P.hop_blk = a.hop_blk;
     P.unit_tiles = a.unit_tiles;
     P.walk_tab = a.walk_tab;
     P.walk_nz = a.walk_nz;

@@ -82,6 +82,7 @@ struct Plan {
     CUevent_st* ev_copy[2] = {nullptr, nullptr};
     CUevent_st* ev_start = nullptr;
     int next_step = -1;             // step expected next on the ring path (-1: permute first)
+    int ring_hop_kernel = 0;        // this pass's hops run in the step kernels (no copy stream)
     int ring_B = 0;                 // batch size cpattn_permute placed (the steps must use the same)
     // backward ring-step path state: K/V of a step arrived, a stage slot's kernels done, the
     // circulating partial ready to send (after the step's add), a partial arrived
@@ -172,6 +173,11 @@ struct AttnLaunch {
     const int32_t* kposL = nullptr; const int32_t* ktile_mm = nullptr;
     int first = -1;            // ring step: write (1) or merge into (0) the running state; -1: step == 0
     int64_t kv_rank_rows = 0;  // all-gather: K/V rows between the gathered copies of consecutive ranks
+    // ring step: the hop to the next step done by the kernel's idle warps (hop_words 16-byte words
+    // per tensor, 0: none); word w of hop_src_* goes to (w + hop_blk) mod hop_words of hop_dst_*
+    const void* hop_src_k = nullptr; const void* hop_src_v = nullptr;
+    void* hop_dst_k = nullptr; void* hop_dst_v = nullptr;
+    int64_t hop_words = 0, hop_blk = 0;
     uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
     int doc_ids = 0;           // loL / tile_lo hold document ids (else a per-query lower bound)
     int reserved_sms = 0;      // SMs the persistent grid leaves free for concurrent work

@@ -151,11 +151,14 @@ cpattn_status_t cpattn_permute(cpattn_plan_t plan, int B, const void* q, const v
  * every virtual rank at once. Rank r attends to the key/value block it holds, that of rank
  * (r - step) mod n_cp, read from the stage slot step % 2 (step 0: its own block in place), and
  * merges the partial (O_s with its maximum and sum) into the fp32 running state in the workspace
- * (the online-softmax merge; cpattn_finalize normalises). On `copy` it
- * enqueues the hop to the next step: every rank's slot (step+1) % 2 receives the block its left
- * neighbour holds now (send right, receive left), ordered against the compute stream with
- * events so that a slot is overwritten only after the step that read it has finished. Steps
- * must be issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan, with
+ * (the online-softmax merge; cpattn_finalize normalises). It also performs the hop to the next
+ * step: every rank's slot (step+1) % 2 receives the block its left neighbour holds now (send
+ * right, receive left). With `copy` NULL the step's own kernel does it: its otherwise idle warps
+ * copy the blocks while the attention runs, so the hop ends with the step and everything stays
+ * on `compute`. With a `copy` stream the hop is enqueued there as device-to-device copies,
+ * ordered against the compute stream with events so that a slot is overwritten only after the
+ * step that read it has finished. One pass uses one kind of hop at every step. Steps must be
+ * issued in order 0..n_cp-1 after cpattn_permute, from one host thread per plan, with
  * cpattn_permute and cpattn_finalize on the stream passed here as `compute` (step 0 orders the
  * copy stream after the compute stream only), and with the B cpattn_permute placed; otherwise
  * CPATTN_ERR_INVALID before any launch. */

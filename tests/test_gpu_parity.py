@@ -104,6 +104,48 @@ def test_ring_step_running_maximum_jumps(causal):
     assert np.max(np.abs(orr - of)) <= 2 * 2 ** -8 * max(1.0, float(np.max(np.abs(of))))
 
 
+@pytest.mark.parametrize("case", [(1024, 4, 2, 128, 4, 1, True), (1560, 2, 2, 128, 4, 2, True),
+                                  (768, 4, 1, 64, 3, 0, False)], ids=["zigzag", "striped-ragged", "contiguous-full"])
+def test_ring_step_hop_in_kernel_equals_copy_stream(case):
+    """The hop done by the step kernels' idle warps delivers the same blocks as the copy-stream
+    hop: the two passes are bit-identical, and both match the oracle."""
+    T, h, n_kv, d, n_cp, layout, causal = case
+    q, k, v = inputs(61 + T, 1, T, h, n_kv, d)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, layout, causal)
+    qd, kd, vd = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    ws = cp.alloc_workspace(plan.ring_workspace_size(1))
+    ok, lk = cp.ring_forward(qd, kd, vd, plan, ws=ws)                       # hops in the kernels
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    oc, lc = cp.ring_forward(qd, kd, vd, plan, ws=ws, copy_stream=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    cp.check(plan, ws)
+    assert torch.equal(ok.view(torch.int16), oc.view(torch.int16)) and torch.equal(lk, lc)
+    ref_o, ref_lse = oracle.get().attention(q, k, v, causal=causal)
+    compare(ok.float().cpu().numpy(), lk.cpu().numpy(), ref_o, ref_lse, what=f"in-kernel hops {case}")
+
+
+def test_ring_pass_keeps_one_kind_of_hop():
+    """A pass that starts with in-kernel hops refuses a copy stream at a later step (and the
+    reverse), before any launch; a new permute starts a new pass."""
+    T, h, n_kv, d, n_cp = 512, 2, 1, 64, 4
+    q, k, v = inputs(63, 1, T, h, n_kv, d)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, 1, True)
+    qd, kd, vd = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    ws = cp.alloc_workspace(plan.ring_workspace_size(1))
+    copy = torch.cuda.Stream()
+    for first, second in ((None, copy), (copy, None)):
+        cp.permute(qd, kd, vd, plan, ws)
+        cp.ring_step(plan, 1, 0, ws, copy=first)
+        with pytest.raises(cp.CpattnError, match="one kind of hop"):
+            cp.ring_step(plan, 1, 1, ws, copy=second)
+        torch.cuda.synchronize()    # the refused pass's step 0 (and any hop it queued) is done
+    o, lse = cp.ring_forward(qd, kd, vd, plan, ws=ws)
+    torch.cuda.synchronize()
+    ref_o, ref_lse = oracle.get().attention(q, k, v, causal=True)
+    compare(o.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_lse, what="after refused passes")
+
+
 def test_ring_step_calls_one_by_one():
     """permute, then each ring step as its own C-ABI call on a compute and a copy stream, then
     finalize: the result equals the oracle for every rank's rows."""
