@@ -126,6 +126,12 @@ struct Cfg {
     static constexpr int NBAR = 15 + 4 * NS;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
+    // Ring steps only (launched with SMEM_BYTES_RING; the other launches keep that shared memory as
+    // L1): each softmax warp's 32 rows x 128 bytes, through which the epilogue's stores and
+    // reductions into the running output move whole row segments.
+    static constexpr int STG_WARP_BYTES = 32 * 128;
+    static constexpr int OFF_STG = (OFF_MISC + 32 + 127) & ~127;
+    static constexpr int SMEM_BYTES_RING = OFF_STG + 8 * STG_WARP_BYTES + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL0 = 0, S_COL1 = 128, O_COL0 = 256, O_COL1 = 256 + D;
 };
@@ -655,7 +661,7 @@ __device__ void ring_hop_copy(const Params& P, int t) {
 // ---------------------------------------------------------------------------------------------
 template <int D, int M>
 __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* unit_slot, const Bars<D>& bars,
-                                 const Waiter& wait) {
+                                 const Waiter& wait, uint32_t stg) {
     using C = Cfg<D>;
     const int wg = (threadIdx.x >> 5) >= 8 ? 1 : 0;
     const int quarter = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
@@ -866,6 +872,12 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                 }
             }
         }
+        // ring step: the warp's 32 rows (consecutive in layout order; row r is lane r's) and which
+        // of them are added or written through the staging buffer
+        const int64_t run_row0 = (((int64_t)U.r * P.B + U.b) * P.h + head) * P.n;
+        const int64_t wrow0 = (int64_t)qt * 128 + quarter * 32;
+        const unsigned add_rows = __ballot_sync(0xffffffffu, mode == kAdd);
+        const unsigned write_rows = __ballot_sync(0xffffffffu, mode == kWrite);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t ot[32];
@@ -885,25 +897,41 @@ __device__ void softmax_epilogue(const Params& P, uint32_t tmem, volatile int* u
                     v.w = pack_bf16(__uint_as_float(ot[8 * q4 + 6]) * inv_l, __uint_as_float(ot[8 * q4 + 7]) * inv_l);
                     st_global_v4_hint(dst + c * 4 + q4, v, pol_o);
                 }
-            } else if (mode == kWrite) {
+            } else if (!P.fused) {
+                // Ring step. A row taking the rescale path merges by itself (read back, rare).
+                // The written and added rows go through the warp's staging buffer (16-byte pieces
+                // XOR-swizzled by row): the stores and reductions then move whole 128-byte row
+                // segments, 8 lanes per row and 4 rows per instruction, instead of 16 bytes of
+                // each of 32 rows per instruction.
+                if (mode == kRescale) {
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    reinterpret_cast<uint4*>(orow)[c * 8 + q4] =
-                        make_uint4(ot[4 * q4], ot[4 * q4 + 1], ot[4 * q4 + 2], ot[4 * q4 + 3]);
-            } else if (mode == kAdd) {
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    red_add_v4_f32(orow + c * 32 + q4 * 4, __uint_as_float(ot[4 * q4]) * f,
-                                   __uint_as_float(ot[4 * q4 + 1]) * f, __uint_as_float(ot[4 * q4 + 2]) * f,
-                                   __uint_as_float(ot[4 * q4 + 3]) * f);
-            } else if (mode == kRescale) {
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    float4* a = reinterpret_cast<float4*>(orow) + c * 8 + q4;
-                    const float4 oa = *a;
-                    *a = make_float4(oa.x * f + __uint_as_float(ot[4 * q4]), oa.y * f + __uint_as_float(ot[4 * q4 + 1]),
-                                     oa.z * f + __uint_as_float(ot[4 * q4 + 2]), oa.w * f + __uint_as_float(ot[4 * q4 + 3]));
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        float4* a = reinterpret_cast<float4*>(orow) + c * 8 + q4;
+                        const float4 oa = *a;
+                        *a = make_float4(oa.x * f + __uint_as_float(ot[4 * q4]), oa.y * f + __uint_as_float(ot[4 * q4 + 1]),
+                                         oa.z * f + __uint_as_float(ot[4 * q4 + 2]),
+                                         oa.w * f + __uint_as_float(ot[4 * q4 + 3]));
+                    }
                 }
+                const float mul = mode == kAdd ? f : 1.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(stg + (lane * 8 + (q ^ (lane & 7))) * 16, __float_as_uint(__uint_as_float(ot[4 * q]) * mul),
+                                 __float_as_uint(__uint_as_float(ot[4 * q + 1]) * mul),
+                                 __float_as_uint(__uint_as_float(ot[4 * q + 2]) * mul),
+                                 __float_as_uint(__uint_as_float(ot[4 * q + 3]) * mul));
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = i * 4 + (lane >> 3), q = lane & 7;
+                    const int4 t = ld_shared_v4(stg + (r * 8 + (q ^ (r & 7))) * 16);
+                    float* dst = P.o_run + (run_row0 + wrow0 + r) * D + c * 32 + q * 4;
+                    if ((add_rows >> r) & 1u)
+                        red_add_v4_f32(dst, __int_as_float(t.x), __int_as_float(t.y), __int_as_float(t.z), __int_as_float(t.w));
+                    else if ((write_rows >> r) & 1u)
+                        *reinterpret_cast<int4*>(dst) = t;
+                }
+                __syncwarp();
             }
         }
         if (j > 0) {
@@ -963,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp >= 2 && P.hop_words > 0) ring_hop_copy(P, (int)threadIdx.x - 64);
     } else {
         setmaxnreg_inc<RegSplit<M>::high>();
-        softmax_epilogue<D, M>(P, tmem, unit_slot, bars, wait);
+        softmax_epilogue<D, M>(P, tmem, unit_slot, bars, wait, sbase + C::OFF_STG + (warp - 4) * C::STG_WARP_BYTES);
     }
     tc_fence_before();
     __syncthreads();
@@ -1099,7 +1127,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     cudaGetDevice(&dev);
     const int ea = attr_once.run(dev, [&]() -> int {
         cudaError_t e = cudaFuncSetAttribute(ring_attention_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
+                                             C::SMEM_BYTES_RING);
         if (e != cudaSuccess) return (int)e;
         // setmaxnreg.inc waits until enough registers are free in the block's allocation: the
         // split must fit in what the block is launched with, or the kernel would never proceed.
@@ -1160,7 +1188,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
         order_by_tiles_kernel<<<1, 1024, 0, st>>>(P.unit_tiles, a.order_scratch, n_rg);
         P.order = a.order_scratch;
     }
-    ring_attention_kernel<D, M><<<grid, kThreads, C::SMEM_BYTES, st>>>(tq, tk, tv, P);
+    ring_attention_kernel<D, M><<<grid, kThreads, a.fused ? C::SMEM_BYTES : C::SMEM_BYTES_RING, st>>>(tq, tk, tv, P);
     return (int)cudaGetLastError();
 }
 
