@@ -146,6 +146,8 @@ struct BCfg {
     static constexpr int SMEM_BYTES = OFF_RING + 16 * kRing + 1024;
     static_assert(OFF_S % 1024 == 0 && OFF_SIDE % 16 == 0 && OFF_BAR % 8 == 0 && OFF_RING % 16 == 0,
                   "shared-memory regions must keep their alignment");
+    // a ring step's epilogue reuses the fixed pair as 4 KB of staging for each elementwise warp
+    static_assert(OFF_F0 == 0 && OFF_F1 == TILE && 8 * 4096 <= 2 * TILE, "ring-step staging in the fixed pair");
     // tensor memory: two accumulators (A0, A1: dV and dK, or dQ), the score tile S and the dP
     // tile (128 columns each). The elementwise warps overwrite the first half of each warpgroup's
     // 64 columns of S with packed bf16 P and of dP with packed bf16 dS, the A operands of the
@@ -642,14 +644,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 0 starts the partial sums), or added into the partial sums that arrived with the
             // blocks by fire-and-forget reductions (one per element and step, ordered by the
             // launches: deterministic); an empty walk adds nothing.
-            const int64_t krow = (((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + jk;
-            float4* fk = reinterpret_cast<float4*>(P.dk_f32 + krow * D);
-            float4* fv = reinterpret_cast<float4*>(P.dv_f32 + krow * D);
+            // The rows go through this warp's 4 KB of the fixed-pair region (free once the last
+            // MMA has drained), as in the dQ kernel: whole 128-byte row segments per reduction.
+            const int64_t jk0 = (int64_t)kt * 128 + quarter * 32;      // the warp's first key row
+            const int64_t krow0 = (((int64_t)kvr * P.B + b) * P.n_kv + kvh) * P.n + jk0;
+            const uint32_t stg = sb + C::OFF_F0 + (uint32_t)(warp - 4) * 4096u;
+            // An empty walk waited for no MMA, so nothing yet says the fixed pair's load has
+            // landed: wait for it before its region is reused.
+            bool staged = n_steps > 0 || !P.dkdv_add;
+            if (staged && n_steps == 0) staged = __all_sync(0xffffffffu, wait(bars.fixed_full(), 0, kBSiteFixed));
 #pragma unroll
-            for (int which = 0; which < 2 && (n_steps > 0 || !P.dkdv_add); ++which) {
+            for (int which = 0; which < 2 && staged; ++which) {
                 const uint32_t col0 = (which ? C::COL_A1 : C::COL_A0) + (uint32_t)(wg * (D / 2));
                 const float mul = which ? P.scale : 1.0f;
-                float4* f = which ? fk : fv;
+                float* g = which ? P.dk_f32 : P.dv_f32;
 #pragma unroll
                 for (int c = 0; c < D / 64; ++c) {
                     uint32_t t[32];
@@ -660,14 +668,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int q = 0; q < 32; ++q) t[q] = 0u;
                     }
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 x = make_float4(__uint_as_float(t[4 * q4]) * mul, __uint_as_float(t[4 * q4 + 1]) * mul,
-                                                     __uint_as_float(t[4 * q4 + 2]) * mul, __uint_as_float(t[4 * q4 + 3]) * mul);
-                        if (!key_valid) continue;
-                        float4* y = f + (wg * (D / 2) + c * 32) / 4 + q4;
-                        if (P.dkdv_add) red_add_v4_f32(reinterpret_cast<float*>(y), x.x, x.y, x.z, x.w);
-                        else *y = x;
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(stg + (lane * 8 + (q ^ (lane & 7))) * 16, __float_as_uint(__uint_as_float(t[4 * q]) * mul),
+                                     __float_as_uint(__uint_as_float(t[4 * q + 1]) * mul),
+                                     __float_as_uint(__uint_as_float(t[4 * q + 2]) * mul),
+                                     __float_as_uint(__uint_as_float(t[4 * q + 3]) * mul));
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = i * 4 + (lane >> 3), q = lane & 7;
+                        const int4 x = ld_shared_v4(stg + (rr * 8 + (q ^ (rr & 7))) * 16);
+                        if (jk0 + rr < P.n) {
+                            float* dst = g + (krow0 + rr) * D + wg * (D / 2) + c * 32 + q * 4;
+                            if (P.dkdv_add)
+                                red_add_v4_f32(dst, __int_as_float(x.x), __int_as_float(x.y), __int_as_float(x.z), __int_as_float(x.w));
+                            else *reinterpret_cast<int4*>(dst) = x;
+                        }
                     }
+                    __syncwarp();
                 }
             }
         } else if (ok) {
@@ -1030,7 +1048,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // writes). The additions are fire-and-forget reductions, one per element and step (the
             // steps are ordered by their launches, so the sum is deterministic): no read of the
             // running rows to wait on. A later step with nothing visible adds nothing.
-            float4* f = reinterpret_cast<float4*>(P.dq_run + ((((int64_t)r * P.B + b) * P.h + head) * P.n + jq) * D);
+            // The rows go through this warp's 4 KB of the fixed-pair region (free once the last
+            // MMA has drained), 16-byte pieces XOR-swizzled by row, so that each reduction moves a
+            // whole 128-byte row segment: 8 lanes per row, 4 rows per instruction.
+            const int64_t jq0 = (int64_t)qt * 128 + quarter * 32;      // the warp's first query row
+            const int64_t qrow0 = (((int64_t)r * P.B + b) * P.h + head) * P.n + jq0;
+            const uint32_t stg = sb + C::OFF_F0 + (uint32_t)(warp - 4) * 4096u;
 #pragma unroll
             for (int c = 0; c < D / 64 && (n_steps > 0 || P.step == 0); ++c) {
                 uint32_t t[32];
@@ -1040,16 +1063,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) t[q] = 0u;
                 }
-                if (q_valid) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const int idx = (wg * (D / 2) + c * 32) / 4 + q4;
-                        float4 x = make_float4(__uint_as_float(t[4 * q4]) * P.scale, __uint_as_float(t[4 * q4 + 1]) * P.scale,
-                                               __uint_as_float(t[4 * q4 + 2]) * P.scale, __uint_as_float(t[4 * q4 + 3]) * P.scale);
-                        if (P.step > 0) red_add_v4_f32(reinterpret_cast<float*>(f + idx), x.x, x.y, x.z, x.w);
-                        else f[idx] = x;
+                for (int q = 0; q < 8; ++q)
+                    st_shared_v4(stg + (lane * 8 + (q ^ (lane & 7))) * 16,
+                                 __float_as_uint(__uint_as_float(t[4 * q]) * P.scale),
+                                 __float_as_uint(__uint_as_float(t[4 * q + 1]) * P.scale),
+                                 __float_as_uint(__uint_as_float(t[4 * q + 2]) * P.scale),
+                                 __float_as_uint(__uint_as_float(t[4 * q + 3]) * P.scale));
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = i * 4 + (lane >> 3), q = lane & 7;
+                    const int4 x = ld_shared_v4(stg + (rr * 8 + (q ^ (rr & 7))) * 16);
+                    if (jq0 + rr < P.n) {
+                        float* dst = P.dq_run + (qrow0 + rr) * D + wg * (D / 2) + c * 32 + q * 4;
+                        if (P.step > 0) red_add_v4_f32(dst, __int_as_float(x.x), __int_as_float(x.y), __int_as_float(x.z), __int_as_float(x.w));
+                        else *reinterpret_cast<int4*>(dst) = x;
                     }
                 }
+                __syncwarp();
             }
         } else if (ok) {
             const int64_t tn = q_valid ? natural_token(P.layout, r, jq, P.n, P.m, P.n_cp) : 0;
