@@ -32,7 +32,7 @@ SYMBOLS = [
     "cpattn_backward_ring_step", "cpattn_backward_finalize",
     "cpattn_allgather_workspace_size", "cpattn_allgather_counts", "cpattn_allgather_forward",
     "cpattn_allgather_gather", "cpattn_allgather_attend", "cpattn_forward_docs", "cpattn_allgather_forward_docs",
-    "cpattn_dist_sizes", "cpattn_dist_begin", "cpattn_dist_step", "cpattn_dist_shift", "cpattn_dist_finalize",
+    "cpattn_dist_sizes", "cpattn_dist_begin", "cpattn_dist_step", "cpattn_dist_shift", "cpattn_dist_step_shift", "cpattn_dist_finalize",
     "cpattn_plan_set_reserved_sms",
 ]
 
@@ -102,6 +102,8 @@ def lib():
     L.cpattn_dist_begin.argtypes = [_P, i, i, i, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_step.argtypes = [_P, i, i, i, i, ctypes.c_float, _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]
     L.cpattn_dist_shift.argtypes = [_P, i, i, _P, _P, ctypes.c_size_t, i, _P]
+    L.cpattn_dist_step_shift.argtypes = [_P, i, i, i, i, ctypes.c_float, _P, _P, i, ctypes.c_size_t, _P,
+                                         ctypes.c_size_t, _P]
     L.cpattn_dist_finalize.argtypes = [_P, i, i, i, _P, _P, _P, ctypes.c_size_t, _P]
     L.cpattn_plan_set_reserved_sms.argtypes = [_P, i]
     L.cpattn_last_error.restype = ctypes.c_char_p
@@ -562,6 +564,15 @@ def dist_begin(plan: Plan, B: int, rank0: int, R: int, q, k, v, ws, slot, pos=No
 def dist_step(plan: Plan, B: int, rank0: int, R: int, step: int, slot, ws, scale: float | None = None, stream=None):
     _check(lib().cpattn_dist_step(plan.handle, B, rank0, R, step, float(scale or 0.0), _dev_ptr(slot, "slot"),
                                   slot.numel(), _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_dist_step")
+
+
+def dist_step_shift(plan: Plan, B: int, rank0: int, R: int, step: int, slot, next_slot, wrap: bool, ws,
+                    scale: float | None = None, stream=None):
+    """cpattn_dist_step_shift: the step on slot, and the shift from slot into next_slot done by the
+    step's kernel (K, V) and copies after it (position tables), all on one stream."""
+    _check(lib().cpattn_dist_step_shift(plan.handle, B, rank0, R, step, float(scale or 0.0), _dev_ptr(slot, "slot"),
+                                        _dev_ptr(next_slot, "next_slot"), int(bool(wrap)), slot.numel(),
+                                        _dev_ptr(ws, "ws"), ws.numel(), _stream_ptr(stream)), "cpattn_dist_step_shift")
 
 
 def dist_shift(plan: Plan, B: int, R: int, src_slot, dst_slot, wrap: bool, stream=None):

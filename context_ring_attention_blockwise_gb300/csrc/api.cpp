@@ -1047,14 +1047,41 @@ cpattn_status_t cpattn_dist_begin(cpattn_plan_t plan, int B, int rank0, int R, c
     return CPATTN_OK;
 }
 
-cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
-                                 const void* slot, size_t slot_bytes, void* ws, size_t ws_bytes,
-                                 cpattn_stream_t stream) {
+namespace {
+// Local rank i + 1's block of regions x_begin..x_end - 1 in dst <- local rank i's in src (i < R - 1),
+// and with wrap local rank 0's <- local rank R - 1's: device-to-device copies on st.
+int shift_regions(const cpattn::DistLayout& w, const void* src_slot, void* dst_slot, int R, int wrap, cudaStream_t st,
+                  int x_begin, int x_end) {
+    const size_t off[4] = {w.slot_k, w.slot_v, w.slot_pos, w.slot_tile};
+    const size_t blk[4] = {w.blk_k, w.blk_v, w.blk_pos, w.blk_tile};
+    const char* src = static_cast<const char*>(src_slot);
+    char* dst = static_cast<char*>(dst_slot);
+    for (int x = x_begin; x < x_end; ++x) {
+        int e = 0;
+        // local rank i + 1 receives the block local rank i holds now
+        if (R > 1) e = cudaMemcpyAsync(dst + off[x] + blk[x], src + off[x], blk[x] * (R - 1), cudaMemcpyDeviceToDevice, st);
+        // a process holding the whole ring passes its last block to its own first rank
+        if (!e && wrap)
+            e = cudaMemcpyAsync(dst + off[x], src + off[x] + blk[x] * (R - 1), blk[x], cudaMemcpyDeviceToDevice, st);
+        if (e) return e;
+    }
+    return 0;
+}
+
+// cpattn_dist_step, and with next_slot the shift into it: K and V by the step kernel's idle warps,
+// the position tables by copies on the same stream after it.
+cpattn_status_t dist_step_impl(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale, const void* slot,
+                               void* next_slot, int wrap, size_t slot_bytes, void* ws, size_t ws_bytes,
+                               cpattn_stream_t stream) {
     Plan* p = as_plan(plan);
     if (!p) return fail(CPATTN_ERR_INVALID, "plan is NULL");
     if (!ws || !slot) return fail(CPATTN_ERR_WORKSPACE, "workspace and slot must be non-NULL");
     cpattn_status_t s = check_dist(*p, B, rank0, R, ws, ws_bytes, slot, slot_bytes);
     if (s) return s;
+    if (next_slot) {
+        if (next_slot == slot) return fail(CPATTN_ERR_INVALID, "the two slots must differ");
+        if ((s = check_dist(*p, B, 0, R, nullptr, 0, next_slot, slot_bytes))) return s;
+    }
     if ((s = check_dist_state(*p, B, rank0, R))) return s;
     if (step != p->dist_next)
         return fail(CPATTN_ERR_INVALID, "ring steps must follow cpattn_dist_begin in order 0..n_cp-1 (expected step " +
@@ -1086,11 +1113,36 @@ cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, in
     a.header = at<uint32_t>(ws, w.header);
     a.timeout_ns = 2000000000ull;
     a.reserved_sms = p->reserved_sms;
+    if (next_slot) {
+        a.hop_src_k = static_cast<const char*>(slot) + w.slot_k;
+        a.hop_src_v = static_cast<const char*>(slot) + w.slot_v;
+        a.hop_dst_k = static_cast<char*>(next_slot) + w.slot_k;
+        a.hop_dst_v = static_cast<char*>(next_slot) + w.slot_v;
+        a.hop_words = (int64_t)(w.blk_k * R / 16);
+        a.hop_blk = (int64_t)(w.blk_k / 16);
+        a.hop_wrap = wrap ? 1 : 0;
+    }
     std::string why;
-    int e = launch_attn(a, reinterpret_cast<cudaStream_t>(stream), &why);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int e = launch_attn(a, st, &why);
     if (e) return why.empty() ? cuda_fail(e, "attention kernel") : fail(CPATTN_ERR_CUDA, why);
+    if (next_slot && (e = shift_regions(w, slot, next_slot, R, wrap, st, 2, 4))) return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
     p->dist_next = step + 1;
     return CPATTN_OK;
+}
+}  // namespace
+
+cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
+                                 const void* slot, size_t slot_bytes, void* ws, size_t ws_bytes,
+                                 cpattn_stream_t stream) {
+    return dist_step_impl(plan, B, rank0, R, step, scale, slot, nullptr, 0, slot_bytes, ws, ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_dist_step_shift(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
+                                       const void* slot, void* next_slot, int wrap, size_t slot_bytes, void* ws,
+                                       size_t ws_bytes, cpattn_stream_t stream) {
+    if (!next_slot) return fail(CPATTN_ERR_INVALID, "next_slot must be non-NULL");
+    return dist_step_impl(plan, B, rank0, R, step, scale, slot, next_slot, wrap, slot_bytes, ws, ws_bytes, stream);
 }
 
 cpattn_status_t cpattn_dist_shift(cpattn_plan_t plan, int B, int R, const void* src_slot, void* dst_slot,
@@ -1103,20 +1155,8 @@ cpattn_status_t cpattn_dist_shift(cpattn_plan_t plan, int B, int R, const void* 
     if (s) return s;
     if ((s = check_dist(*p, B, 0, R, nullptr, 0, src_slot, slot_bytes))) return s;
     const cpattn::DistLayout w = cpattn::dist_layout(*p, B, R);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t off[4] = {w.slot_k, w.slot_v, w.slot_pos, w.slot_tile};
-    const size_t blk[4] = {w.blk_k, w.blk_v, w.blk_pos, w.blk_tile};
-    const char* src = static_cast<const char*>(src_slot);
-    char* dst = static_cast<char*>(dst_slot);
-    for (int x = 0; x < 4; ++x) {
-        int e = 0;
-        // local rank i + 1 receives the block local rank i holds now
-        if (R > 1) e = cudaMemcpyAsync(dst + off[x] + blk[x], src + off[x], blk[x] * (R - 1), cudaMemcpyDeviceToDevice, st);
-        // a process holding the whole ring passes its last block to its own first rank
-        if (!e && wrap)
-            e = cudaMemcpyAsync(dst + off[x], src + off[x] + blk[x] * (R - 1), blk[x], cudaMemcpyDeviceToDevice, st);
-        if (e) return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
-    }
+    const int e = shift_regions(w, src_slot, dst_slot, R, wrap, reinterpret_cast<cudaStream_t>(stream), 0, 4);
+    if (e) return cuda_fail(e, "cudaMemcpyAsync(ring hop)");
     return CPATTN_OK;
 }
 

@@ -110,6 +110,7 @@ struct Params {
     uint4* hop_dst_k;
     uint4* hop_dst_v;
     int64_t hop_words, hop_blk;
+    int hop_wrap;           // the last rank's block wraps to rank 0 (else rank 0's is left alone)
 };
 
 template <int D>
@@ -623,7 +624,8 @@ __device__ void mma_issuer(const Params& P, uint32_t tmem, uint32_t sQ, uint32_t
 // ---------------------------------------------------------------------------------------------
 // warps 2..3 of a ring step (otherwise idle): the hop to the next step ("Pass them around a ring":
 // send right, receive left). Word w of a tensor's rank-major blocks moves to w + hop_blk, the
-// last rank's block wrapping to rank 0. The CTAs split the two tensors' words evenly; the 64
+// last rank's block wrapping to rank 0 (or, in a process holding only part of the ring, left
+// for the transport that brings the previous process's block). The CTAs split the two tensors' words evenly; the 64
 // threads of a CTA take consecutive words (coalesced), four loads in flight per thread. The
 // source is read-only in this launch and the destination slot is read only by the next step.
 // ---------------------------------------------------------------------------------------------
@@ -649,8 +651,9 @@ __device__ void ring_hop_copy(const Params& P, int t) {
             if (w < end) {
                 const bool isv = w >= P.hop_words;
                 int64_t o = (isv ? w - P.hop_words : w) + P.hop_blk;
-                if (o >= P.hop_words) o -= P.hop_words;
-                st_global_v4_hint((isv ? P.hop_dst_v : P.hop_dst_k) + o, v[u], pol);
+                const bool wraps = o >= P.hop_words;
+                if (wraps) o -= P.hop_words;
+                if (!wraps || P.hop_wrap) st_global_v4_hint((isv ? P.hop_dst_v : P.hop_dst_k) + o, v[u], pol);
             }
         }
     }
@@ -1163,7 +1166,7 @@ int launch_d(const AttnLaunch& a, cudaStream_t st, std::string* why) {
     P.kv_rank_rows = a.kv_rank_rows;
     P.hop_src_k = static_cast<const uint4*>(a.hop_src_k); P.hop_src_v = static_cast<const uint4*>(a.hop_src_v);
     P.hop_dst_k = static_cast<uint4*>(a.hop_dst_k); P.hop_dst_v = static_cast<uint4*>(a.hop_dst_v);
-    P.hop_words = a.hop_words; P.hop_blk = a.hop_blk;
+    P.hop_words = a.hop_words; P.hop_blk = a.hop_blk; P.hop_wrap = a.hop_wrap;
     P.unit_tiles = a.unit_tiles;
     P.walk_tab = a.walk_tab;
     P.walk_nz = a.walk_nz;

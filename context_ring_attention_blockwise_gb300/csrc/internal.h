@@ -178,6 +178,7 @@ struct AttnLaunch {
     const void* hop_src_k = nullptr; const void* hop_src_v = nullptr;
     void* hop_dst_k = nullptr; void* hop_dst_v = nullptr;
     int64_t hop_words = 0, hop_blk = 0;
+    int hop_wrap = 1;          // the last rank's block goes to rank 0 (0: rank 0's is left alone)
     uint64_t kv_rows = 0;      // rows the K/V tensor maps span (0: n_cp B n_kv n)
     int doc_ids = 0;           // loL / tile_lo hold document ids (else a per-query lower bound)
     int reserved_sms = 0;      // SMs the persistent grid leaves free for concurrent work

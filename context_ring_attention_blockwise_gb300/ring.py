@@ -132,6 +132,11 @@ class LibraryBackend:
         from . import dist_shift
         dist_shift(self.plan, self.B, self.R, src, dst, wrap, stream=stream)
 
+    def step_shift(self, s, slot, next_slot, wrap, scale, stream):
+        from . import dist_step_shift
+        dist_step_shift(self.plan, self.B, self.rank0, self.R, s, slot, next_slot, wrap, self.ws, scale=scale,
+                        stream=stream)
+
     def finalize(self, out, lse, stream):
         from . import dist_finalize
         dist_finalize(self.plan, self.B, self.rank0, self.R, self.ws, out, lse, stream=stream)
@@ -157,19 +162,26 @@ class RingProcess:
         self.counters = HopCounters(kv=[0] * self.R, tables=[0] * self.R)
 
     def forward(self, q, k, v, pos=None, scale=None, out=None, lse=None, stream=None, copy_stream=None,
-                timeline=None, lo=None):
+                timeline=None, lo=None, shift_in_kernel=True):
         """timeline: a list to which each step appends (end of its compute, end of the hop that
-        runs beside it) as timing events on the two streams (device backend only). Without a
-        copy_stream the hops go to a new high-priority stream: the next step waits on them, so they
-        should not queue behind other copies the caller runs. lo: the tokens' per-query lower
-        bounds (document masks of packed sequences), in the order of q."""
+        runs beside it) as timing events on the two streams (device backend only). With
+        shift_in_kernel (and a backend that has it) each step's kernel also moves the blocks
+        between this process's own ranks, so only the block that crosses to the next process
+        uses the copy stream; otherwise the whole shift runs there too. Without a copy_stream the
+        hops go to a new high-priority stream: the next step waits on them, so they should not
+        queue behind other copies the caller runs. lo: the tokens' per-query lower bounds
+        (document masks of packed sequences), in the order of q."""
         import torch
         be, R, n_cp = self.backend, self.R, self.plan.n_cp
         B, h, n = self.B, self.plan.h, self.plan.T // n_cp
         on_gpu = getattr(be, "device", None) is not None and be.device.type == "cuda"
+        in_kernel = bool(shift_in_kernel) and hasattr(be, "step_shift")
         if on_gpu:
             compute = stream if stream is not None else torch.cuda.current_stream(be.device)
-            copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=be.device, priority=-1)
+            if in_kernel and self.world == 1 and copy_stream is None:
+                copy = compute          # nothing runs beside the steps: the kernels move every block
+            else:
+                copy = copy_stream if copy_stream is not None else torch.cuda.Stream(device=be.device, priority=-1)
         else:
             compute = copy = None
         if out is None:
@@ -190,14 +202,18 @@ class RingProcess:
             cur, nxt = slots[s % 2], slots[(s + 1) % 2]
             if s > 0:
                 be.wait(compute, arrived)
-            be.step(s, cur, scale, compute)
+            if in_kernel and s + 1 < n_cp:
+                be.step_shift(s, cur, nxt, self.world == 1, scale, compute)
+            else:
+                be.step(s, cur, scale, compute)
             self.counters.steps.append((s, s % 2))
             used[s % 2] = be.event(compute)
             if s + 1 < n_cp:
                 # slot nxt was read by step s - 1; slot cur was filled by the hop before this step
                 # (or, at step 0, by the placement on the compute stream)
                 be.wait(copy, placed if s == 0 else used[(s + 1) % 2])
-                be.shift(cur, nxt, self.world == 1, copy)
+                if not in_kernel:
+                    be.shift(cur, nxt, self.world == 1, copy)
                 if self.world > 1:
                     send = [be.region(cur, x, R - 1) for x in range(4)]
                     recv = [be.region(nxt, x, 0) for x in range(4)]

@@ -354,6 +354,12 @@ cpattn_status_t cpattn_allgather_attend(cpattn_plan_t plan, int B, float scale, 
  *     in src_slot, for i < R - 1, all four regions; with wrap != 0 (a process that holds the whole
  *     ring) also local rank 0's block <- local rank R - 1's. Otherwise local rank 0's block in
  *     dst_slot is the caller's to fill with the block the previous process sends.
+ *   cpattn_dist_step_shift: cpattn_dist_step on `slot` and cpattn_dist_shift from `slot` into
+ *     next_slot (a different slot) on the same stream, in one call: the K and V blocks move inside
+ *     the step's kernel, by warps that have no part in the attention, while it runs; the position
+ *     tables follow by copies on `stream`. next_slot must not be read by anyone until the call's
+ *     work on `stream` has finished; it must not be written either, except local rank 0's block
+ *     when wrap is 0 (the transport's).
  *   cpattn_dist_finalize: after the last step, o [B][R n][h][d_k] bf16 and lse [B][h][R n] fp32 in
  *     the process's token order (that of q).
  * Out-of-order steps, or a B, rank0 or R other than cpattn_dist_begin's, return CPATTN_ERR_INVALID
@@ -368,6 +374,9 @@ cpattn_status_t cpattn_dist_step(cpattn_plan_t plan, int B, int rank0, int R, in
                                  cpattn_stream_t stream);
 cpattn_status_t cpattn_dist_shift(cpattn_plan_t plan, int B, int R, const void* src_slot, void* dst_slot,
                                   size_t slot_bytes, int wrap, cpattn_stream_t stream);
+cpattn_status_t cpattn_dist_step_shift(cpattn_plan_t plan, int B, int rank0, int R, int step, float scale,
+                                       const void* slot, void* next_slot, int wrap, size_t slot_bytes, void* ws,
+                                       size_t ws_bytes, cpattn_stream_t stream);
 cpattn_status_t cpattn_dist_finalize(cpattn_plan_t plan, int B, int rank0, int R, void* o, float* lse, void* ws,
                                      size_t ws_bytes, cpattn_stream_t stream);
 

@@ -85,6 +85,24 @@ def test_one_process_ring_matches_oracle_and_ring_step_path(case):
     assert ring.counters.kv == [oracle.get().kv_bytes_recv(B, n, n_kv, d, n_cp)] * n_cp
 
 
+def test_one_process_ring_shift_in_kernel_or_on_copy_stream():
+    """The shift between a process's own ranks done by the step kernels gives the same blocks as
+    the shift by copies on a copy stream: bit-identical outputs."""
+    B, T, h, n_kv, d, n_cp = 1, 1560, 2, 2, 128, 4
+    q, k, v = inputs(95, B, T, h, n_kv, d)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, "zigzag", True)
+    toks = local_tokens(plan.T, plan.n_cp, plan.layout, 0, n_cp)
+    outs = []
+    for in_kernel in (True, False):
+        ring = RingProcess(plan, B, rank=0, world=1, device="cuda")
+        o, lse = ring.forward(to_device_bf16(_shard(q, toks)), to_device_bf16(_shard(k, toks)),
+                              to_device_bf16(_shard(v, toks)), shift_in_kernel=in_kernel)
+        torch.cuda.synchronize()
+        cp.check(plan, ring.backend.ws)
+        outs.append((o.view(torch.int16).clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_one_process_ring_with_position_ids():
     B, T, h, n_kv, d, n_cp = 1, 1024, 2, 1, 128, 4
     q, k, v = inputs(91, B, T, h, n_kv, d)
