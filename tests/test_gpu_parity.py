@@ -104,16 +104,17 @@ def test_ring_step_running_maximum_jumps(causal):
     assert np.max(np.abs(orr - of)) <= 2 * 2 ** -8 * max(1.0, float(np.max(np.abs(of))))
 
 
-@pytest.mark.parametrize("case", [(1024, 4, 2, 128, 4, 1, True), (1560, 2, 2, 128, 4, 2, True),
-                                  (768, 4, 1, 64, 3, 0, False)], ids=["zigzag", "striped-ragged", "contiguous-full"])
+@pytest.mark.parametrize("case", [(1024, 4, 2, 128, 4, 1, True, 1), (1560, 2, 2, 128, 4, 2, True, 1),
+                                  (768, 4, 1, 64, 3, 0, False, 1), (1024, 2, 2, 64, 4, 1, True, 2)],
+                         ids=["zigzag", "striped-ragged", "contiguous-full", "zigzag-B2"])
 def test_ring_step_hop_in_kernel_equals_copy_stream(case):
     """The hop done by the step kernels' idle warps delivers the same blocks as the copy-stream
     hop: the two passes are bit-identical, and both match the oracle."""
-    T, h, n_kv, d, n_cp, layout, causal = case
-    q, k, v = inputs(61 + T, 1, T, h, n_kv, d)
+    T, h, n_kv, d, n_cp, layout, causal, B = case
+    q, k, v = inputs(61 + T, B, T, h, n_kv, d)
     plan = cp.Plan(T, h, n_kv, d, n_cp, layout, causal)
     qd, kd, vd = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
-    ws = cp.alloc_workspace(plan.ring_workspace_size(1))
+    ws = cp.alloc_workspace(plan.ring_workspace_size(B))
     ok, lk = cp.ring_forward(qd, kd, vd, plan, ws=ws)                       # hops in the kernels
     torch.cuda.synchronize()
     cp.check(plan, ws)
