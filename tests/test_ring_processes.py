@@ -87,9 +87,23 @@ class TaggedBlocks:
         lse.zero_()
 
 
-def _run_ring(plan, rank, world, transport):
+class TaggedBlocksStepShift(TaggedBlocks):
+    """The same stand-in with cpattn_dist_step_shift: the step, then the shift from its slot into
+    the next, both regions and tables, leaving local rank 0's block alone unless wrap (the
+    transport fills it)."""
+
+    def step_shift(self, s, slot, next_slot, wrap, scale, stream):
+        assert next_slot is not slot
+        self.step(s, slot, scale, stream)
+        if not wrap:   # the transport's block must come from the transport, not from this shift
+            for x in range(4):
+                self.region(next_slot, x, 0).fill_(255)
+        self.shift(slot, next_slot, wrap, stream)
+
+
+def _run_ring(plan, rank, world, transport, step_shift=False):
     R = plan.n_cp // world
-    be = TaggedBlocks(plan, B, rank * R, R)
+    be = (TaggedBlocksStepShift if step_shift else TaggedBlocks)(plan, B, rank * R, R)
     ring = RingProcess(plan, B, rank=rank, world=world, transport=transport, backend=be)
     n = plan.T // plan.n_cp
     q = torch.zeros((B, R * n, H, D), dtype=torch.bfloat16)
@@ -115,12 +129,12 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _rank_main(rank, world, port, n_cp, layout):
+def _rank_main(rank, world, port, n_cp, layout, step_shift=False):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         plan = cp.Plan(T, H, NKV, D, n_cp, layout, True)
-        ring, be = _run_ring(plan, rank, world, HostTransport(rank, world))
+        ring, be = _run_ring(plan, rank, world, HostTransport(rank, world), step_shift)
         _check(plan, rank, world, ring, be)
         dist.barrier()
     finally:
@@ -138,6 +152,21 @@ def test_one_process_holds_the_whole_ring(layout):
                                                (2, 8, "striped")])
 def test_gloo_ranks_pass_blocks_around_the_ring(world, n_cp, layout):
     mp.spawn(_rank_main, args=(world, _free_port(), n_cp, layout), nprocs=world, join=True)
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "striped"])
+def test_one_process_ring_with_the_shift_in_the_step(layout):
+    """The step-and-shift protocol (cpattn_dist_step_shift) with one process holding the ring."""
+    plan = cp.Plan(T, H, NKV, D, 8, layout, True)
+    ring, be = _run_ring(plan, 0, 1, None, step_shift=True)
+    _check(plan, 0, 1, ring, be)
+
+
+@pytest.mark.parametrize("world,n_cp,layout", [(2, 4, "zigzag"), (4, 4, "striped"), (2, 8, "contiguous")])
+def test_gloo_ranks_with_the_shift_in_the_step(world, n_cp, layout):
+    """The step-and-shift protocol across gloo ranks: the shift leaves local rank 0's block to the
+    transport, which must fill it before the next step reads it."""
+    mp.spawn(_rank_main, args=(world, _free_port(), n_cp, layout, True), nprocs=world, join=True)
 
 
 def test_local_tokens_follow_the_oracle_layout():
