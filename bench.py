@@ -38,9 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
 # scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
 # to be re-read once two KV heads in flight fill L2.
-MEASURED_TRAFFIC = {"b2a4120e4af4f338": {"llama70b_zigzag_T128k": (4 * (673353728 + 490607616),
-                                                        "one-launch ncu capture at T=32768 (673,353,728 B read + "
-                                                        "490,607,616 B written) scaled by the work units (x4); a lower "
+MEASURED_TRAFFIC = {"68e344386ec180c4": {"llama70b_zigzag_T128k": (4 * (673071360 + 490299392),
+                                                        "one-launch ncu capture at T=32768 (673,071,360 B read + "
+                                                        "490,299,392 B written) scaled by the work units (x4); a lower "
                                                         "bound at 128K")}}
 
 
