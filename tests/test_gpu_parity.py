@@ -105,8 +105,9 @@ def test_ring_step_running_maximum_jumps(causal):
 
 
 @pytest.mark.parametrize("case", [(1024, 4, 2, 128, 4, 1, True, 1), (1560, 2, 2, 128, 4, 2, True, 1),
-                                  (768, 4, 1, 64, 3, 0, False, 1), (1024, 2, 2, 64, 4, 1, True, 2)],
-                         ids=["zigzag", "striped-ragged", "contiguous-full", "zigzag-B2"])
+                                  (768, 4, 1, 64, 3, 0, False, 1), (1024, 2, 2, 64, 4, 1, True, 2),
+                                  (512, 2, 1, 128, 2, 1, True, 1)],
+                         ids=["zigzag", "striped-ragged", "contiguous-full", "zigzag-B2", "two-ranks"])
 def test_ring_step_hop_in_kernel_equals_copy_stream(case):
     """The hop done by the step kernels' idle warps delivers the same blocks as the copy-stream
     hop: the two passes are bit-identical, and both match the oracle."""
@@ -124,6 +125,24 @@ def test_ring_step_hop_in_kernel_equals_copy_stream(case):
     assert torch.equal(ok.view(torch.int16), oc.view(torch.int16)) and torch.equal(lk, lc)
     ref_o, ref_lse = oracle.get().attention(q, k, v, causal=causal)
     compare(ok.float().cpu().numpy(), lk.cpu().numpy(), ref_o, ref_lse, what=f"in-kernel hops {case}")
+
+
+def test_ring_step_hop_in_kernel_with_reserved_sms():
+    """With SMs left free the step kernels have fewer CTAs, each moving a larger share of the
+    blocks: the same results, bit for bit."""
+    T, h, n_kv, d, n_cp = 2048, 4, 2, 128, 8
+    q, k, v = inputs(67, 1, T, h, n_kv, d)
+    plan = cp.Plan(T, h, n_kv, d, n_cp, 1, True)
+    qd, kd, vd = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    ws = cp.alloc_workspace(plan.ring_workspace_size(1))
+    o0, l0 = cp.ring_forward(qd, kd, vd, plan, ws=ws)
+    torch.cuda.synchronize()
+    plan.set_reserved_sms(148)              # a handful of CTAs copy every block
+    o1, l1 = cp.ring_forward(qd, kd, vd, plan, ws=ws)
+    torch.cuda.synchronize()
+    plan.set_reserved_sms(0)
+    cp.check(plan, ws)
+    assert torch.equal(o0.view(torch.int16), o1.view(torch.int16)) and torch.equal(l0, l1)
 
 
 def test_ring_pass_keeps_one_kind_of_hop():

@@ -158,7 +158,8 @@ def _rank_main(rank, world, port, case, outdir, with_docs=False):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[4]], ids=["zigzag", "striped", "ragged"])
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[4], (1, 1024, 2, 2, 128, 2, "zigzag", True)],
+                         ids=["zigzag", "striped", "ragged", "one-rank-each"])
 def test_two_processes_on_one_gpu_exchange_through_host_memory(case):
     B, T, h, n_kv, d, n_cp, layout, causal = case
     world = 2
