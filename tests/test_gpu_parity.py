@@ -45,11 +45,13 @@ def test_forward_matches_oracle(case, layout, causal):
 
 
 @pytest.mark.parametrize("layout", [0, 1, 2], ids=["contiguous", "zigzag", "striped"])
-def test_uniform_scores_give_mean_of_values(layout):
-    """Q = 0: every visible key has the same score, so O is the running mean of V (closed form)."""
+@pytest.mark.parametrize("path", ["fused", "ring"])
+def test_uniform_scores_give_mean_of_values(layout, path):
+    """Q = 0: every visible key has the same score, so O is the running mean of V (closed form);
+    on the ring-step path every step after the first adds at the running maximum's own scale."""
     T, h, d, n_cp = 512, 2, 128, 4
     q, k, v = inputs(7, 1, T, h, h, d, q_zero=True)
-    o, lse, _, _ = run(q, k, v, n_cp, layout, True)
+    o, lse, _, _ = run(q, k, v, n_cp, layout, True, path=path)
     vf = synth.bf16_bits_to_f32(v).astype(np.float64)
     mean = np.cumsum(vf, axis=1) / np.arange(1, T + 1)[None, :, None, None]
     assert np.max(np.abs(o - mean)) < 1e-2
@@ -192,15 +194,16 @@ def test_ring_step_calls_one_by_one():
 
 
 @pytest.mark.parametrize("layout", [0, 1, 2], ids=["contiguous", "zigzag", "striped"])
-def test_position_ids_drive_the_mask(layout):
+@pytest.mark.parametrize("path", ["fused", "ring"])
+def test_position_ids_drive_the_mask(layout, path):
     T, h, d, n_cp = 768, 2, 64, 4
     q, k, v = inputs(31, 1, T, h, 1, d)
     rng = np.random.default_rng(9)
     for pos in (np.arange(T)[::-1].copy(), rng.permutation(T), rng.integers(0, 50, T), np.arange(T) // 7):
         pos = pos.astype(np.int32)
         ref_o, ref_lse = oracle.get().attention(q, k, v, causal=True, pos=pos)
-        o, lse, _, _ = run(q, k, v, n_cp, layout, True, pos=pos)
-        compare(o, lse, ref_o, ref_lse, what=f"custom positions, layout {layout}")
+        o, lse, _, _ = run(q, k, v, n_cp, layout, True, pos=pos, path=path)
+        compare(o, lse, ref_o, ref_lse, what=f"custom positions, layout {layout}, {path}")
 
 
 def test_explicit_scale():
