@@ -246,6 +246,8 @@ def config_of(w, args):
     if args.path == "ring":
         par = (f"ring over {args.gpus} processes, {w.n_cp // args.gpus} ranks each" if args.gpus > 1
                else "single GPU, one process holding all ranks")
+    elif args.path == "steps":
+        par = "replicas of the ring-step path" if args.gpus > 1 else "single GPU, one launch per ring step"
     else:
         par = "replicas" if args.gpus > 1 else "single GPU"
     return {"workload": w.name, "B": w.B, "T": w.T, "h": w.h, "n_kv": w.n_kv, "d_k": w.d, "n_cp": w.n_cp,
@@ -428,7 +430,7 @@ def run_gpu(args, w):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
     q, k, v = to_dev(q_h), to_dev(k_h), to_dev(v_h)
     plan = cp.Plan(w.T, w.h, w.n_kv, w.d, w.n_cp, args.layout, w.causal)
-    ring = args.path == "ring"
+    ring = args.path == "steps"           # the ring-step path: permute, n_cp ring steps, finalize
     ws = cp.alloc_workspace(plan.ring_workspace_size(w.B) if ring else plan.workspace_size(w.B), dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.h, w.T), dtype=torch.float32, device=dev)
@@ -444,7 +446,7 @@ def run_gpu(args, w):
         if evs:
             evs[0].record(stream)
         if ring:
-            cp.ring_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream, copy_stream=copy)
+            cp.ring_forward(q, k, v, plan, ws=ws, out=o, lse=lse, stream=stream)
         else:
             cp.permute(q, k, v, plan, ws, stream=stream)
             if evs:
@@ -517,7 +519,7 @@ def run_gpu(args, w):
             if read[s] is not None:
                 stream.wait_event(read[s])
             if ring:
-                cp.ring_forward(qb, kb, vb, plan, ws=ws, out=ob, lse=lb, stream=stream, copy_stream=copy)
+                cp.ring_forward(qb, kb, vb, plan, ws=ws, out=ob, lse=lb, stream=stream)
             else:
                 cp.forward(qb, kb, vb, plan, ws=ws, out=ob, lse=lb, stream=stream)
             computed[s] = torch.cuda.Event()
@@ -928,9 +930,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.CONFIGS))
     ap.add_argument("--layout", default=None, help="contiguous|zigzag|striped (default: the workload's first)")
-    ap.add_argument("--path", choices=["fused", "ring"], default="fused",
+    ap.add_argument("--path", choices=["fused", "ring", "steps"], default="fused",
                     help="fused: one persistent launch over every rank and step; ring: the ring across "
-                         "processes (one per GPU), each holding n_cp / processes ranks")
+                         "processes (one per GPU), each holding n_cp / processes ranks; steps: the "
+                         "single-process ring-step path (one launch per step, hops inside the step kernels)")
     ap.add_argument("--traffic", type=float, default=None, help="DRAM bytes per attention launch from ncu, if known")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
