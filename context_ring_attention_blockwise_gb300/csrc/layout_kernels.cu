@@ -192,29 +192,32 @@ __global__ void __launch_bounds__(256, 4) permute_kernel(const uint4* __restrict
     }
 }
 
-// Ring-step path: the running state [n_cp][B][h][n] (O unnormalised over d columns, its maximum
-// m_run in log2 units and its sum l_run) -> O / l_run in bf16 natural order [B,T,h,d] and
-// lse = (m_run + log2 l_run) ln 2 as [B,h,T]; a row that saw no key gets 0 and -inf. One thread
-// per 4 outputs, destination order.
+// The two kernels below go from layout order [n_cp][B][H][n][d] (fp32) back to natural order
+// [B][T][H][d] (bf16). One warp per token (b, t): its rank and local index are found once, then
+// the warp walks the token's H rows, d / 4 lanes per row (one float4 each), 32 / (d / 4) rows at a
+// time. (Taking the index apart for every float4 cost more instructions than the bytes allowed:
+// the kernel ran at half the copy bandwidth.)
+
+// Ring-step path: the running state (O unnormalised over d columns, its maximum m_run in log2
+// units and its sum l_run) -> O / l_run in bf16 and lse = (m_run + log2 l_run) ln 2 as [B,h,T]; a
+// row that saw no key gets 0 and -inf.
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ o_run, const float* __restrict__ m_run,
                                                        const float* __restrict__ l_run, uint2* __restrict__ o,
                                                        float* __restrict__ lse, int B, int64_t T, int64_t n, int64_t m,
                                                        int h, int d, int n_cp, int layout) {
-    const int cpr = d / 4;
-    const int64_t no = (int64_t)B * T * h * cpr;
-    const int64_t nl = (int64_t)B * h * T;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < no + nl; i += (int64_t)gridDim.x * blockDim.x) {
-        if (i < no) {
-            const int c = (int)(i % cpr);
-            int64_t rest = i / cpr;
-            const int hd = (int)(rest % h);
-            rest /= h;
-            const int64_t t = rest % T;
-            const int b = (int)(rest / T);
-            int r;
-            int64_t j;
-            rank_of(layout, t, n, m, n_cp, r, j);
-            const int64_t row = (((int64_t)r * B + b) * h + hd) * n + j;
+    const int cpr = d / 4, per = 32 / cpr;
+    const int lane = threadIdx.x & 31, c = lane % cpr, sub = lane / cpr;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t tok = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < (int64_t)B * T;
+         tok += warps) {
+        const int b = (int)(tok / T);
+        const int64_t t = tok - (int64_t)b * T;
+        int r;
+        int64_t j;
+        rank_of(layout, t, n, m, n_cp, r, j);
+        const int64_t row0 = ((int64_t)r * B + b) * h * n + j;      // head hd's row: row0 + hd n
+        for (int hd = sub; hd < h; hd += per) {
+            const int64_t row = row0 + (int64_t)hd * n;
             const float4 x = o_run[row * cpr + c];
             const float lr = l_run[row];
             const float inv = lr > 0.f ? 1.0f / lr : 0.f;
@@ -222,45 +225,35 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
             uint2 out;
             out.x = *reinterpret_cast<uint32_t*>(&lo);
             out.y = *reinterpret_cast<uint32_t*>(&hi);
-            o[i] = out;
-        } else {
-            const int64_t e = i - no;
-            const int64_t t = e % T;
-            const int64_t bh = e / T;
-            const int b = (int)(bh / h), hd = (int)(bh % h);
-            int r;
-            int64_t j;
-            rank_of(layout, t, n, m, n_cp, r, j);
-            const int64_t row = (((int64_t)r * B + b) * h + hd) * n + j;
-            const float lr = l_run[row];
-            lse[e] = lr > 0.f ? (m_run[row] + log2f(lr)) * 0.69314718055994531f : -INFINITY;
+            o[(tok * h + hd) * cpr + c] = out;
+            if (c == 0) lse[((int64_t)b * h + hd) * T + t] = lr > 0.f ? (m_run[row] + log2f(lr)) * 0.69314718055994531f : -INFINITY;
         }
     }
 }
 
-// fp32 [n_cp][B][H][n][d] in layout order -> bf16 [B,T,H,d] in natural order (the backward
-// ring-step path's gradients). One thread per 4 outputs, destination order.
+// The backward ring-step path's gradients: fp32 -> bf16, same orders.
 __global__ void __launch_bounds__(256) unpermute_f32_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, int B,
                                                             int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
                                                             int layout) {
-    const int cpr = d / 4;
-    const int64_t no = (int64_t)B * T * H * cpr;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < no; i += (int64_t)gridDim.x * blockDim.x) {
-        const int c = (int)(i % cpr);
-        int64_t rest = i / cpr;
-        const int hd = (int)(rest % H);
-        rest /= H;
-        const int64_t t = rest % T;
-        const int b = (int)(rest / T);
+    const int cpr = d / 4, per = 32 / cpr;
+    const int lane = threadIdx.x & 31, c = lane % cpr, sub = lane / cpr;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t tok = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tok < (int64_t)B * T;
+         tok += warps) {
+        const int b = (int)(tok / T);
+        const int64_t t = tok - (int64_t)b * T;
         int r;
         int64_t j;
         rank_of(layout, t, n, m, n_cp, r, j);
-        const float4 x = src[((((int64_t)r * B + b) * H + hd) * n + j) * cpr + c];
-        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
-        uint2 out;
-        out.x = *reinterpret_cast<uint32_t*>(&lo);
-        out.y = *reinterpret_cast<uint32_t*>(&hi);
-        dst[i] = out;
+        const int64_t row0 = ((int64_t)r * B + b) * H * n + j;
+        for (int hd = sub; hd < H; hd += per) {
+            const float4 x = src[(row0 + (int64_t)hd * n) * cpr + c];
+            __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+            uint2 out;
+            out.x = *reinterpret_cast<uint32_t*>(&lo);
+            out.y = *reinterpret_cast<uint32_t*>(&hi);
+            dst[(tok * H + hd) * cpr + c] = out;
+        }
     }
 }
 
@@ -487,7 +480,7 @@ int launch_permute(const PermuteArgs& a, void* stream) {
 }
 
 int launch_finalize(const FinalizeArgs& a, void* stream) {
-    const int64_t work = (int64_t)a.B * a.T * a.h * (a.d / 4 + 1);
+    const int64_t work = (int64_t)a.B * a.T * 32;          // a warp per token
     finalize_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(a.o_run), a.lse_run, a.l_run, static_cast<uint2*>(a.o), a.lse, a.B, a.T, a.n, a.m,
         a.h, a.d, a.n_cp, a.layout);
@@ -496,7 +489,7 @@ int launch_finalize(const FinalizeArgs& a, void* stream) {
 
 int launch_unpermute_f32(const float* src, void* dst, int B, int64_t T, int64_t n, int64_t m, int H, int d, int n_cp,
                          int layout, void* stream) {
-    const int64_t work = (int64_t)B * T * H * (d / 4);
+    const int64_t work = (int64_t)B * T * 32;              // a warp per token
     unpermute_f32_kernel<<<grid_for(work, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(src), static_cast<uint2*>(dst), B, T, n, m, H, d, n_cp, layout);
     return (int)cudaGetLastError();
