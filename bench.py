@@ -585,9 +585,11 @@ def run_gpu(args, w):
             "clocks": clocks,
         }
     del qp, kp, vp, outs, bufs
-    if rank == 0 and args.extras and not ring:
+    # the secondary measurements and the CPU baseline belong to the single-GPU line: with more
+    # ranks they would hold every GPU idle behind rank 0
+    if rank == 0 and world == 1 and args.extras and not ring:
         result["extras"] = extras(cp, plan, w, q, k, v, ws, stream, copy, dev, peaks)
-    if rank == 0 and args.cpu_baseline:
+    if rank == 0 and world == 1 and args.cpu_baseline:
         rate, dt, desc = oracle_sample_rate(w, q_h, k_h, v_h, args.cpu_rows, seed=7)
         result["cpu_baseline"] = cpu_baseline_entry(w, rate, dt, desc)
     if rank == 0:
