@@ -38,17 +38,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
 # scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
 # to be re-read once two KV heads in flight fill L2.
-MEASURED_TRAFFIC = {"68e344386ec180c4": {"llama70b_zigzag_T128k": (4 * (673071360 + 490299392),
+MEASURED_TRAFFIC = {"d3d05013087c7b18": {"llama70b_zigzag_T128k": (4 * (673071360 + 490299392),
                                                         "one-launch ncu capture at T=32768 (673,071,360 B read + "
                                                         "490,299,392 B written) scaled by the work units (x4); a lower "
                                                         "bound at 128K")}}
 
 
-def attention_source_hash() -> str:
+def source_key(text: str) -> str:
+    """sha256 of C++ source with its comments and blank space taken out, so that a comment edit
+    does not orphan counters taken on the same code."""
     import hashlib
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)      # block comments
+    text = re.sub(r"//[^\n]*", " ", text)                   # line comments
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
+def attention_source_hash() -> str:
     path = os.path.join(ROOT, "context_ring_attention_blockwise_gb300", "csrc", "attention.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path, encoding="utf-8") as f:
+        return source_key(f.read())
 
 
 def measured_traffic(workload_name: str):

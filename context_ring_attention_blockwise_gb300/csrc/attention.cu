@@ -25,7 +25,8 @@
 //               O_i += P_i V with P_i read from tensor memory (TS form). It takes the number of
 //               key tiles of each unit from a table a small kernel writes before the launch, so
 //               no table lookup of the key walk sits between two of its MMA groups.
-//   warps 2, 3  idle.
+//   warps 2, 3  idle, except in a ring step with the hop in the kernel: they copy every rank's
+//               K and V block into the next rank's slot of the stage while the attention runs.
 //   warps 4..7  softmax warpgroup 0 (query tile 0), one thread per row.
 //   warps 8..11 softmax warpgroup 1 (query tile 1). Each thread reads its row of S from TMEM,
 //               masks, takes the max, exponentiates with exp2, sums, writes P (fp16) back over
@@ -35,6 +36,11 @@
 //
 // MMAs from the issuing thread execute in order. So QK_i of the next tile, which overwrites
 // S_i / P_i, is issued only after PV_i of this tile, which reads P_i.
+//
+// One ring step (instead of every step at once) merges each unit's output into a running state
+// in HBM: O unnormalised against a running maximum, with its sum (the online softmax carried
+// across launches; the finalize kernel divides). Those launches take 32 KB more shared memory,
+// through which the epilogue's stores and reductions move whole row segments.
 //
 // Rescaling is lazy: a row keeps a stale maximum until a tile raises it by more than 8 (log2
 // units). P then stays below 2^8 and the final O / l is unchanged. Every wait is bounded by a

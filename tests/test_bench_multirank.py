@@ -46,6 +46,14 @@ def test_single_rank_helpers():
     assert bench.measured_traffic("no_such_workload") == (None, None)
 
 
+def test_source_key_ignores_comments_only():
+    """The traffic bookkeeping's key: comment and spacing edits keep it, any code edit changes it."""
+    base = bench.source_key("int a = 1;  // one\n/* block\n comment */ float b;\n")
+    assert bench.source_key("int a = 1;\nfloat b;   // other words\n") == base
+    assert bench.source_key("int a = 2;\nfloat b;\n") != base
+    assert bench.source_key("int a = 1;\ndouble b;\n") != base
+
+
 def test_hop_summary_slack_and_exposure():
     """The ring-step timelines' arithmetic: a forward hop must end before its own step's compute,
     a backward gradient hop before the next step's; the last step's hop is not counted."""
