@@ -38,10 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # than the launch time, so its figure is a one-launch capture of the same kernel at T = 32768,
 # scaled by the work units to the 128K launch (4 times): a lower bound there, where K/V tiles start
 # to be re-read once two KV heads in flight fill L2.
-MEASURED_TRAFFIC = {"d3d05013087c7b18": {"llama70b_zigzag_T128k": (4 * (673071360 + 490299392),
-                                                        "one-launch ncu capture at T=32768 (673,071,360 B read + "
-                                                        "490,299,392 B written) scaled by the work units (x4); a lower "
-                                                        "bound at 128K")}}
+MEASURED_TRAFFIC = {"d3d05013087c7b18": {"llama70b_zigzag_T128k": (4593913600 + 2132709888,
+                                                        "one-launch ncu capture of the 128K launch itself, a single "
+                                                        "pass (4,593,913,600 B read + 2,132,709,888 B written); the "
+                                                        "reads exceed Q, K and V once by the K/V tiles L2 could not "
+                                                        "keep between the units that share them")}}
 
 
 def source_key(text: str) -> str:
