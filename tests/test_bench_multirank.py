@@ -80,3 +80,15 @@ def test_effective_flops_follow_the_visible_pairs(name):
     assert exact == (w.T * (w.T + 1) // 2 if w.causal else w.T * w.T)
     effective = exact - w.T / 2 if w.causal else exact
     assert bench.flops_eff(w) == 4.0 * w.B * w.h * w.d * effective
+
+
+def test_config_names_each_path():
+    """The JSON line's config says which path and parallelism a run measured."""
+    import argparse
+    w = bench.synth.workload("llama70b_zigzag_T128k")
+    def cfg(path, gpus):
+        return bench.config_of(w, argparse.Namespace(path=path, gpus=gpus, layout=1))
+    assert cfg("fused", 1)["parallelism"] == "single GPU" and cfg("fused", 8)["parallelism"] == "replicas"
+    assert cfg("steps", 1)["path"] == "steps" and "one launch per ring step" in cfg("steps", 1)["parallelism"]
+    assert cfg("ring", 2)["parallelism"].startswith("ring over 2 processes")
+    assert cfg("ring", 1)["parallelism"] == "single GPU, one process holding all ranks"
